@@ -1,0 +1,366 @@
+// api.cu -- the C ABI of libpkv: host-side argument checks, per-device context
+// (error word, workspace), tensor-map encoding, launch tracing, and dispatch to
+// the kernels.  Every compute step runs on the GPU; nothing here touches tensor data.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <mutex>
+#include <vector>
+
+#include "pkv_internal.cuh"
+
+namespace pkv {
+
+// ------------------------------------------------------------------ status helpers
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
+
+namespace {
+std::mutex g_mu;
+constexpr int kMaxDevices = 64;
+DeviceCtx g_ctx[kMaxDevices];
+bool g_ctx_ready[kMaxDevices] = {};
+}  // namespace
+
+DeviceCtx* device_ctx(int* status) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    *status = PKV_ERR_CUDA;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_ctx_ready[dev]) {
+    DeviceCtx& c = g_ctx[dev];
+    c.device = dev;
+    if (cudaDeviceGetAttribute(&c.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      *status = PKV_ERR_CUDA;
+      return nullptr;
+    }
+    void* p = nullptr;
+    if (cudaMalloc(&p, 256) != cudaSuccess) {
+      *status = PKV_ERR_NO_MEMORY;
+      return nullptr;
+    }
+    if (cudaMemset(p, 0, 256) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+      cudaFree(p);
+      *status = PKV_ERR_CUDA;
+      return nullptr;
+    }
+    c.err = static_cast<uint32_t*>(p);
+    g_ctx_ready[dev] = true;
+  }
+  return &g_ctx[dev];
+}
+
+int ensure_workspace(DeviceCtx* ctx, size_t bytes, cudaStream_t stream) {
+  if (ctx->ws_bytes >= bytes) return PKV_OK;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return PKV_ERR_CUDA;
+  if (cap != cudaStreamCaptureStatusNone) return PKV_ERR_NO_MEMORY;  // never allocate while capturing
+  size_t want = ctx->ws_bytes ? ctx->ws_bytes : (1u << 20);
+  while (want < bytes) want *= 2;
+  if (ctx->ws) {
+    if (cudaFree(ctx->ws) != cudaSuccess) return PKV_ERR_CUDA;  // device-wide sync: no kernel still reads it
+    ctx->ws = nullptr;
+    ctx->ws_bytes = 0;
+  }
+  if (cudaMalloc(&ctx->ws, want) != cudaSuccess) {
+    ctx->ws = nullptr;
+    return PKV_ERR_NO_MEMORY;
+  }
+  ctx->ws_bytes = want;
+  return PKV_OK;
+}
+
+// ------------------------------------------------------------------ tensor maps
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+}  // namespace
+
+int encode_tensor_map_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                         uint32_t box_inner, uint32_t box_outer) {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) return PKV_ERR_CUDA;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_INVALID_ARG;
+}
+
+int encode_tensor_map_3d(CUtensorMap* map, const void* base, const uint64_t dims_in[3], const uint64_t strides_in[2],
+                         const uint32_t box_in[3]) {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) return PKV_ERR_CUDA;
+  const cuuint64_t dims[3] = {dims_in[0], dims_in[1], dims_in[2]};
+  const cuuint64_t strides[2] = {strides_in[0], strides_in[1]};
+  const cuuint32_t box[3] = {box_in[0], box_in[1], box_in[2]};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_INVALID_ARG;
+}
+
+// ------------------------------------------------------------------ tracing
+namespace {
+constexpr int kTraceSlots = 8192;
+bool g_trace_on = false;
+int g_trace_device = -1;
+std::vector<cudaEvent_t> g_ev_start, g_ev_stop;
+std::vector<int> g_pending_kind;  // kind per used slot
+int64_t g_launches[PKV_TRACE_KINDS] = {};
+double g_ms[PKV_TRACE_KINDS] = {};
+const char* kTraceNames[PKV_TRACE_KINDS] = {"slot_mapping", "write", "copy_blocks", "plan",
+                                            "decode", "prefill", "generic_attention", "other"};
+}  // namespace
+
+TraceScope::TraceScope(int k, cudaStream_t s) : kind(k), stream(s), slot(-1) {
+  if (!g_trace_on) return;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != g_trace_device) return;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (static_cast<int>(g_pending_kind.size()) >= kTraceSlots) return;
+  slot = static_cast<int>(g_pending_kind.size());
+  g_pending_kind.push_back(kind);
+  cudaEventRecord(g_ev_start[slot], stream);
+}
+TraceScope::~TraceScope() {
+  if (slot >= 0) cudaEventRecord(g_ev_stop[slot], stream);
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+// ------------------------------------------------------------------ argument checks
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_cache(const pkv_cache_desc* c) {
+  if (!c) return PKV_ERR_INVALID_ARG;
+  if (c->block_size != PKV_BLOCK_SIZE || c->num_blocks <= 0 || c->num_kv_heads <= 0 || c->head_dim <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if (c->num_blocks > (int64_t(1) << 40)) return PKV_ERR_INVALID_ARG;
+  if (c->dtype == PKV_F32 && (c->head_dim == 64 || c->head_dim == 128)) return PKV_OK;
+  if (c->dtype == PKV_BF16 && c->head_dim == 128) return PKV_OK;
+  return PKV_ERR_UNSUPPORTED;
+}
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+extern "C" {
+
+int pkv_slot_mapping(const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                     const int32_t* query_start_loc, int32_t num_seqs, int64_t num_tokens, int64_t* slot_mapping,
+                     void* stream) {
+  if (num_tokens < 0 || num_seqs < 0) return PKV_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PKV_OK;
+  if (num_seqs == 0 || max_blocks_per_seq <= 0 || !block_tables || !seq_lens || !query_start_loc ||
+      !slot_mapping)
+    return PKV_ERR_INVALID_ARG;
+  int st = PKV_OK;
+  DeviceCtx* ctx = device_ctx(&st);
+  if (!ctx) return st;
+  return launch_slot_mapping(block_tables, max_blocks_per_seq, seq_lens, query_start_loc, num_seqs, num_tokens,
+                             slot_mapping, ctx->err, as_stream(stream));
+}
+
+int pkv_write(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens, void* k_cache,
+              void* v_cache, const pkv_cache_desc* cache, void* stream) {
+  int st = check_cache(cache);
+  if (st) return st;
+  if (num_tokens < 0) return PKV_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_INVALID_ARG;
+  DeviceCtx* ctx = device_ctx(&st);
+  if (!ctx) return st;
+  return launch_write(k, v, slot_mapping, num_tokens, k_cache, v_cache, *cache, ctx->err, as_stream(stream));
+}
+
+int pkv_copy_blocks(const int32_t* src, const int32_t* dst, int64_t n, void* k_cache, void* v_cache,
+                    const pkv_cache_desc* cache, void* stream) {
+  int st = check_cache(cache);
+  if (st) return st;
+  if (n < 0) return PKV_ERR_INVALID_ARG;
+  if (n == 0) return PKV_OK;
+  if (!src || !dst || !k_cache || !v_cache || !aligned16(k_cache) || !aligned16(v_cache))
+    return PKV_ERR_INVALID_ARG;
+  DeviceCtx* ctx = device_ctx(&st);
+  if (!ctx) return st;
+  return launch_copy_blocks(src, dst, n, k_cache, v_cache, *cache, ctx->err, as_stream(stream));
+}
+
+int paged_attention(const void* q, const void* k_cache, const void* v_cache, const pkv_cache_desc* cache,
+                    const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                    const int32_t* query_start_loc, int32_t num_seqs, int32_t num_q_heads, int64_t num_tokens,
+                    int32_t max_query_len, int32_t max_seq_len, float scale, void* out, void* stream) {
+  int st = check_cache(cache);
+  if (st) return st;
+  if (num_tokens < 0 || num_seqs < 0 || num_q_heads <= 0 || num_q_heads % cache->num_kv_heads != 0)
+    return PKV_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PKV_OK;
+  if (num_seqs == 0 || max_blocks_per_seq <= 0 || max_query_len <= 0 || max_seq_len <= 0) return PKV_ERR_INVALID_ARG;
+  if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !query_start_loc || !out)
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return PKV_ERR_INVALID_ARG;
+  DeviceCtx* ctx = device_ctx(&st);
+  if (!ctx) return st;
+  AttnArgs a{q,        k_cache,    v_cache,       *cache,      block_tables, max_blocks_per_seq, seq_lens,
+             query_start_loc, num_seqs, num_q_heads, num_tokens, max_query_len, max_seq_len, scale, out};
+  return launch_generic_attention(a, ctx->err, as_stream(stream));
+}
+
+int pkv_peek_error_bits(void* stream, uint32_t* bits) {
+  if (!bits) return PKV_ERR_INVALID_ARG;
+  int st = PKV_OK;
+  DeviceCtx* ctx = device_ctx(&st);
+  if (!ctx) return st;
+  if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return PKV_ERR_CUDA;
+  if (cudaMemcpy(bits, ctx->err, sizeof(uint32_t), cudaMemcpyDeviceToHost) != cudaSuccess) return PKV_ERR_CUDA;
+  return PKV_OK;
+}
+
+int pkv_get_last_error(void* stream) {
+  uint32_t bits = 0;
+  int st = pkv_peek_error_bits(stream, &bits);
+  if (st) return st;
+  int dummy = PKV_OK;
+  DeviceCtx* ctx = device_ctx(&dummy);
+  if (cudaMemset(ctx->err, 0, sizeof(uint32_t)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
+    return PKV_ERR_CUDA;
+  if (bits & kErrTimeout) return PKV_ERR_TIMEOUT;
+  if (bits) return PKV_ERR_INDEX;
+  return PKV_OK;
+}
+
+const char* pkv_status_string(int status) {
+  switch (status) {
+    case PKV_OK: return "PKV_OK";
+    case PKV_ERR_INVALID_ARG: return "PKV_ERR_INVALID_ARG";
+    case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED";
+    case PKV_ERR_INDEX: return "PKV_ERR_INDEX";
+    case PKV_ERR_CUDA: return "PKV_ERR_CUDA";
+    case PKV_ERR_NO_MEMORY: return "PKV_ERR_NO_MEMORY";
+    case PKV_ERR_TIMEOUT: return "PKV_ERR_TIMEOUT";
+    default: return "PKV_ERR_UNKNOWN";
+  }
+}
+
+int pkv_num_workers(int32_t* workers) {
+  if (!workers) return PKV_ERR_INVALID_ARG;
+  int st = PKV_OK;
+  DeviceCtx* ctx = device_ctx(&st);
+  if (!ctx) return st;
+  *workers = ctx->num_sms;
+  return PKV_OK;
+}
+
+void pkv_shutdown(void) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  int prev = 0;
+  cudaGetDevice(&prev);
+  for (int d = 0; d < kMaxDevices; ++d) {
+    if (!g_ctx_ready[d]) continue;
+    cudaSetDevice(d);
+    cudaDeviceSynchronize();
+    if (g_ctx[d].ws) cudaFree(g_ctx[d].ws);
+    if (g_ctx[d].err) cudaFree(g_ctx[d].err);
+    g_ctx[d] = DeviceCtx{};
+    g_ctx_ready[d] = false;
+  }
+  cudaSetDevice(prev);
+}
+
+int pkv_trace_enable(int on) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (on) {
+    if (g_ev_start.empty() || g_trace_device != dev) {
+      for (auto e : g_ev_start) cudaEventDestroy(e);
+      for (auto e : g_ev_stop) cudaEventDestroy(e);
+      g_ev_start.assign(kTraceSlots, nullptr);
+      g_ev_stop.assign(kTraceSlots, nullptr);
+      for (int i = 0; i < kTraceSlots; ++i) {
+        if (cudaEventCreate(&g_ev_start[i]) != cudaSuccess || cudaEventCreate(&g_ev_stop[i]) != cudaSuccess)
+          return PKV_ERR_CUDA;
+      }
+    }
+    g_trace_device = dev;
+    g_pending_kind.clear();
+    for (int k = 0; k < PKV_TRACE_KINDS; ++k) {
+      g_launches[k] = 0;
+      g_ms[k] = 0.0;
+    }
+  }
+  g_trace_on = on != 0;
+  return PKV_OK;
+}
+
+int pkv_trace_read(int64_t* launches, double* total_ms) {
+  if (!launches || !total_ms) return PKV_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return PKV_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  for (size_t i = 0; i < g_pending_kind.size(); ++i) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, g_ev_start[i], g_ev_stop[i]) != cudaSuccess) return PKV_ERR_CUDA;
+    g_launches[g_pending_kind[i]] += 1;
+    g_ms[g_pending_kind[i]] += ms;
+  }
+  g_pending_kind.clear();
+  for (int k = 0; k < PKV_TRACE_KINDS; ++k) {
+    launches[k] = g_launches[k];
+    total_ms[k] = g_ms[k];
+    g_launches[k] = 0;
+    g_ms[k] = 0.0;
+  }
+  return PKV_OK;
+}
+
+const char* pkv_trace_kind_name(int kind) {
+  if (kind < 0 || kind >= PKV_TRACE_KINDS) return "unknown";
+  return kTraceNames[kind];
+}
+
+int pkv_umma_selftest(const int32_t* params, const void* a_img, const void* b_img, float* d_out, void* stream) {
+  if (!params || !a_img || !b_img || !d_out) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(a_img) || !aligned16(b_img)) return PKV_ERR_INVALID_ARG;
+  int st = PKV_OK;
+  DeviceCtx* ctx = device_ctx(&st);
+  if (!ctx) return st;
+  return run_umma_selftest(params, a_img, b_img, d_out, ctx->err, as_stream(stream));
+}
+
+int pkv_tma_selftest(const void* src, int64_t rows, int32_t row0, void* dump, void* stream) {
+  if (!src || !dump || !aligned16(src) || !aligned16(dump)) return PKV_ERR_INVALID_ARG;
+  int st = PKV_OK;
+  DeviceCtx* ctx = device_ctx(&st);
+  if (!ctx) return st;
+  return run_tma_selftest(src, rows, row0, dump, ctx->err, as_stream(stream));
+}
+
+}  // extern "C"

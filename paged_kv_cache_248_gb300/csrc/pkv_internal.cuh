@@ -1,0 +1,119 @@
+// pkv_internal.cuh -- definitions shared by the library's translation units.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "../../include/pkv.h"
+
+namespace pkv {
+
+constexpr int kBlock = 16;  // tokens per KV block
+
+// Device error word bits (pkv_peek_error_bits).
+enum : uint32_t {
+  kErrBlockId = 1u << 0,   // block id outside [0, num_blocks)
+  kErrSlot = 1u << 1,      // slot past the pool
+  kErrLength = 1u << 2,    // seq_len < q_len, or more blocks than a table row holds
+  kErrTimeout = 1u << 3,   // a bounded wait gave up
+};
+
+// Trace kinds (pkv_trace_read).
+enum TraceKind : int {
+  kTraceSlotMap = 0,
+  kTraceWrite = 1,
+  kTraceCopy = 2,
+  kTracePlan = 3,
+  kTraceDecode = 4,
+  kTracePrefill = 5,
+  kTraceGeneric = 6,
+};
+
+__device__ __forceinline__ void flag_error(uint32_t* err, uint32_t bits) {
+  if (err != nullptr) atomicOr(err, bits);
+}
+
+template <typename T>
+struct Elem;
+template <>
+struct Elem<float> {
+  static __device__ __forceinline__ float to_f32(float x) { return x; }
+  static __device__ __forceinline__ float from_f32(float x) { return x; }
+};
+template <>
+struct Elem<__nv_bfloat16> {
+  static __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+  static __device__ __forceinline__ __nv_bfloat16 from_f32(float x) { return __float2bfloat16_rn(x); }
+};
+
+// Binary search: the request owning query token t (last i with qsl[i] <= t).
+__device__ __forceinline__ int find_seq(const int32_t* __restrict__ qsl, int num_seqs, int64_t t) {
+  int lo = 0, hi = num_seqs - 1;
+  while (lo < hi) {
+    int mid = lo + (hi - lo + 1) / 2;
+    if (static_cast<int64_t>(__ldg(qsl + mid)) <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+}  // namespace pkv
+
+// ------------------------------------------------------------------ host side
+namespace pkv {
+
+struct DeviceCtx {
+  int device = -1;
+  int num_sms = 0;
+  uint32_t* err = nullptr;     // device error word
+  void* ws = nullptr;          // workspace
+  size_t ws_bytes = 0;
+};
+
+// Per-device context (created on first use on the current device).
+DeviceCtx* device_ctx(int* status);
+// Ensures the workspace holds at least `bytes`; refuses to grow during capture.
+int ensure_workspace(DeviceCtx* ctx, size_t bytes, cudaStream_t stream);
+
+// Tracing: bracket a launch with events when tracing is on.
+struct TraceScope {
+  int kind;
+  cudaStream_t stream;
+  int slot;
+  TraceScope(int kind, cudaStream_t stream);
+  ~TraceScope();
+};
+
+int cuda_status(cudaError_t e);
+
+// Launchers implemented in the kernel translation units (return pkv_status).
+int launch_slot_mapping(const int32_t* bt, int32_t max_blocks, const int32_t* seq_lens, const int32_t* qsl,
+                        int32_t num_seqs, int64_t num_tokens, int64_t* slots, uint32_t* err, cudaStream_t s);
+int launch_write(const void* k, const void* v, const int64_t* slots, int64_t T, void* kc, void* vc,
+                 const pkv_cache_desc& c, uint32_t* err, cudaStream_t s);
+int launch_copy_blocks(const int32_t* src, const int32_t* dst, int64_t n, void* kc, void* vc,
+                       const pkv_cache_desc& c, uint32_t* err, cudaStream_t s);
+
+struct AttnArgs {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  pkv_cache_desc cache;
+  const int32_t* block_tables;
+  int32_t max_blocks;
+  const int32_t* seq_lens;
+  const int32_t* qsl;
+  int32_t num_seqs;
+  int32_t num_q_heads;
+  int64_t num_tokens;
+  int32_t max_query_len;
+  int32_t max_seq_len;
+  float scale;
+  void* out;
+};
+int launch_generic_attention(const AttnArgs& a, uint32_t* err, cudaStream_t s);
+
+int run_umma_selftest(const int32_t* params, const void* a_img, const void* b_img, float* d_out, uint32_t* err,
+                      cudaStream_t s);
+int run_tma_selftest(const void* src, int64_t rows, int32_t row0, void* dump, uint32_t* err, cudaStream_t s);
+
+}  // namespace pkv

@@ -1,0 +1,73 @@
+"""Shared helpers for the parity tests: run one step on the GPU through the C ABI,
+run the same step through the oracle, and compare.
+
+A step is: slot mapping of the new tokens, scatter of their K/V into the pool,
+then attention over the mixed batch.  The oracle gets the same seeded inputs
+(the pool as drawn, before the GPU writes into it) and performs its own slot
+mapping and scatter; nothing it reads comes from the CUDA path.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+
+# tolerances: bf16 inputs, fp32 accumulation vs fp64 -> max-abs 2e-2, mean-abs 2e-3;
+# fp32 inputs -> max-abs 1e-4
+TOL = {"bf16": (2e-2, 2e-3), "f32": (1e-4, 1e-4)}
+
+
+def bits(x: torch.Tensor) -> np.ndarray:
+    """CPU copy as the oracle reads it: fp32 array or bf16 bit patterns (int16)."""
+    x = x.detach().cpu().contiguous()
+    if x.dtype == torch.bfloat16:
+        return x.view(torch.int16).numpy().copy()
+    return x.numpy().copy()
+
+
+def to_gpu_meta(w, bt=None):
+    dev = torch.device("cuda")
+    return dict(
+        block_tables=torch.from_numpy(np.ascontiguousarray(w.block_tables if bt is None else bt)).to(dev),
+        seq_lens=torch.from_numpy(w.seq_lens).to(dev),
+        query_start_loc=torch.from_numpy(w.query_start_loc).to(dev),
+    )
+
+
+def gpu_step(pkv, w, t: dict, bt=None, cow: bool = False):
+    """Run copy (optional) + slot mapping + write + attention on the GPU; tensors in
+    ``t`` must already be on the GPU (the caches are modified in place)."""
+    m = to_gpu_meta(w, bt)
+    if cow:
+        pkv.pkv_copy_blocks(torch.from_numpy(w.cow_src).cuda(), torch.from_numpy(w.cow_dst).cuda(),
+                            t["k_cache"], t["v_cache"])
+    slots = pkv.pkv_slot_mapping(m["block_tables"], m["seq_lens"], m["query_start_loc"], w.num_tokens)
+    pkv.pkv_write(t["k_new"], t["v_new"], slots, t["k_cache"], t["v_cache"])
+    out = pkv.paged_attention(t["q"], t["k_cache"], t["v_cache"], m["block_tables"], m["seq_lens"],
+                              m["query_start_loc"], w.scale, max(1, w.max_query_len), max(1, w.max_seq_len))
+    st = pkv.pkv_get_last_error()
+    return out, slots, st
+
+
+def oracle_step(w, t_cpu: dict, bt=None, rows=None, cow: bool = False):
+    """The same step by the oracle, from host copies of the drawn inputs."""
+    kc, vc = bits(t_cpu["k_cache"]), bits(t_cpu["v_cache"])
+    table = w.block_tables if bt is None else bt
+    if cow:
+        oracle.copy_blocks(w.cow_src, w.cow_dst, kc, vc)
+    slots = oracle.slot_mapping(table, w.seq_lens, w.query_start_loc)
+    oracle.write(bits(t_cpu["k_new"]), bits(t_cpu["v_new"]), slots, kc, vc)
+    out = oracle.attention(bits(t_cpu["q"]), kc, vc, table, w.seq_lens, w.query_start_loc, w.scale, rows=rows)
+    return out, slots, kc, vc
+
+
+def compare(got: torch.Tensor, ref: np.ndarray, dtype: str, what: str = ""):
+    g = got.detach().float().cpu().double().numpy()
+    assert g.shape == ref.shape, (g.shape, ref.shape)
+    err = np.abs(g - ref)
+    max_tol, mean_tol = TOL[dtype]
+    assert np.isfinite(g).all(), f"{what}: non-finite output"
+    assert err.max() <= max_tol, f"{what}: max-abs {err.max():.3e} > {max_tol}"
+    assert err.mean() <= mean_tol, f"{what}: mean-abs {err.mean():.3e} > {mean_tol}"
+    return float(err.max()), float(err.mean())
