@@ -1,0 +1,466 @@
+"""Benchmark of the PagedAttention hot path on GB300.
+
+One step = one pass of the whole path over one batch: slot mapping of the step's
+new tokens, their K/V scatter into the paged pool, and attention over the mixed
+batch of chunked prefills and decodes.  Default workload: the continuous-batching
+step with an 8192-token budget (8 chunked-prefill chunks of 512 queries after a
+cached context uniform in [0, 3072], plus 4096 decodes with seq_lens uniform in
+[256, 2048]; 32/8 heads, head_dim 128, bf16, block tables randomly permuted).
+The line also carries the long-context decode KV-read bandwidth (32 requests x
+32768 tokens, 64/8 heads).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload mixed|long|decode|prefix|tiny] [--no-e2e] [--no-cpu]
+
+Inputs are drawn on the device and resident in HBM when timing starts; each step
+reads ~19 GB of KV (far above the 129 MB L2), so no L2 flush is needed between
+steps.  Times are CUDA events on the launching stream, max over ranks.  With
+--gpus N > 1 (torchrun) every rank runs an independent replica (the path has no
+exchange step) and ``value`` sums the ranks' tokens over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "decode KV-read GB/s (% of HBM peak); mixed-step tokens/sec at 1 GB300"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------- work accounting
+
+def algorithmic_bytes(w) -> dict:
+    """Bytes an ideal implementation must move for one attention launch, split by
+    request kind: K and V of every visible context token (unique physical tokens
+    where requests share blocks), q and out, the block-table entries read."""
+    eb = w.elem_bytes
+    kv_tok = 2 * w.num_kv_heads * w.head_dim * eb
+    q_tok = w.num_q_heads * w.head_dim * eb
+    ql = w.q_lens
+    dec = ql == 1
+    pre = ql > 1
+    L = w.seq_lens.astype(np.int64)
+    bt_bytes = ((L + 15) // 16) * 4
+    if w.name == "prefix":
+        n_prefix = w.notes["prefix_blocks"] * 16
+        dec_kv = (n_prefix + int((L - n_prefix).sum())) * kv_tok
+    else:
+        dec_kv = int(L[dec].sum()) * kv_tok
+    pre_kv = int(L[pre].sum()) * kv_tok
+    dec_io = int(dec.sum()) * 2 * q_tok + int(bt_bytes[dec].sum())
+    pre_io = int(ql[pre].sum()) * 2 * q_tok + int(bt_bytes[pre].sum())
+    return {"decode": dec_kv + dec_io, "decode_kv": dec_kv, "prefill": pre_kv + pre_io,
+            "total": dec_kv + dec_io + pre_kv + pre_io}
+
+
+def algorithmic_flops(w) -> dict:
+    """4 * head_dim * Hq flops per (query, visible key) pair; causal pairs only."""
+    ql = w.q_lens.astype(np.int64)
+    L = w.seq_lens.astype(np.int64)
+    per_pair = 4 * w.head_dim * w.num_q_heads
+    dec = int(L[ql == 1].sum())
+    pre = 0
+    for n, l in zip(ql[ql > 1], L[ql > 1]):
+        c = l - n
+        pre += int(n * c + n * (n + 1) // 2)
+    return {"decode": dec * per_pair, "prefill": pre * per_pair}
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- the step
+
+class Step:
+    """Device-resident inputs of one workload and the three C-ABI calls of a step."""
+
+    def __init__(self, pkv, w, device):
+        self.pkv, self.w = pkv, w
+        t = w.make_tensors(device)
+        self.t = t
+        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)  # noqa: E731
+        self.bt, self.sl, self.qsl = dev(w.block_tables), dev(w.seq_lens), dev(w.query_start_loc)
+        self.slots = torch.empty(w.num_tokens, dtype=torch.int64, device=device)
+        self.out = torch.empty_like(t["q"])
+        self.cow = (dev(w.cow_src), dev(w.cow_dst)) if w.cow_src is not None else None
+
+    def run(self):
+        p, w, t = self.pkv, self.w, self.t
+        if self.cow is not None:
+            p.pkv_copy_blocks(self.cow[0], self.cow[1], t["k_cache"], t["v_cache"])
+        p.pkv_slot_mapping(self.bt, self.sl, self.qsl, w.num_tokens, out=self.slots)
+        p.pkv_write(t["k_new"], t["v_new"], self.slots, t["k_cache"], t["v_cache"])
+        p.paged_attention(t["q"], t["k_cache"], t["v_cache"], self.bt, self.sl, self.qsl, w.scale,
+                          w.max_query_len, w.max_seq_len, out=self.out)
+
+    def attention_only(self):
+        p, w, t = self.pkv, self.w, self.t
+        p.paged_attention(t["q"], t["k_cache"], t["v_cache"], self.bt, self.sl, self.qsl, w.scale,
+                          w.max_query_len, w.max_seq_len, out=self.out)
+
+
+class E2EStep:
+    """The same step from pinned HOST buffers: H2D of the step's inputs (q, new K/V,
+    block tables, lengths), the three calls, D2H of the attention output."""
+
+    def __init__(self, step: Step):
+        self.s = step
+        t = step.t
+        pin = lambda x: x.detach().to("cpu").pin_memory()  # noqa: E731
+        self.h = {k: pin(t[k]) for k in ("q", "k_new", "v_new")}
+        self.h_bt, self.h_sl, self.h_qsl = pin(step.bt), pin(step.sl), pin(step.qsl)
+        self.h_out = torch.empty(t["q"].shape, dtype=t["q"].dtype).pin_memory()
+        self.d = {k: torch.empty_like(t[k]) for k in ("q", "k_new", "v_new")}
+        self.h2d = sum(x.numel() * x.element_size() for x in list(self.h.values()) + [self.h_bt, self.h_sl,
+                                                                                           self.h_qsl])
+        self.d2h = self.h_out.numel() * self.h_out.element_size()
+
+    def run(self):
+        s, p, w, t = self.s, self.s.pkv, self.s.w, self.s.t
+        for k in self.d:
+            self.d[k].copy_(self.h[k], non_blocking=True)
+        s.bt.copy_(self.h_bt, non_blocking=True)
+        s.sl.copy_(self.h_sl, non_blocking=True)
+        s.qsl.copy_(self.h_qsl, non_blocking=True)
+        p.pkv_slot_mapping(s.bt, s.sl, s.qsl, w.num_tokens, out=s.slots)
+        p.pkv_write(self.d["k_new"], self.d["v_new"], s.slots, t["k_cache"], t["v_cache"])
+        p.paged_attention(self.d["q"], t["k_cache"], t["v_cache"], s.bt, s.sl, s.qsl, w.scale, w.max_query_len,
+                          w.max_seq_len, out=s.out)
+        self.h_out.copy_(s.out, non_blocking=True)
+
+
+def timed(fn, steps, warmup, barrier=None):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    return e0.elapsed_time(e1) / steps
+
+
+# ----------------------------------------------------------------------------- CPU oracle sample
+
+def cpu_sample(w, t_gpu, target_s: float = 12.0, seed: int = 0):
+    """Time the oracle (as it stands) on a bounded sample of the workload: a sub-batch
+    of requests (all chunks, a subset of decodes) with sampled query rows; returns
+    (tokens/s, description, threads)."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    qsl = w.query_start_loc
+    ql = w.q_lens
+    dec_ids = np.nonzero(ql == 1)[0]
+    pre_ids = np.nonzero(ql > 1)[0]
+
+    def build(n_dec, rows_per_chunk):
+        pick_dec = rng.choice(dec_ids, size=min(n_dec, len(dec_ids)), replace=False) if len(dec_ids) else []
+        seq_ids = np.concatenate([pre_ids, np.sort(pick_dec)]).astype(np.int64)
+        bt = w.block_tables[seq_ids]
+        used = np.unique(bt[bt >= 0])
+        remap = np.full(w.num_blocks, -1, np.int32)
+        remap[used] = np.arange(len(used), dtype=np.int32)
+        bt2 = np.where(bt >= 0, remap[np.maximum(bt, 0)], -1).astype(np.int32)
+        idx = torch.from_numpy(used.astype(np.int64)).to(t_gpu["k_cache"].device)
+        to_bits = lambda x: (x.view(torch.int16) if x.dtype == torch.bfloat16 else x).cpu().numpy().copy()  # noqa
+        kc = to_bits(t_gpu["k_cache"].index_select(0, idx))
+        vc = to_bits(t_gpu["v_cache"].index_select(0, idx))
+        rows = np.concatenate([np.arange(qsl[i], qsl[i + 1]) for i in seq_ids]).astype(np.int64)
+        ridx = torch.from_numpy(rows).to(t_gpu["q"].device)
+        q = to_bits(t_gpu["q"].index_select(0, ridx))
+        kn = to_bits(t_gpu["k_new"].index_select(0, ridx))
+        vn = to_bits(t_gpu["v_new"].index_select(0, ridx))
+        q_lens = ql[seq_ids]
+        qsl2 = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+        sel = []
+        for j, i in enumerate(seq_ids):
+            n = int(q_lens[j])
+            if n == 1:
+                sel.append(qsl2[j])
+            else:
+                k = min(n, rows_per_chunk)
+                sel.extend(qsl2[j] + np.sort(rng.choice(n, size=k, replace=False)))
+        sel = np.asarray(sel, np.int64)
+        L = w.seq_lens[seq_ids].copy()
+        return kc, vc, q, kn, vn, bt2, L, qsl2, sel
+
+    def run(args):
+        kc, vc, q, kn, vn, bt2, L, qsl2, sel = args
+        t0 = time.perf_counter()
+        slots = oracle.slot_mapping(bt2, L, qsl2)
+        oracle.write(kn, vn, slots, kc, vc)
+        oracle.attention(q, kc, vc, bt2, L, qsl2, w.scale, rows=sel)
+        return time.perf_counter() - t0, len(sel)
+
+    n_dec0, rpc0 = 32, 4
+    dt, n = run(build(n_dec0, rpc0))
+    scale = max(1.0, min(64.0, target_s / max(dt, 1e-3)))
+    n_dec, rpc = int(n_dec0 * scale), int(rpc0 * scale)
+    args = build(n_dec, rpc)
+    dt, n = run(args)
+    n_pre_rows = int(sum(min(int(x), rpc) for x in w.q_lens[w.q_lens > 1]))
+    desc = (f"oracle step (slot mapping + write + attention) on {n} query rows: "
+            f"{n - n_pre_rows} decode requests and {n_pre_rows} sampled prefill rows of the "
+            f"{w.name} workload; wall {dt:.2f} s")
+    return n / dt, desc, oracle.max_threads(), dt
+
+
+# ----------------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="mixed", choices=list(wl.NAMES))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-decode-line", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    barrier = None
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+        barrier = dist.barrier
+
+    w = wl.make(args.workload)
+    if args.impl == "reference":
+        return reference_arm(args, w, rank, world)
+
+    import paged_kv_cache_248_gb300 as pkv
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    pk = peaks()
+    step = Step(pkv, w, device)
+    work_b = algorithmic_bytes(w)
+    work_f = algorithmic_flops(w)
+
+    # ---- timed region: K steps, tracing the library's launches on the same stream
+    pkv.pkv_trace_enable(True)
+    pkv.pkv_trace_read()
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    pkv.pkv_trace_read()
+    with ClockSampler(local) as clk:
+        ms = timed(step.run, args.steps, 0, barrier)
+    trace = pkv.pkv_trace_read()
+    pkv.pkv_trace_enable(False)
+    st = pkv.pkv_get_last_error()
+    if st != 0:
+        raise RuntimeError(f"device error during bench: {pkv.status_string(st)}")
+    clocks = clk.summary()
+
+    ms_max = ms
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([ms], device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_max = float(tt.item())
+    tokens = w.num_tokens * world
+    value = tokens / (ms_max / 1e3)
+
+    launches = sum(n for n, _ in trace.values())
+    kernel_ms = {k: (n, t) for k, (n, t) in trace.items() if n}
+    # dominant kernel of the step and its roofline
+    dom = max(kernel_ms, key=lambda k: kernel_ms[k][1])
+    n_dom, t_dom = kernel_ms[dom]
+    per_launch_ms = t_dom / n_dom
+    if dom == "prefill":
+        flops = work_f["prefill"]
+        ach = flops / (per_launch_ms / 1e3) / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops_sustained"],
+                "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops_sustained"], "traffic": None}
+    else:
+        b = work_b["decode"] if dom == "decode" else work_b["total"]
+        ach = b / (per_launch_ms / 1e3) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / pk["hbm_gbs"], "traffic": None, "algorithmic_bytes_per_launch": b}
+    roof["peak_source"] = pk["source"]
+
+    res = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded N(0,1), shapes of the workload)",
+        "config": {"workload": f"{w.name}: {describe(w)}", "global_batch_tokens": tokens,
+                   "l2": "no flush: each step reads %.1f GB of KV, far above the 129 MB L2" % (
+                       work_b["total"] / 1e9),
+                   "parallelism": "replicas only" if world > 1 else "single GPU"},
+        "clocks": clocks, "roofline": roof, "gpu_launches": launches,
+        "kernels": {k: {"launches": n, "ms_total": t, "ms_per_launch": t / n} for k, (n, t) in kernel_ms.items()},
+        "work": {"bytes": work_b, "flops": work_f},
+    }
+
+    if not args.no_e2e:
+        e2e = E2EStep(step)
+        ms_e2e = timed(e2e.run, max(3, args.steps // 2), 3, barrier)
+        res["e2e"] = {"value": w.num_tokens * world / (ms_e2e / 1e3), "unit": "tokens/s",
+                      "h2d_bytes_per_step": e2e.h2d, "d2h_bytes_per_step": e2e.d2h, "ms_per_step": ms_e2e}
+        if pkv.pkv_get_last_error() != 0:
+            raise RuntimeError("device error during e2e")
+        del e2e
+
+    if not args.no_decode_line and args.workload == "mixed":
+        res["decode_kv_read"] = decode_line(pkv, device, pk, args)
+
+    if not args.no_cpu and rank == 0 and world == 1:
+        v, desc, cores, dt = cpu_sample(w, step.t)
+        res["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc}
+
+    if rank == 0:
+        print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def decode_line(pkv, device, pk, args) -> dict:
+    """KV-read bandwidth of the long-context decode (32 x 32768, 64/8 heads): the
+    paged_attention launch alone, K timed launches after warm-up."""
+    w = wl.make("long")
+    s = Step(pkv, w, device)
+    s.run()
+    pkv.pkv_trace_enable(True)
+    pkv.pkv_trace_read()
+    ms = timed(s.attention_only, max(10, args.steps), args.warmup)
+    trace = pkv.pkv_trace_read()
+    pkv.pkv_trace_enable(False)
+    if pkv.pkv_get_last_error() != 0:
+        raise RuntimeError("device error in decode line")
+    b = algorithmic_bytes(w)
+    kv = b["decode_kv"]
+    gbs = kv / (ms / 1e3) / 1e9
+    ker = {k: {"launches": n, "ms_per_launch": t / n} for k, (n, t) in trace.items() if n}
+    dom = max(ker, key=lambda k: ker[k]["ms_per_launch"] * ker[k]["launches"])
+    kgbs = b["decode"] / (ker[dom]["ms_per_launch"] / 1e3) / 1e9
+    out = {"workload": f"long: {describe(w)}", "kv_bytes": kv, "ms_per_call": ms, "kv_gbs": gbs,
+           "frac_of_hbm": gbs / pk["hbm_gbs"], "peak_gbs": pk["hbm_gbs"], "peak_source": pk["source"],
+           "kernel": dom, "kernel_gbs": kgbs, "kernel_frac": kgbs / pk["hbm_gbs"], "kernels": ker}
+    del s
+    torch.cuda.empty_cache()
+    return out
+
+
+def describe(w) -> str:
+    return (f"{w.num_seqs} requests, {w.num_tokens} query tokens, max context {w.max_seq_len}, "
+            f"{w.num_q_heads}/{w.num_kv_heads} heads, head_dim {w.head_dim}, {w.dtype}, pool {w.num_blocks} blocks")
+
+
+def reference_arm(args, w, rank, world):
+    """The oracle (CPU, fp64) timed as it stands on this host's cores: each step is a
+    bounded sample of the same workload.  Rank 0 only."""
+    if rank != 0:
+        return
+    import oracle
+    torch.manual_seed(0)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = w.make_tensors(dev)
+    rates, descs, dts = [], [], []
+    for i in range(args.warmup + args.steps):
+        v, desc, cores, dt = cpu_sample(w, t, target_s=4.0, seed=i)
+        if i >= args.warmup:
+            rates.append(v)
+            dts.append(dt)
+            descs.append(desc)
+    value = float(np.mean(rates))
+    res = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": float(np.mean(dts)) * 1e3,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic (seeded N(0,1), shapes of the workload)",
+           "config": {"workload": f"{w.name}: {describe(w)}", "parallelism": "host cores"},
+           "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.max_threads(), "kind": "oracle",
+                            "sample": descs[-1]},
+           "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(res))
+
+
+if __name__ == "__main__":
+    main()

@@ -72,6 +72,26 @@ int ensure_workspace(DeviceCtx* ctx, size_t bytes, cudaStream_t stream) {
   return PKV_OK;
 }
 
+size_t layout_workspace(void* base, int32_t num_seqs, int32_t hkv, int32_t group, int32_t head_dim,
+                        int64_t max_dec_items, Workspace* ws) {
+  size_t off = 0;
+  auto take = [&](size_t bytes) -> void* {
+    void* p = base ? static_cast<char*>(base) + off : nullptr;
+    off += (bytes + 255) & ~static_cast<size_t>(255);
+    return p;
+  };
+  Workspace w{};
+  w.counters = static_cast<int32_t*>(take(kNumQueueCounters * sizeof(int32_t)));
+  w.dec_prefix = static_cast<int32_t*>(take((static_cast<size_t>(num_seqs) + 1) * sizeof(int32_t)));
+  w.pre_prefix = static_cast<int32_t*>(take((static_cast<size_t>(num_seqs) + 1) * sizeof(int32_t)));
+  w.unit_arrive = static_cast<int32_t*>(take(static_cast<size_t>(num_seqs) * hkv * sizeof(int32_t)));
+  w.unit_bad = static_cast<int32_t*>(take(static_cast<size_t>(num_seqs) * hkv * sizeof(int32_t)));
+  w.part_ml = static_cast<float*>(take(static_cast<size_t>(max_dec_items) * group * 2 * sizeof(float)));
+  w.part_o = static_cast<float*>(take(static_cast<size_t>(max_dec_items) * group * head_dim * sizeof(float)));
+  if (ws) *ws = w;
+  return off;
+}
+
 // ------------------------------------------------------------------ tensor maps
 namespace {
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -231,7 +251,30 @@ int paged_attention(const void* q, const void* k_cache, const void* v_cache, con
   if (!ctx) return st;
   AttnArgs a{q,        k_cache,    v_cache,       *cache,      block_tables, max_blocks_per_seq, seq_lens,
              query_start_loc, num_seqs, num_q_heads, num_tokens, max_query_len, max_seq_len, scale, out};
-  return launch_generic_attention(a, ctx->err, as_stream(stream));
+  cudaStream_t s = as_stream(stream);
+  if (cache->dtype == PKV_F32) return launch_generic_attention(a, ctx->err, s);
+  // bf16, head_dim 128: tensor-core path
+  const int32_t hkv = cache->num_kv_heads;
+  const int32_t group = num_q_heads / hkv;
+  if (group > 16) return PKV_ERR_UNSUPPORTED;
+  const int32_t gp = group <= 4 ? 4 : (group <= 8 ? 8 : 16);
+  const int64_t max_splits = (static_cast<int64_t>(max_seq_len) + kSplitKeys - 1) / kSplitKeys;
+  const int64_t max_dec_items = static_cast<int64_t>(num_seqs) * hkv * max_splits;
+  if (max_dec_items >= (int64_t(1) << 31)) return PKV_ERR_UNSUPPORTED;
+  const size_t need = layout_workspace(nullptr, num_seqs, hkv, group, cache->head_dim, max_dec_items, nullptr);
+  st = ensure_workspace(ctx, need, s);
+  if (st) return st;
+  Workspace ws;
+  layout_workspace(ctx->ws, num_seqs, hkv, group, cache->head_dim, max_dec_items, &ws);
+  PlanArgs plan{seq_lens, query_start_loc, num_seqs, num_tokens, hkv, max_blocks_per_seq, max_seq_len,
+                kSplitKeys, kTileKeys / gp, ws.counters, ws.dec_prefix, ws.pre_prefix, ws.unit_arrive,
+                ws.unit_bad, ctx->err};
+  st = launch_plan(plan, s);
+  if (st) return st;
+  st = launch_decode_tc(a, ws, ctx->num_sms, ctx->err, s);
+  if (st) return st;
+  if (max_query_len > 1) st = launch_prefill_tc(a, ws, ctx->num_sms, ctx->err, s);
+  return st;
 }
 
 int pkv_peek_error_bits(void* stream, uint32_t* bits) {

@@ -1,0 +1,669 @@
+// k_decode.cu -- split-KV GQA decode on tcgen05 tensor cores (bf16, head_dim 128).
+//
+// What it computes ("vLLM's PagedAttention" teardown, section "PagedAttention":
+// the kernel is handed a per-request block table and gathers K/V from wherever the
+// 16-token blocks live): for a decode request i (one query token at position
+// seq_len - 1) and kv head h, the G query heads of h attend to all seq_len keys.
+//
+// Work decomposition.  Each (request, kv head) is cut into key splits of
+// kSplitKeys keys (a function of the request's own length only), giving
+// (request, kv head, split) items handed out by an atomic queue to persistent CTAs,
+// one per SM.  A split walks 128-key tiles (8 blocks).  A split that is the whole
+// request writes the output directly; otherwise it stores its fp32 partial
+// (running max, sum, unnormalised accumulator) and the last split to arrive
+// merges all partials in split order (log-sum-exp merge), so results never depend
+// on scheduling.
+//
+// Per CTA (192 threads):
+//   warp 0     producer: fetches items, loads the G query rows into shared memory,
+//              and per tile issues 4 TMA boxes per block (K and V, two 64-column
+//              halves each, 128-byte swizzle) straight from the block's physical
+//              location -- the block-table gather.  kStages tiles in flight.
+//   warp 1     MMA issuer (one lane): S^T = K Q^T with the 128 keys on M and the
+//              query-head group on N = 16, then O^T = V^T P^T with head_dim on M,
+//              both accumulating fp32 in TMEM.  V^T is read MN-major from the same
+//              swizzled V tile, so no transpose is ever materialised.
+//   warps 2-5  softmax: thread r owns TMEM lane r (key r of the tile for S^T, head
+//              element r for O^T).  Tile maxima per head by warp shuffles plus a
+//              4-warp exchange; exp2 of scaled logits; P^T written as bf16 into an
+//              unswizzled MN-major operand; partial O folded into registers with
+//              the online-softmax rescale.
+// Every wait is bounded; on a timeout the CTA raises an abort flag, reports
+// PKV_ERR_TIMEOUT, drains its in-flight copies and MMAs, frees TMEM and exits.
+#include "ptx.cuh"
+#include "pkv_internal.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kStages = 3;
+constexpr int kHalfBytes = 16384;             // one 64-column half of a 128-key tile
+constexpr int kKBytes = 2 * kHalfBytes;       // K tile: [2 halves][128 keys][128 B]
+constexpr int kStageBytes = 2 * kKBytes;      // K + V
+constexpr int kQBytes = 4096;                 // Q: [2 halves][16 rows][128 B]
+constexpr int kPBytes = 4096;                 // P^T: 128 keys x 16 heads, MN-major, no swizzle
+constexpr int kRing = 4;
+constexpr uint32_t kTmemCols = 64;            // S^T x2 (cols 0, 16), O^T x2 (cols 32, 48)
+constexpr int kBlocksPerTile = kTileKeys / kBlock;
+
+struct alignas(16) ItemInfo {
+  int32_t idx;  // decode item index; -1 = queue exhausted
+  int32_t seq, head, split;
+  int32_t nsplit, key_start, key_end, valid;
+};
+
+struct Ctl {
+  uint64_t full[kStages], empty[kStages];
+  uint64_t s_full[2], s_free[2], p_full[2], p_free[2], o_full[2], o_free[2];
+  uint64_t q_full[2], q_free[2];
+  uint64_t item_full[kRing], item_empty[kRing];
+  uint64_t drain;
+  uint64_t group_bar;  // the four softmax warps' exchange barrier
+  ItemInfo ring[kRing];
+  int bad[kRing];
+  float red[2][4][16];
+  uint32_t tmem_base;
+  int abort_flag;
+  int merge_flag;
+};
+
+constexpr int kSmemBytes = kStages * kStageBytes + 2 * kQBytes + 2 * kPBytes + static_cast<int>(sizeof(Ctl)) + 1024;
+
+struct DecodeParams {
+  const __nv_bfloat16* q;
+  __nv_bfloat16* out;
+  const int32_t* bt;
+  const int32_t* seq_lens;
+  const int32_t* qsl;
+  const int32_t* dec_prefix;
+  int32_t* queue;
+  int32_t* unit_arrive;
+  int32_t* unit_bad;
+  float* part_o;   // [items][G][128]
+  float* part_ml;  // [items][G][2]
+  uint32_t* err;
+  int64_t num_blocks;
+  int64_t num_tokens;
+  int32_t num_seqs, max_blocks, hkv, group, hq, split_keys;
+  float scale_log2;
+};
+
+__device__ __forceinline__ void raise_abort(Ctl& c, uint32_t* err) {
+  *reinterpret_cast<volatile int*>(&c.abort_flag) = 1;
+  flag_error(err, kErrTimeout);
+}
+
+// Barrier among the four softmax warps (one arrival per warp), bounded like every
+// other wait; `phase` counts the syncs this thread has made.
+__device__ __forceinline__ bool group_sync(Ctl& c, uint32_t& phase) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&c.group_bar);
+  const bool ok = mbar_wait(&c.group_bar, phase & 1, &c.abort_flag);
+  ++phase;
+  return ok;
+}
+
+__device__ ItemInfo make_item(const DecodeParams& P, int idx, int total) {
+  ItemInfo r{};
+  if (idx >= total) {
+    r.idx = -1;
+    return r;
+  }
+  int lo = 0, hi = P.num_seqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (P.dec_prefix[mid] <= idx) lo = mid; else hi = mid - 1;
+  }
+  const int i = lo;
+  const int base = P.dec_prefix[i];
+  const int nsplit = (P.dec_prefix[i + 1] - base) / P.hkv;
+  if (nsplit <= 0) {  // cannot happen for a consistent plan; treat as an invalid item
+    r.idx = idx;
+    r.seq = i;
+    r.nsplit = 1;
+    return r;
+  }
+  const int local = idx - base;
+  r.idx = idx;
+  r.seq = i;
+  r.head = local / nsplit;
+  r.split = local % nsplit;
+  r.nsplit = nsplit;
+  const int64_t L = P.seq_lens[i];
+  const int64_t t = P.qsl[i];
+  const bool ok = L >= 1 && (L + kBlock - 1) / kBlock <= P.max_blocks &&
+                  static_cast<int64_t>(nsplit) == (L + P.split_keys - 1) / P.split_keys && t >= 0 &&
+                  t < P.num_tokens && P.qsl[i + 1] == t + 1;
+  r.valid = ok ? 1 : 0;
+  r.key_start = ok ? r.split * P.split_keys : 0;
+  const int64_t split_end = static_cast<int64_t>(r.key_start) + P.split_keys;
+  r.key_end = ok ? static_cast<int32_t>(L < split_end ? L : split_end) : 0;
+  return r;
+}
+
+// ------------------------------------------------------------------ producer warp
+__device__ void producer_warp(const DecodeParams& P, const CUtensorMap* kmap, const CUtensorMap* vmap, Ctl& c,
+                              uint8_t* stages, uint8_t* qbuf) {
+  const int lane = threadIdx.x & 31;
+  const int total = P.dec_prefix[P.num_seqs];
+  uint32_t it = 0, tc = 0, qc = 0;
+  volatile int* abort_flag = &c.abort_flag;
+  while (true) {
+    const int slot = it % kRing;
+    if (!mbar_wait(&c.item_empty[slot], ((it / kRing) & 1) ^ 1, abort_flag)) {
+      if (!*abort_flag && lane == 0) raise_abort(c, P.err);
+      break;
+    }
+    if (lane == 0) {
+      const int idx = atomicAdd(P.queue, 1);
+      c.ring[slot] = make_item(P, idx, total);
+      c.bad[slot] = 0;
+      mbar_arrive(&c.item_full[slot]);
+    }
+    __syncwarp();
+    const ItemInfo info = c.ring[slot];
+    ++it;
+    if (info.idx < 0) break;
+    if (!info.valid) continue;
+
+    // the G query rows of this (token, kv head), K-major with the 128B swizzle
+    const int qb = qc & 1;
+    if (!mbar_wait(&c.q_free[qb], ((qc >> 1) & 1) ^ 1, abort_flag)) {
+      if (!*abort_flag && lane == 0) raise_abort(c, P.err);
+      break;
+    }
+    {
+      uint8_t* qs = qbuf + qb * kQBytes;
+      const int64_t trow = P.qsl[info.seq];
+      const uint4* src = reinterpret_cast<const uint4*>(P.q + (trow * P.hq + static_cast<int64_t>(info.head) * P.group) * 128);
+      for (int ch = lane; ch < P.group * 16; ch += 32) {
+        const int r = ch >> 4, cc = ch & 15, half = cc >> 3, c8 = cc & 7;
+        *reinterpret_cast<uint4*>(qs + half * 2048 + r * 128 + ((c8 ^ (r & 7)) << 4)) = __ldg(src + ch);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&c.q_full[qb]);
+      ++qc;
+    }
+
+    const int nt = (info.key_end - info.key_start + kTileKeys - 1) / kTileKeys;
+    const int32_t* btrow = P.bt + static_cast<int64_t>(info.seq) * P.max_blocks;
+    bool ok = true;
+    for (int j = 0; j < nt; ++j) {
+      const int st = tc % kStages;
+      if (!mbar_wait(&c.empty[st], ((tc / kStages) & 1) ^ 1, abort_flag)) {
+        if (!*abort_flag && lane == 0) raise_abort(c, P.err);
+        ok = false;
+        break;
+      }
+      const int t0 = info.key_start + j * kTileKeys;
+      const int nblk = min(kBlocksPerTile, (info.key_end - t0 + kBlock - 1) / kBlock);
+      int id = 0;
+      bool bad = false;
+      if (lane < nblk) {
+        id = __ldg(btrow + t0 / kBlock + lane);
+        if (id < 0 || id >= P.num_blocks) {
+          bad = true;
+          id = 0;
+        }
+      }
+      if (__any_sync(0xffffffffu, bad)) {
+        if (bad) flag_error(P.err, kErrBlockId);
+        if (lane == 0) c.bad[slot] = 1;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(&c.full[st], static_cast<uint32_t>(nblk) * 8192u);
+      __syncwarp();
+      if (lane < nblk) {
+        uint8_t* s = stages + st * kStageBytes + lane * 2048;
+        const int32_t row = (id * P.hkv + info.head) * kBlock;
+        tma_load_2d(s, kmap, &c.full[st], 0, row);
+        tma_load_2d(s + kHalfBytes, kmap, &c.full[st], 64, row);
+        tma_load_2d(s + kKBytes, vmap, &c.full[st], 0, row);
+        tma_load_2d(s + kKBytes + kHalfBytes, vmap, &c.full[st], 64, row);
+      }
+      ++tc;
+    }
+    if (!ok) break;
+  }
+  if (*abort_flag) {
+    // let copies already issued land before the CTA's shared memory goes away
+    const uint32_t first = tc > static_cast<uint32_t>(kStages) ? tc - kStages : 0;
+    for (uint32_t cnt = first; cnt < tc; ++cnt) mbar_wait(&c.full[cnt % kStages], (cnt / kStages) & 1, nullptr);
+  }
+}
+
+// ------------------------------------------------------------------ MMA warp
+__device__ void mma_warp(const DecodeParams& P, Ctl& c, uint8_t* stages, uint8_t* qbuf, uint8_t* pbuf,
+                         uint32_t tmem) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t idesc_s = umma_idesc_bf16(128, 16, false, false);
+  const uint32_t idesc_o = umma_idesc_bf16(128, 16, true, true);
+  volatile int* abort_flag = &c.abort_flag;
+  uint32_t it = 0, tc = 0, qc = 0;
+  bool issued = false;
+
+  auto pv = [&](uint32_t cnt) -> bool {
+    const int st = cnt % kStages, b = cnt & 1;
+    const uint32_t ph = (cnt >> 1) & 1;
+    if (!mbar_wait(&c.p_full[b], ph, abort_flag) || !mbar_wait(&c.o_free[b], ph ^ 1, abort_flag)) return false;
+    tc_fence_after();
+    if (lane == 0) {
+      const uint64_t a = umma_smem_desc(smem_u32(stages + st * kStageBytes + kKBytes), kHalfBytes, 1024, kLayout128B);
+      const uint64_t bd = umma_smem_desc(smem_u32(pbuf + b * kPBytes), 128, 2048, kLayoutNone);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        umma_f16_ss(tmem + 32 + 16 * b, umma_desc_advance(a, kk * 2048), umma_desc_advance(bd, kk * 256), idesc_o,
+                    kk > 0);
+      umma_commit(&c.o_full[b]);
+      umma_commit(&c.p_free[b]);
+      umma_commit(&c.empty[st]);
+    }
+    __syncwarp();
+    return true;
+  };
+
+  bool ok = true;
+  while (ok) {
+    const int slot = it % kRing;
+    if (!mbar_wait(&c.item_full[slot], (it / kRing) & 1, abort_flag)) {
+      ok = false;
+      break;
+    }
+    const ItemInfo info = c.ring[slot];
+    ++it;
+    if (info.idx < 0) break;
+    if (info.valid) {
+      const int qb = qc & 1;
+      if (!mbar_wait(&c.q_full[qb], (qc >> 1) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      const int nt = (info.key_end - info.key_start + kTileKeys - 1) / kTileKeys;
+      for (int j = 0; j < nt && ok; ++j) {
+        const int st = tc % kStages, sb = tc & 1;
+        if (!mbar_wait(&c.full[st], (tc / kStages) & 1, abort_flag) ||
+            !mbar_wait(&c.s_free[sb], ((tc >> 1) & 1) ^ 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint64_t a = umma_smem_desc(smem_u32(stages + st * kStageBytes), 16, 1024, kLayout128B);
+          const uint64_t b = umma_smem_desc(smem_u32(qbuf + qb * kQBytes), 16, 1024, kLayout128B);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma_f16_ss(tmem + 16 * sb, umma_desc_advance(a, (kk >> 2) * kHalfBytes + (kk & 3) * 32),
+                        umma_desc_advance(b, (kk >> 2) * 2048 + (kk & 3) * 32), idesc_s, kk > 0);
+          umma_commit(&c.s_full[sb]);
+          if (j == nt - 1) umma_commit(&c.q_free[qb]);
+          issued = true;
+        }
+        __syncwarp();
+        if (j > 0 && !pv(tc - 1)) ok = false;
+        ++tc;
+      }
+      if (ok && !pv(tc - 1)) ok = false;
+      ++qc;
+    }
+    if (!ok) break;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&c.item_empty[slot]);
+  }
+  if (!ok && !*abort_flag && lane == 0) raise_abort(c, P.err);
+  if (!ok && issued && lane == 0) {
+    umma_commit(&c.drain);  // wait for every MMA issued so far before TMEM is freed
+    mbar_wait(&c.drain, 0, nullptr);
+  }
+  __syncwarp();
+}
+
+// ------------------------------------------------------------------ softmax warps
+template <int GP>
+__device__ void softmax_warps(const DecodeParams& P, Ctl& c, uint8_t* stages, uint8_t* pbuf, uint32_t tmem) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wq = warp & 3;                       // TMEM lane quarter this warp may access
+  const int r = wq * 32 + lane;                  // key of the tile (S^T) / head element (O^T)
+  const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+  const int G = P.group;
+  volatile int* abort_flag = &c.abort_flag;
+  uint32_t it = 0, tc = 0, gph = 0;
+  bool ok = true;
+  while (ok) {
+    const int slot = it % kRing;
+    if (!mbar_wait(&c.item_full[slot], (it / kRing) & 1, abort_flag)) {
+      ok = false;
+      break;
+    }
+    const ItemInfo info = c.ring[slot];
+    ++it;
+    if (info.idx < 0) break;
+    if (!info.valid) {
+      // report once per request and zero what can be addressed
+      if (info.split == 0 && info.head == 0 && r == 0) flag_error(P.err, kErrLength);
+      const int64_t trow = P.qsl[info.seq];
+      if (info.split == 0 && trow >= 0 && trow < P.num_tokens && P.qsl[info.seq + 1] == trow + 1)
+        for (int g = 0; g < G; ++g)
+          P.out[(trow * P.hq + static_cast<int64_t>(info.head) * G + g) * 128 + r] = __float2bfloat16_rn(0.f);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&c.item_empty[slot]);
+      continue;
+    }
+
+    float m_run[GP], l_run[GP], acc[GP], alpha_prev[GP];
+#pragma unroll
+    for (int g = 0; g < GP; ++g) {
+      m_run[g] = -INFINITY;
+      l_run[g] = 0.f;
+      acc[g] = 0.f;
+      alpha_prev[g] = 0.f;
+    }
+    auto fold = [&](uint32_t cnt, const float (&a)[GP]) -> bool {
+      const int b = cnt & 1;
+      if (!mbar_wait(&c.o_full[b], (cnt >> 1) & 1, abort_flag)) return false;
+      tc_fence_after();
+      uint32_t o[16];
+      tmem_ld16(tmem + lane_off + 32 + 16 * b, o);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&c.o_free[b]);
+#pragma unroll
+      for (int g = 0; g < GP; ++g) acc[g] = fmaf(acc[g], a[g], __uint_as_float(o[g]));
+      return true;
+    };
+
+    const int nt = (info.key_end - info.key_start + kTileKeys - 1) / kTileKeys;
+    for (int j = 0; j < nt && ok; ++j) {
+      const int st = tc % kStages, sb = tc & 1;
+      const uint32_t ph2 = (tc >> 1) & 1;
+      const int t0 = info.key_start + j * kTileKeys;
+      // S^T lane r = logits of key t0 + r for every head of the group
+      if (!mbar_wait(&c.s_full[sb], ph2, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sraw[16];
+      tmem_ld16(tmem + lane_off + 16 * sb, sraw);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&c.s_free[sb]);
+      const bool valid_key = t0 + r < info.key_end;
+      float x[GP], tmax[GP];
+#pragma unroll
+      for (int g = 0; g < GP; ++g) {
+        x[g] = valid_key ? __uint_as_float(sraw[g]) * P.scale_log2 : -INFINITY;
+        float v = x[g];
+#pragma unroll
+        for (int sh = 16; sh > 0; sh >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, sh));
+        tmax[g] = v;
+      }
+      const int rb = gph & 1;
+      if (lane == 0) {
+#pragma unroll
+        for (int g = 0; g < GP; ++g) c.red[rb][wq][g] = tmax[g];
+      }
+      if (!group_sync(c, gph)) {
+        ok = false;
+        break;
+      }
+      float alpha[GP], p[GP];
+#pragma unroll
+      for (int g = 0; g < GP; ++g) {
+        const float mt = fmaxf(fmaxf(c.red[rb][0][g], c.red[rb][1][g]), fmaxf(c.red[rb][2][g], c.red[rb][3][g]));
+        const float m_new = fmaxf(m_run[g], mt);
+        alpha[g] = exp2f(m_run[g] - m_new);
+        p[g] = exp2f(x[g] - m_new);
+        l_run[g] = fmaf(l_run[g], alpha[g], p[g]);
+        m_run[g] = m_new;
+      }
+      // the stage's K/V have landed (needed to zero V rows of masked keys, and to
+      // order the producer's bad-block flag before it is read)
+      if (!mbar_wait(&c.full[st], (tc / kStages) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      if (!valid_key) {
+        uint8_t* vrow = stages + st * kStageBytes + kKBytes + r * 128;
+        const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int c16 = 0; c16 < 8; ++c16) {
+          *reinterpret_cast<uint4*>(vrow + c16 * 16) = z;
+          *reinterpret_cast<uint4*>(vrow + kHalfBytes + c16 * 16) = z;
+        }
+      }
+      // P^T row r (MN-major, unswizzled): heads 0-7 in one 16-byte chunk, 8-15 in another
+      const int pb = tc & 1;
+      if (!mbar_wait(&c.p_free[pb], ph2 ^ 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      {
+        float p16[16];
+#pragma unroll
+        for (int g = 0; g < 16; ++g) p16[g] = 0.f;
+#pragma unroll
+        for (int g = 0; g < GP; ++g) p16[g] = g < G ? p[g] : 0.f;
+        uint32_t w[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          __nv_bfloat162 h2 = __floats2bfloat162_rn(p16[2 * k], p16[2 * k + 1]);
+          w[k] = *reinterpret_cast<uint32_t*>(&h2);
+        }
+        uint8_t* prow = pbuf + pb * kPBytes + (r >> 3) * 128 + (r & 7) * 16;
+        *reinterpret_cast<uint4*>(prow) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(prow + 2048) = make_uint4(w[4], w[5], w[6], w[7]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&c.p_full[pb]);
+      if (j > 0 && !fold(tc - 1, alpha_prev)) {
+        ok = false;
+        break;
+      }
+#pragma unroll
+      for (int g = 0; g < GP; ++g) alpha_prev[g] = alpha[g];
+      ++tc;
+    }
+    if (!ok) break;
+    if (!fold(tc - 1, alpha_prev)) {
+      ok = false;
+      break;
+    }
+
+    // total softmax denominators: sum the per-thread partial sums over the 128 keys lanes
+    float lt[GP];
+#pragma unroll
+    for (int g = 0; g < GP; ++g) {
+      float v = l_run[g];
+#pragma unroll
+      for (int sh = 16; sh > 0; sh >>= 1) v += __shfl_xor_sync(0xffffffffu, v, sh);
+      lt[g] = v;
+    }
+    {
+      const int rb = gph & 1;
+      if (lane == 0) {
+#pragma unroll
+        for (int g = 0; g < GP; ++g) c.red[rb][wq][g] = lt[g];
+      }
+      if (!group_sync(c, gph)) {
+        ok = false;
+        break;
+      }
+#pragma unroll
+      for (int g = 0; g < GP; ++g) lt[g] = c.red[rb][0][g] + c.red[rb][1][g] + c.red[rb][2][g] + c.red[rb][3][g];
+    }
+    const bool bad = c.bad[slot] != 0;
+    const int64_t trow = P.qsl[info.seq];
+    const int64_t unit = static_cast<int64_t>(info.seq) * P.hkv + info.head;
+    __nv_bfloat16* orow = P.out + (trow * P.hq + static_cast<int64_t>(info.head) * G) * 128 + r;
+    if (info.nsplit == 1) {
+#pragma unroll
+      for (int g = 0; g < GP; ++g)
+        if (g < G) orow[g * 128] = __float2bfloat16_rn(bad ? 0.f : acc[g] / lt[g]);
+    } else {
+      float* po = P.part_o + static_cast<int64_t>(info.idx) * G * 128 + r;
+      float* pml = P.part_ml + static_cast<int64_t>(info.idx) * G * 2;
+#pragma unroll
+      for (int g = 0; g < GP; ++g) {
+        if (g < G) {
+          po[g * 128] = acc[g];
+          if (r == g) {
+            pml[2 * g] = m_run[g];
+            pml[2 * g + 1] = lt[g];
+          }
+        }
+      }
+      if (bad && r == 0) P.unit_bad[unit] = 1;
+      __threadfence();
+      if (!group_sync(c, gph)) {
+        ok = false;
+        break;
+      }
+      if (r == 0) {
+        const int old = atomicAdd(P.unit_arrive + unit, 1);
+        c.merge_flag = old == info.nsplit - 1;
+      }
+      if (!group_sync(c, gph)) {
+        ok = false;
+        break;
+      }
+      if (c.merge_flag) {
+        __threadfence();
+        const bool any_bad = *reinterpret_cast<volatile int*>(P.unit_bad + unit) != 0;
+        const int64_t base = info.idx - info.split;
+        for (int g = 0; g < G; ++g) {
+          float M = -INFINITY;
+          for (int s = 0; s < info.nsplit; ++s) M = fmaxf(M, __ldcg(P.part_ml + ((base + s) * G + g) * 2));
+          float num = 0.f, den = 0.f;
+          for (int s = 0; s < info.nsplit; ++s) {
+            const float f = exp2f(__ldcg(P.part_ml + ((base + s) * G + g) * 2) - M);
+            den = fmaf(__ldcg(P.part_ml + ((base + s) * G + g) * 2 + 1), f, den);
+            num = fmaf(__ldcg(P.part_o + ((base + s) * G + g) * 128 + r), f, num);
+          }
+          orow[g * 128] = __float2bfloat16_rn(any_bad ? 0.f : num / den);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&c.item_empty[slot]);
+  }
+  if (!ok && !*abort_flag && lane == 0) raise_abort(c, P.err);
+}
+
+template <int GP>
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ CUtensorMap kmap,
+                                                             const __grid_constant__ CUtensorMap vmap,
+                                                             const DecodeParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* base = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  uint8_t* stages = base;
+  uint8_t* qbuf = stages + kStages * kStageBytes;
+  uint8_t* pbuf = qbuf + 2 * kQBytes;
+  Ctl& c = *reinterpret_cast<Ctl*>(pbuf + 2 * kPBytes);
+  const int warp = threadIdx.x >> 5;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&c.full[s], 1);
+      mbar_init(&c.empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&c.s_full[b], 1);
+      mbar_init(&c.s_free[b], 4);
+      mbar_init(&c.p_full[b], 4);
+      mbar_init(&c.p_free[b], 1);
+      mbar_init(&c.o_full[b], 1);
+      mbar_init(&c.o_free[b], 4);
+      mbar_init(&c.q_full[b], 1);
+      mbar_init(&c.q_free[b], 1);
+    }
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(&c.item_full[s], 1);
+      mbar_init(&c.item_empty[s], 5);
+    }
+    mbar_init(&c.drain, 1);
+    mbar_init(&c.group_bar, 4);
+    c.abort_flag = 0;
+    c.merge_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_map(&kmap);
+    tma_prefetch_map(&vmap);
+  }
+  // zero Q (padding rows stay zero) and P^T buffers
+  for (int i = threadIdx.x; i < (2 * kQBytes + 2 * kPBytes) / 16; i += kThreads)
+    reinterpret_cast<uint4*>(qbuf)[i] = make_uint4(0, 0, 0, 0);
+  fence_proxy_async_smem();
+  if (warp == 1) tmem_alloc(&c.tmem_base, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = c.tmem_base;
+
+  if (warp == 0) producer_warp(P, &kmap, &vmap, c, stages, qbuf);
+  else if (warp == 1) mma_warp(P, c, stages, qbuf, pbuf, tmem);
+  else softmax_warps<GP>(P, c, stages, pbuf, tmem);
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+    tmem_relinquish();
+  }
+}
+
+template <int GP>
+int launch_gp(const CUtensorMap& km, const CUtensorMap& vm, const DecodeParams& p, int grid, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<GP>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return cuda_status(e);
+  decode_kernel<GP><<<grid, kThreads, kSmemBytes, s>>>(km, vm, p);
+  return cuda_status(cudaGetLastError());
+}
+
+}  // namespace
+
+int launch_decode_tc(const AttnArgs& a, const Workspace& ws, int num_sms, uint32_t* err, cudaStream_t s) {
+  const int hkv = a.cache.num_kv_heads;
+  const int group = a.num_q_heads / hkv;
+  if (group > 16 || a.cache.head_dim != 128 || a.cache.dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+  const uint64_t rows = static_cast<uint64_t>(a.cache.num_blocks) * hkv * kBlock;
+  if (rows >= (1ull << 31)) return PKV_ERR_UNSUPPORTED;
+  CUtensorMap km, vm;
+  int st = encode_tensor_map_2d(&km, a.k_cache, 128, rows, 256, 64, 16);
+  if (st) return st;
+  st = encode_tensor_map_2d(&vm, a.v_cache, 128, rows, 256, 64, 16);
+  if (st) return st;
+  DecodeParams p;
+  p.q = static_cast<const __nv_bfloat16*>(a.q);
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.bt = a.block_tables;
+  p.seq_lens = a.seq_lens;
+  p.qsl = a.qsl;
+  p.dec_prefix = ws.dec_prefix;
+  p.queue = ws.counters + 0;
+  p.unit_arrive = ws.unit_arrive;
+  p.unit_bad = ws.unit_bad;
+  p.part_o = ws.part_o;
+  p.part_ml = ws.part_ml;
+  p.err = err;
+  p.num_blocks = a.cache.num_blocks;
+  p.num_tokens = a.num_tokens;
+  p.num_seqs = a.num_seqs;
+  p.max_blocks = a.max_blocks;
+  p.hkv = hkv;
+  p.group = group;
+  p.hq = a.num_q_heads;
+  p.split_keys = kSplitKeys;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  TraceScope trace(kTraceDecode, s);
+  if (group <= 4) return launch_gp<4>(km, vm, p, num_sms, s);
+  if (group <= 8) return launch_gp<8>(km, vm, p, num_sms, s);
+  return launch_gp<16>(km, vm, p, num_sms, s);
+}
+
+}  // namespace pkv

@@ -25,7 +25,8 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kGenThreads) generic_attention_kernel(
     const T* __restrict__ q, const T* __restrict__ kc, const T* __restrict__ vc, int64_t num_blocks, int hkv,
     const int32_t* __restrict__ bt, int32_t max_blocks, const int32_t* __restrict__ seq_lens,
-    const int32_t* __restrict__ qsl, int num_seqs, int hq, float scale_log2, T* __restrict__ out, uint32_t* err) {
+    const int32_t* __restrict__ qsl, int num_seqs, int hq, float scale_log2, T* __restrict__ out, uint32_t* err,
+    int prefill_only) {
   constexpr int E = D / 32;
   __shared__ int bad;
   __shared__ float sm_m[kGenWarps][kHeadChunk];
@@ -47,6 +48,7 @@ __global__ void __launch_bounds__(kGenThreads) generic_attention_kernel(
   const int64_t q0 = __ldg(qsl + i), q1 = __ldg(qsl + i + 1);
   const int64_t L = __ldg(seq_lens + i);
   const int64_t p = L - (q1 - q0) + (t - q0);
+  if (prefill_only && q1 - q0 == 1 && t == q0) return;  // decode rows belong to the decode kernel
   if (threadIdx.x == 0) bad = 0;
   __syncthreads();
   const bool len_ok = t >= q0 && t < q1 && p >= 0 && (L + kBlock - 1) / kBlock <= max_blocks;
@@ -140,7 +142,7 @@ __global__ void __launch_bounds__(kGenThreads) generic_attention_kernel(
 }
 
 template <typename T, int D>
-int launch_typed(const AttnArgs& a, uint32_t* err, cudaStream_t s) {
+int launch_typed(const AttnArgs& a, uint32_t* err, cudaStream_t s, bool prefill_only) {
   const int hkv = a.cache.num_kv_heads;
   const int group = a.num_q_heads / hkv;
   const int nchunks = (group + kHeadChunk - 1) / kHeadChunk;
@@ -149,21 +151,21 @@ int launch_typed(const AttnArgs& a, uint32_t* err, cudaStream_t s) {
   generic_attention_kernel<T, D><<<static_cast<unsigned>(blocks), kGenThreads, 0, s>>>(
       static_cast<const T*>(a.q), static_cast<const T*>(a.k_cache), static_cast<const T*>(a.v_cache),
       a.cache.num_blocks, hkv, a.block_tables, a.max_blocks, a.seq_lens, a.qsl, a.num_seqs, a.num_q_heads,
-      a.scale * kLog2e, static_cast<T*>(a.out), err);
+      a.scale * kLog2e, static_cast<T*>(a.out), err, prefill_only ? 1 : 0);
   return cuda_status(cudaGetLastError());
 }
 
 }  // namespace
 
-int launch_generic_attention(const AttnArgs& a, uint32_t* err, cudaStream_t s) {
+int launch_generic_attention(const AttnArgs& a, uint32_t* err, cudaStream_t s, bool prefill_only) {
   if (a.num_tokens == 0) return PKV_OK;
   TraceScope trace(kTraceGeneric, s);
   const int d = a.cache.head_dim;
   if (a.cache.dtype == PKV_F32) {
-    if (d == 64) return launch_typed<float, 64>(a, err, s);
-    if (d == 128) return launch_typed<float, 128>(a, err, s);
+    if (d == 64) return launch_typed<float, 64>(a, err, s, prefill_only);
+    if (d == 128) return launch_typed<float, 128>(a, err, s, prefill_only);
   } else if (a.cache.dtype == PKV_BF16) {
-    if (d == 128) return launch_typed<__nv_bfloat16, 128>(a, err, s);
+    if (d == 128) return launch_typed<__nv_bfloat16, 128>(a, err, s, prefill_only);
   }
   return PKV_ERR_UNSUPPORTED;
 }

@@ -1,0 +1,565 @@
+// k_prefill.cu -- causal varlen chunked prefill on tcgen05 tensor cores (bf16, head_dim 128).
+//
+// What it computes ("vLLM's PagedAttention" teardown, section "Continuous
+// batching": a long prompt is split across steps by chunked prefill; a chunk
+// attends to its cached prior context and, causally, to itself).  For a request
+// with q_len query tokens and context seq_len, query j sits at position
+// seq_len - q_len + j and sees keys 0..that position, gathered through the block
+// table like the decode path.
+//
+// Work decomposition.  The G query heads that share a kv head are folded into the
+// 128 rows of one MMA tile: R = 128 / GP queries x GP heads (GP = G rounded up to
+// 4, 8 or 16), row r <-> (query j0 + r / GP, head r % GP).  One K/V tile then feeds
+// the whole group.  Items (request, kv head, query tile), heaviest query tiles of a
+// request first, come from an atomic queue to persistent CTAs, one per SM.
+//
+// Per CTA (192 threads):
+//   warp 0     producer: TMA-loads the Q tile (a 3-D box over [token][head][dim])
+//              and, per 128-key tile, 4 boxes per 16-token block from the block's
+//              physical location (the block-table gather), 128-byte swizzle.
+//   warp 1     MMA issuer: S = Q K^T (M = 128 rows, N = 128 keys) into one of two
+//              TMEM buffers, then O += P V into a TMEM accumulator, V read MN-major.
+//   warps 2-5  softmax: thread r owns row r.  It loads its S row from TMEM, applies
+//              the causal mask, and keeps a per-row reference maximum; only when a
+//              row's maximum grows by more than 2^8 does the warp rescale its O rows
+//              in TMEM (after the previous P V has landed).  P is written as bf16 into
+//              a swizzled K-major operand.  The final O / l is stored per row.
+// All waits are bounded (see ptx.cuh); a timeout raises the CTA abort flag.
+#include "ptx.cuh"
+#include "pkv_internal.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kStages = 2;
+constexpr int kHalfBytes = 16384;          // 128 rows x 128 B
+constexpr int kTileBytes = 2 * kHalfBytes;  // 128 x 128 bf16, K-major, two 64-column halves
+constexpr int kStageBytes = 2 * kTileBytes; // K tile + V tile
+constexpr int kRing = 4;
+constexpr uint32_t kTmemCols = 512;         // S x2 (cols 0, 128), O (col 256)
+constexpr uint32_t kOCol = 256;
+constexpr int kBlocksPerTile = kTileKeys / kBlock;
+constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale O when a row max grows by > 2^8
+
+struct alignas(16) PItem {
+  int32_t idx;  // -1: queue exhausted
+  int32_t seq, head, qt;
+  int32_t q_len, ctx, j0, nq;
+  int32_t nt, valid, t0, kend;
+};
+
+struct Ctl {
+  uint64_t full[kStages], empty[kStages];
+  uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
+  uint64_t o_full, o_free;
+  uint64_t q_full, q_free;
+  uint64_t item_full[kRing], item_empty[kRing];
+  uint64_t drain;
+  PItem ring[kRing];
+  int bad[kRing];
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+constexpr int kSmemBytes = kTileBytes /*Q*/ + kStages * kStageBytes + 2 * kTileBytes /*P x2*/ +
+                           static_cast<int>(sizeof(Ctl)) + 1024;
+static_assert(kSmemBytes <= 232448, "prefill shared memory");
+
+struct PrefillParams {
+  __nv_bfloat16* out;
+  const int32_t* bt;
+  const int32_t* seq_lens;
+  const int32_t* qsl;
+  const int32_t* pre_prefix;
+  int32_t* queue;
+  uint32_t* err;
+  int64_t num_blocks;
+  int64_t num_tokens;
+  int32_t num_seqs, max_blocks, hkv, group, gp, rows_q, hq;
+  float scale_log2;
+};
+
+__device__ __forceinline__ void raise_abort(Ctl& c, uint32_t* err) {
+  *reinterpret_cast<volatile int*>(&c.abort_flag) = 1;
+  flag_error(err, kErrTimeout);
+}
+
+__device__ PItem make_item(const PrefillParams& P, int idx, int total) {
+  PItem r{};
+  if (idx >= total) {
+    r.idx = -1;
+    return r;
+  }
+  int lo = 0, hi = P.num_seqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (P.pre_prefix[mid] <= idx) lo = mid; else hi = mid - 1;
+  }
+  const int i = lo;
+  const int base = P.pre_prefix[i];
+  const int cnt = P.pre_prefix[i + 1] - base;
+  const int nqt = cnt / P.hkv;
+  r.idx = idx;
+  r.seq = i;
+  if (nqt <= 0) return r;  // inconsistent plan: invalid item
+  const int local = idx - base;
+  r.qt = nqt - 1 - local / P.hkv;  // heaviest (latest) query tiles first
+  r.head = local % P.hkv;
+  const int64_t q0 = P.qsl[i], q1 = P.qsl[i + 1];
+  const int64_t L = P.seq_lens[i];
+  const int64_t q_len = q1 - q0;
+  r.q_len = static_cast<int32_t>(q_len);
+  r.t0 = static_cast<int32_t>(q0);
+  r.j0 = r.qt * P.rows_q;
+  const int64_t left = q_len - r.j0;
+  r.nq = static_cast<int32_t>(left < P.rows_q ? left : P.rows_q);
+  const bool ok = q_len > 1 && L >= q_len && (L + kBlock - 1) / kBlock <= P.max_blocks && q0 >= 0 &&
+                  q1 <= P.num_tokens && (q_len + P.rows_q - 1) / P.rows_q == nqt && r.nq > 0;
+  r.valid = ok ? 1 : 0;
+  if (ok) {
+    r.ctx = static_cast<int32_t>(L - q_len);
+    r.kend = r.ctx + r.j0 + r.nq;  // keys [0, kend) are visible to some row of the tile
+    r.nt = (r.kend + kTileKeys - 1) / kTileKeys;
+  }
+  return r;
+}
+
+// ------------------------------------------------------------------ producer warp
+__device__ void producer_warp(const PrefillParams& P, const CUtensorMap* qmap, const CUtensorMap* kmap,
+                              const CUtensorMap* vmap, Ctl& c, uint8_t* qbuf, uint8_t* stages) {
+  const int lane = threadIdx.x & 31;
+  const int total = P.pre_prefix[P.num_seqs];
+  volatile int* abort_flag = &c.abort_flag;
+  uint32_t it = 0, tc = 0, qc = 0;
+  bool ok = true;
+  while (ok) {
+    const int slot = it % kRing;
+    if (!mbar_wait(&c.item_empty[slot], ((it / kRing) & 1) ^ 1, abort_flag)) {
+      ok = false;
+      break;
+    }
+    if (lane == 0) {
+      const int idx = atomicAdd(P.queue, 1);
+      c.ring[slot] = make_item(P, idx, total);
+      c.bad[slot] = 0;
+      mbar_arrive(&c.item_full[slot]);
+    }
+    __syncwarp();
+    const PItem info = c.ring[slot];
+    ++it;
+    if (info.idx < 0) break;
+    if (!info.valid) continue;
+    if (!mbar_wait(&c.q_free, (qc & 1) ^ 1, abort_flag)) {
+      ok = false;
+      break;
+    }
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&c.q_full, kTileBytes);
+      const int32_t y = info.head * P.group, z = info.t0 + info.j0;
+      tma_load_3d(qbuf, qmap, &c.q_full, 0, y, z, l2_policy_evict_first());
+      tma_load_3d(qbuf + kHalfBytes, qmap, &c.q_full, 64, y, z, l2_policy_evict_first());
+    }
+    ++qc;
+    const int32_t* btrow = P.bt + static_cast<int64_t>(info.seq) * P.max_blocks;
+    for (int j = 0; j < info.nt; ++j) {
+      const int st = tc % kStages;
+      if (!mbar_wait(&c.empty[st], ((tc / kStages) & 1) ^ 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      const int t0 = j * kTileKeys;
+      const int nblk = min(kBlocksPerTile, (info.kend - t0 + kBlock - 1) / kBlock);
+      int id = 0;
+      bool bad = false;
+      if (lane < nblk) {
+        id = __ldg(btrow + t0 / kBlock + lane);
+        if (id < 0 || id >= P.num_blocks) {
+          bad = true;
+          id = 0;
+        }
+      }
+      if (__any_sync(0xffffffffu, bad)) {
+        if (bad) flag_error(P.err, kErrBlockId);
+        if (lane == 0) c.bad[slot] = 1;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(&c.full[st], static_cast<uint32_t>(nblk) * 8192u);
+      __syncwarp();
+      if (lane < nblk) {
+        uint8_t* s = stages + st * kStageBytes + lane * 2048;
+        const int32_t row = (id * P.hkv + info.head) * kBlock;
+        tma_load_2d(s, kmap, &c.full[st], 0, row);
+        tma_load_2d(s + kHalfBytes, kmap, &c.full[st], 64, row);
+        tma_load_2d(s + kTileBytes, vmap, &c.full[st], 0, row);
+        tma_load_2d(s + kTileBytes + kHalfBytes, vmap, &c.full[st], 64, row);
+      }
+      ++tc;
+    }
+  }
+  if (!ok && !*abort_flag && lane == 0) raise_abort(c, P.err);
+  if (*abort_flag) {
+    const uint32_t first = tc > static_cast<uint32_t>(kStages) ? tc - kStages : 0;
+    for (uint32_t cnt = first; cnt < tc; ++cnt) mbar_wait(&c.full[cnt % kStages], (cnt / kStages) & 1, nullptr);
+    if (qc > 0) mbar_wait(&c.q_full, (qc - 1) & 1, nullptr);
+  }
+}
+
+// ------------------------------------------------------------------ MMA warp
+__device__ void mma_warp(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uint8_t* stages, uint8_t* pbuf,
+                         uint32_t tmem) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t idesc_s = umma_idesc_bf16(128, 128, false, false);
+  const uint32_t idesc_o = umma_idesc_bf16(128, 128, false, true);
+  volatile int* abort_flag = &c.abort_flag;
+  uint32_t it = 0, tc = 0, qc = 0, ic = 0;
+  bool issued = false, ok = true;
+
+  // O (+)= P_j V_j for tile counter cnt; `first` starts the accumulator of an item
+  auto pv = [&](uint32_t cnt, bool first) -> bool {
+    const int st = cnt % kStages, b = cnt & 1;
+    if (!mbar_wait(&c.p_full[b], (cnt >> 1) & 1, abort_flag)) return false;
+    // the previous item's O must have been read out before its accumulator restarts
+    if (first && !mbar_wait(&c.o_free, (ic & 1) ^ 1, abort_flag)) return false;
+    tc_fence_after();
+    if (lane == 0) {
+      const uint64_t a = umma_smem_desc(smem_u32(pbuf + b * kTileBytes), 16, 1024, kLayout128B);
+      const uint64_t bd = umma_smem_desc(smem_u32(stages + st * kStageBytes + kTileBytes), kHalfBytes, 1024,
+                                         kLayout128B);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        umma_f16_ss(tmem + kOCol, umma_desc_advance(a, (kk >> 2) * kHalfBytes + (kk & 3) * 32),
+                    umma_desc_advance(bd, kk * 2048), idesc_o, (!first || kk > 0) ? 1u : 0u);
+      umma_commit(&c.o_full);
+      umma_commit(&c.p_free[b]);
+      umma_commit(&c.empty[st]);
+    }
+    __syncwarp();
+    return true;
+  };
+
+  while (ok) {
+    const int slot = it % kRing;
+    if (!mbar_wait(&c.item_full[slot], (it / kRing) & 1, abort_flag)) {
+      ok = false;
+      break;
+    }
+    const PItem info = c.ring[slot];
+    ++it;
+    if (info.idx < 0) break;
+    if (info.valid) {
+      if (!mbar_wait(&c.q_full, qc & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      for (int j = 0; j < info.nt && ok; ++j) {
+        const int st = tc % kStages, sb = tc & 1;
+        if (!mbar_wait(&c.full[st], (tc / kStages) & 1, abort_flag) ||
+            !mbar_wait(&c.s_free[sb], ((tc >> 1) & 1) ^ 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint64_t a = umma_smem_desc(smem_u32(qbuf), 16, 1024, kLayout128B);
+          const uint64_t b = umma_smem_desc(smem_u32(stages + st * kStageBytes), 16, 1024, kLayout128B);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+            umma_f16_ss(tmem + 128 * sb, umma_desc_advance(a, off), umma_desc_advance(b, off), idesc_s, kk > 0);
+          }
+          umma_commit(&c.s_full[sb]);
+          if (j == info.nt - 1) umma_commit(&c.q_free);
+          issued = true;
+        }
+        __syncwarp();
+        if (j > 0 && !pv(tc - 1, j == 1)) ok = false;
+        ++tc;
+      }
+      if (ok && !pv(tc - 1, info.nt == 1)) ok = false;
+      ++qc;
+      ++ic;
+    }
+    if (!ok) break;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&c.item_empty[slot]);
+  }
+  if (!ok && !*abort_flag && lane == 0) raise_abort(c, P.err);
+  if (!ok && issued && lane == 0) {
+    umma_commit(&c.drain);
+    mbar_wait(&c.drain, 0, nullptr);
+  }
+  __syncwarp();
+}
+
+// ------------------------------------------------------------------ softmax warps
+__device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* stages, uint8_t* pbuf, uint32_t tmem) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wq = warp & 3;
+  const int r = wq * 32 + lane;  // tile row
+  const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+  volatile int* abort_flag = &c.abort_flag;
+  uint32_t it = 0, tc = 0;
+  bool ok = true;
+  const int rj = r / P.gp, rg = r % P.gp;  // query offset and head of this row within a tile
+
+  while (ok) {
+    const int slot = it % kRing;
+    if (!mbar_wait(&c.item_full[slot], (it / kRing) & 1, abort_flag)) {
+      ok = false;
+      break;
+    }
+    const PItem info = c.ring[slot];
+    ++it;
+    if (info.idx < 0) break;
+    const int j_row = info.j0 + rj;
+    const bool row_out = info.nq > 0 && rj < info.nq && rg < P.group;  // a real (token, head) row
+    __nv_bfloat16* orow = P.out + ((static_cast<int64_t>(info.t0) + j_row) * P.hq +
+                                   static_cast<int64_t>(info.head) * P.group + rg) * 128;
+    if (!info.valid) {
+      if (r == 0 && info.head == 0) flag_error(P.err, kErrLength);
+      const int64_t q0 = P.qsl[info.seq], q1 = P.qsl[info.seq + 1];
+      const int jj = info.qt * P.rows_q + rj;
+      if (q0 >= 0 && q1 <= P.num_tokens && q0 + jj < q1 && rg < P.group) {
+        __nv_bfloat16* zrow = P.out + ((q0 + jj) * P.hq + static_cast<int64_t>(info.head) * P.group + rg) * 128;
+        for (int k = 0; k < 16; ++k) reinterpret_cast<uint4*>(zrow)[k] = make_uint4(0, 0, 0, 0);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&c.item_empty[slot]);
+      continue;
+    }
+    // causal bound of this row (padding rows borrow the last real query's bound)
+    const int pos = info.ctx + min(j_row, info.q_len - 1);
+    const int L = info.ctx + info.q_len;
+    // V rows from here on are either past the context or not loaded this item:
+    // they are zeroed so that 0-weight keys cannot carry non-finite bytes into P V
+    const int zero_from = min(L, ((info.kend + kBlock - 1) / kBlock) * kBlock);
+    float m_ref = -INFINITY, l_sum = 0.f;
+
+    for (int j = 0; j < info.nt && ok; ++j) {
+      const int st = tc % kStages, sb = tc & 1, pb = tc & 1;
+      const int k0 = j * kTileKeys;
+      if (!mbar_wait(&c.s_full[sb], (tc >> 1) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float s[128];
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        uint32_t v[16];
+        tmem_ld16(tmem + lane_off + 128 * sb + 16 * ch, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < 16; ++k) s[16 * ch + k] = __uint_as_float(v[k]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&c.s_free[sb]);
+      float tmax = -INFINITY;
+      const int nvis = pos - k0 + 1;  // keys k0 .. k0 + nvis - 1 are visible to this row
+#pragma unroll
+      for (int k = 0; k < 128; ++k) {
+        s[k] = k < nvis ? s[k] * P.scale_log2 : -INFINITY;
+        tmax = fmaxf(tmax, s[k]);
+      }
+      if (j == 0) {
+        m_ref = tmax;  // key 0 is visible to every row, so this is finite
+      } else {
+        const bool need = tmax > m_ref + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {
+          // rescale this warp's O rows once the previous P V has landed
+          if (!mbar_wait(&c.o_full, (tc - 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const float m_new = need ? tmax : m_ref;
+          const float alpha = exp2f(m_ref - m_new);
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {
+            uint32_t v[16];
+            tmem_ld16(tmem + lane_off + kOCol + 16 * ch, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int k = 0; k < 16; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
+            tmem_st16(tmem + lane_off + kOCol + 16 * ch, v);
+          }
+          tmem_st_wait();
+          l_sum *= alpha;
+          m_ref = m_new;
+        }
+      }
+      // K/V of this stage have landed (also orders the producer's bad-block flag)
+      if (!mbar_wait(&c.full[st], (tc / kStages) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      if (k0 + r >= zero_from) {
+        uint8_t* vrow = stages + st * kStageBytes + kTileBytes + r * 128;
+#pragma unroll
+        for (int c16 = 0; c16 < 8; ++c16) {
+          *reinterpret_cast<uint4*>(vrow + c16 * 16) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(vrow + kHalfBytes + c16 * 16) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      if (!mbar_wait(&c.p_free[pb], ((tc >> 1) & 1) ^ 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      uint8_t* prow = pbuf + pb * kTileBytes + r * 128;
+#pragma unroll
+      for (int kc = 0; kc < 16; ++kc) {
+        uint32_t w[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float a = exp2f(s[8 * kc + 2 * q] - m_ref);
+          const float b = exp2f(s[8 * kc + 2 * q + 1] - m_ref);
+          l_sum += a + b;
+          __nv_bfloat162 h2 = __floats2bfloat162_rn(a, b);
+          w[q] = *reinterpret_cast<uint32_t*>(&h2);
+        }
+        const int half = kc >> 3, c8 = kc & 7;
+        *reinterpret_cast<uint4*>(prow + half * kHalfBytes + ((c8 ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&c.p_full[pb]);
+      ++tc;
+    }
+    if (!ok) break;
+    // final O of the item
+    if (!mbar_wait(&c.o_full, (tc - 1) & 1, abort_flag)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    const bool bad = c.bad[slot] != 0;
+    const float inv = bad ? 0.f : 1.f / l_sum;
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {
+      uint32_t v[16];
+      tmem_ld16(tmem + lane_off + kOCol + 16 * ch, v);
+      tmem_ld_wait();
+      if (row_out) {
+        uint32_t w[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(v[2 * q]) * inv, __uint_as_float(v[2 * q + 1]) * inv);
+          w[q] = *reinterpret_cast<uint32_t*>(&h2);
+        }
+        reinterpret_cast<uint4*>(orow)[2 * ch] = make_uint4(w[0], w[1], w[2], w[3]);
+        reinterpret_cast<uint4*>(orow)[2 * ch + 1] = make_uint4(w[4], w[5], w[6], w[7]);
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(&c.o_free);
+      mbar_arrive(&c.item_empty[slot]);
+    }
+  }
+  if (!ok && !*abort_flag && lane == 0) raise_abort(c, P.err);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap qmap,
+                                                              const __grid_constant__ CUtensorMap kmap,
+                                                              const __grid_constant__ CUtensorMap vmap,
+                                                              const PrefillParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* base = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  uint8_t* qbuf = base;
+  uint8_t* stages = qbuf + kTileBytes;
+  uint8_t* pbuf = stages + kStages * kStageBytes;
+  Ctl& c = *reinterpret_cast<Ctl*>(pbuf + 2 * kTileBytes);
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&c.full[s], 1);
+      mbar_init(&c.empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&c.s_full[b], 1);
+      mbar_init(&c.s_free[b], 4);
+      mbar_init(&c.p_full[b], 4);
+      mbar_init(&c.p_free[b], 1);
+    }
+    mbar_init(&c.o_full, 1);
+    mbar_init(&c.o_free, 4);
+    mbar_init(&c.q_full, 1);
+    mbar_init(&c.q_free, 1);
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(&c.item_full[s], 1);
+      mbar_init(&c.item_empty[s], 5);
+    }
+    mbar_init(&c.drain, 1);
+    c.abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_map(&qmap);
+    tma_prefetch_map(&kmap);
+    tma_prefetch_map(&vmap);
+  }
+  if (warp == 1) tmem_alloc(&c.tmem_base, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = c.tmem_base;
+  if (warp == 0) producer_warp(P, &qmap, &kmap, &vmap, c, qbuf, stages);
+  else if (warp == 1) mma_warp(P, c, qbuf, stages, pbuf, tmem);
+  else softmax_warps(P, c, stages, pbuf, tmem);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+    tmem_relinquish();
+  }
+}
+
+}  // namespace
+
+int launch_prefill_tc(const AttnArgs& a, const Workspace& ws, int num_sms, uint32_t* err, cudaStream_t s) {
+  const int hkv = a.cache.num_kv_heads;
+  const int group = a.num_q_heads / hkv;
+  if (group > 16 || a.cache.head_dim != 128 || a.cache.dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+  const int gp = group <= 4 ? 4 : (group <= 8 ? 8 : 16);
+  const uint64_t rows = static_cast<uint64_t>(a.cache.num_blocks) * hkv * kBlock;
+  if (rows >= (1ull << 31) || a.num_tokens >= (int64_t(1) << 31)) return PKV_ERR_UNSUPPORTED;
+  CUtensorMap qm, km, vm;
+  int st = encode_tensor_map_2d(&km, a.k_cache, 128, rows, 256, 64, 16);
+  if (st) return st;
+  st = encode_tensor_map_2d(&vm, a.v_cache, 128, rows, 256, 64, 16);
+  if (st) return st;
+  const uint64_t qdims[3] = {128, static_cast<uint64_t>(a.num_q_heads), static_cast<uint64_t>(a.num_tokens)};
+  const uint64_t qstrides[2] = {256, static_cast<uint64_t>(a.num_q_heads) * 256};
+  const uint32_t qbox[3] = {64, static_cast<uint32_t>(gp), static_cast<uint32_t>(kTileKeys / gp)};
+  st = encode_tensor_map_3d(&qm, a.q, qdims, qstrides, qbox);
+  if (st) return st;
+  PrefillParams p;
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.bt = a.block_tables;
+  p.seq_lens = a.seq_lens;
+  p.qsl = a.qsl;
+  p.pre_prefix = ws.pre_prefix;
+  p.queue = ws.counters + 1;
+  p.err = err;
+  p.num_blocks = a.cache.num_blocks;
+  p.num_tokens = a.num_tokens;
+  p.num_seqs = a.num_seqs;
+  p.max_blocks = a.max_blocks;
+  p.hkv = hkv;
+  p.group = group;
+  p.gp = gp;
+  p.rows_q = kTileKeys / gp;
+  p.hq = a.num_q_heads;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  TraceScope trace(kTracePrefill, s);
+  cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return cuda_status(e);
+  prefill_kernel<<<num_sms, kThreads, kSmemBytes, s>>>(qm, km, vm, p);
+  return cuda_status(cudaGetLastError());
+}
+
+}  // namespace pkv

@@ -120,9 +120,6 @@ int run_umma_selftest(const int32_t* params, const void* a_img, const void* b_im
   return cuda_status(cudaGetLastError());
 }
 
-int encode_tensor_map_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
-                         uint32_t box_inner, uint32_t box_outer);
-
 int run_tma_selftest(const void* src, int64_t rows, int32_t row0, void* dump, uint32_t* err, cudaStream_t s) {
   if (rows < 16 || row0 < 0 || row0 + 16 > rows) return PKV_ERR_INVALID_ARG;
   CUtensorMap map;

@@ -1,5 +1,6 @@
 // pkv_internal.cuh -- definitions shared by the library's translation units.
 #pragma once
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cstdint>
@@ -17,6 +18,10 @@ enum : uint32_t {
   kErrLength = 1u << 2,    // seq_len < q_len, or more blocks than a table row holds
   kErrTimeout = 1u << 3,   // a bounded wait gave up
 };
+
+constexpr int kTileKeys = 128;       // keys per tensor-core tile (8 blocks)
+constexpr int kSplitKeys = 1024;     // decode key-split length (a multiple of kTileKeys)
+constexpr int kNumQueueCounters = 8; // work-queue counters in the workspace
 
 // Trace kinds (pkv_trace_read).
 enum TraceKind : int {
@@ -110,7 +115,48 @@ struct AttnArgs {
   float scale;
   void* out;
 };
-int launch_generic_attention(const AttnArgs& a, uint32_t* err, cudaStream_t s);
+// prefill_only: skip the rows of requests with exactly one query token.
+int launch_generic_attention(const AttnArgs& a, uint32_t* err, cudaStream_t s, bool prefill_only = false);
+
+// Per-call workspace carved from the library-owned device buffer.
+struct Workspace {
+  int32_t* counters;     // [kNumQueueCounters] work-queue heads
+  int32_t* dec_prefix;   // [num_seqs + 1] exclusive prefix of decode items
+  int32_t* pre_prefix;   // [num_seqs + 1] exclusive prefix of prefill items
+  int32_t* unit_arrive;  // [num_seqs * hkv] split arrivals per (request, kv head)
+  int32_t* unit_bad;     // [num_seqs * hkv] a split saw a bad block id
+  float* part_ml;        // [max_dec_items * G * 2] split running max and sum
+  float* part_o;         // [max_dec_items * G * head_dim] split accumulators
+};
+// Computes the layout at `base` (nullptr: only the size) and returns the bytes needed.
+size_t layout_workspace(void* base, int32_t num_seqs, int32_t hkv, int32_t group, int32_t head_dim,
+                        int64_t max_dec_items, Workspace* ws);
+
+struct PlanArgs {
+  const int32_t* seq_lens;
+  const int32_t* qsl;
+  int32_t num_seqs;
+  int64_t num_tokens;
+  int32_t hkv;
+  int32_t max_blocks;
+  int64_t max_seq_len;
+  int32_t split_keys;
+  int32_t rows_per_tile;
+  int32_t* counters;
+  int32_t* dec_prefix;
+  int32_t* pre_prefix;
+  int32_t* unit_arrive;
+  int32_t* unit_bad;
+  uint32_t* err;
+};
+int launch_plan(const PlanArgs& p, cudaStream_t s);
+int launch_decode_tc(const AttnArgs& a, const Workspace& ws, int num_sms, uint32_t* err, cudaStream_t s);
+int launch_prefill_tc(const AttnArgs& a, const Workspace& ws, int num_sms, uint32_t* err, cudaStream_t s);
+int encode_tensor_map_3d(CUtensorMap* map, const void* base, const uint64_t dims[3], const uint64_t strides[2],
+                         const uint32_t box[3]);
+
+int encode_tensor_map_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                         uint32_t box_inner, uint32_t box_outer);
 
 int run_umma_selftest(const int32_t* params, const void* a_img, const void* b_img, float* d_out, uint32_t* err,
                       cudaStream_t s);
