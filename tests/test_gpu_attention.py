@@ -73,6 +73,26 @@ def test_prefill_edge_lengths_bf16(pkv, lens, qs):
     run_pair(pkv, w)
 
 
+@pytest.mark.parametrize("scale", [0.3, 1.0])
+def test_prefill_rescale_path_bf16(pkv, scale):
+    # a large logit scale makes row maxima jump between key tiles, so the prefill
+    # kernel's conditional rescale of the TMEM accumulator runs many times
+    w = wl.sized_case(24, [900, 700, 130], [300, 200, 129], 32, 8, 128, "bf16", scale=scale)
+    run_pair(pkv, w)
+
+
+@pytest.mark.parametrize("group,hkv", [(1, 8), (2, 4), (3, 2), (4, 8), (5, 1), (8, 2), (16, 1)])
+def test_prefill_head_folding_bf16(pkv, group, hkv):
+    # G heads folded into the 128 tile rows (R = 128 / GP queries); G below GP leaves padding rows
+    w = wl.sized_case(25, [777, 64, 300], [333, 17, 300], group * hkv, hkv, 128, "bf16")
+    run_pair(pkv, w)
+
+
+def test_decode_large_scale_bf16(pkv):
+    w = wl.sized_case(26, [3000, 2049, 77], [1, 1, 1], 64, 8, 128, "bf16", scale=0.5)
+    run_pair(pkv, w)
+
+
 def test_request_without_query_tokens(pkv):
     # a request that contributes no tokens this step is skipped; its neighbours are not disturbed
     w = wl.sized_case(23, [50, 70, 90], [3, 0, 1], 8, 2, 128, "bf16")
