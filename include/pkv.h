@@ -147,6 +147,35 @@ PKV_API int paged_attention(const void* q, const void* k_cache, const void* v_ca
                     const int32_t* query_start_loc, int32_t num_seqs, int32_t num_q_heads, int64_t num_tokens,
                     int32_t max_query_len, int32_t max_seq_len, float scale, void* out, void* stream);
 
+/*
+ * paged_attention_noalloc -- paged_attention() for callers that cannot let a library
+ * allocate device memory.  The pages have no counterpart for this call; it exists
+ * for deployment.  paged_attention() grows a workspace with cudaMalloc when a batch
+ * needs more split-KV scratch; a caller whose allocator must own every byte of
+ * device memory, a runtime that captures the step into a CUDA graph (allocation is
+ * not allowed inside a capture), or a service that forbids allocation after start-up
+ * cannot accept that.  This call computes the same result with its scratch in a
+ * fixed 16 MiB static device array that the library holds on every GPU that loads
+ * it, until the process exits.
+ *  - Same arguments and results as paged_attention(), bf16 with head_dim 128 only.
+ *  - error_bits: optional device uint32 the kernels OR their data-error bits into
+ *    (the bits of pkv_peek_error_bits); NULL discards them.  The caller clears it.
+ *  - A batch whose scratch need exceeds the array returns PKV_ERR_NO_MEMORY and
+ *    launches nothing.  The need is about num_seqs * num_kv_heads *
+ *    ceil(max_seq_len / 1024) * group * 520 bytes plus a few arrays per request.
+ *  - The first call on a device looks up the array's device address (with that
+ *    device current); make it before any stream capture.
+ *  - All calls share the array and the library re-zeroes what each call needs, but
+ *    calls whose kernels overlap on the GPU race on it: serialise them.
+ *  - Calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+PKV_API int paged_attention_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                    const pkv_cache_desc* cache, const int32_t* block_tables,
+                                    int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                    const int32_t* query_start_loc, int32_t num_seqs, int32_t num_q_heads,
+                                    int64_t num_tokens, int32_t max_query_len, int32_t max_seq_len, float scale,
+                                    void* out, uint32_t* error_bits, void* stream);
+
 /* Synchronises `stream`, returns the device error word of the current device as a
  * pkv_status (PKV_OK, PKV_ERR_INDEX or PKV_ERR_TIMEOUT) and clears it. */
 PKV_API int pkv_get_last_error(void* stream);
