@@ -5,7 +5,7 @@ pairs, and N(0,1) tensors.  It holds none of the method's arithmetic (no slot
 mapping, no attention, no copy); both the CUDA path and the oracle consume what
 it produces, and neither is imported here.
 
-The five named workloads follow the shapes the pages' subject implies (16-token
+The named workloads follow the shapes the pages' subject implies (16-token
 blocks, per-request block tables drawn from one physical pool, shared prefix
 blocks, continuous batches that mix chunked prefills and decodes):
 
@@ -24,6 +24,9 @@ blocks, continuous batches that mix chunked prefills and decodes):
    pool = ceil(1.1 x blocks needed).
 5. ``long``   -- bf16, 32 requests of 32768 tokens (2048 blocks each), 64/8
    heads, head_dim 128, pool of 70000.
+6. ``prefill`` -- the chunk half of ``mixed`` on its own: 8 chunked-prefill chunks
+   of 512 query tokens after a cached context uniform in [0, 3072]; pool =
+   ceil(1.1 x blocks needed).  Used to measure the prefill kernel alone.
 
 Every draw is seeded (``seed = 248000 + index`` by default); uniform integer
 ranges are inclusive.  Lengths, permutations and pairs come from a numpy
@@ -38,7 +41,7 @@ from dataclasses import dataclass, field
 import numpy as np
 
 BLOCK = 16
-NAMES = ("tiny", "decode", "prefix", "mixed", "long")
+NAMES = ("tiny", "decode", "prefix", "mixed", "long", "prefill")
 BASE_SEED = 248000
 
 
@@ -135,7 +138,7 @@ def _qsl(q_lens):
 
 
 def make(name: str, seed: int | None = None) -> Workload:
-    """One of the five named workloads (host-side metadata; tensors via make_tensors)."""
+    """One of the named workloads (host-side metadata; tensors via make_tensors)."""
     idx = NAMES.index(name)
     seed = BASE_SEED + idx if seed is None else seed
     rng = np.random.default_rng(seed)
@@ -196,6 +199,16 @@ def make(name: str, seed: int | None = None) -> Workload:
         bt, _ = _tables(L, rng.permutation(pool).astype(np.int32))
         return Workload(name, "bf16", 64, 8, 128, pool, 1.0 / math.sqrt(128), L,
                         _qsl(np.ones(n, np.int32)), bt, seed)
+    if name == "prefill":
+        n_chunks, chunk = 8, 512
+        ctx = rng.integers(0, 3072, size=n_chunks, endpoint=True).astype(np.int32)
+        L = (ctx + chunk).astype(np.int32)
+        need = int(sum((int(x) + BLOCK - 1) // BLOCK for x in L))
+        pool = int(math.ceil(1.1 * need))
+        bt, _ = _tables(L, rng.permutation(pool).astype(np.int32))
+        return Workload(name, "bf16", 32, 8, 128, pool, 1.0 / math.sqrt(128), L,
+                        _qsl(np.full(n_chunks, chunk, np.int32)), bt, seed,
+                        notes={"prefill_chunks": n_chunks, "chunk": chunk})
     raise KeyError(name)
 
 
