@@ -14,11 +14,14 @@
 // merges all partials in split order (log-sum-exp merge), so results never depend
 // on scheduling.
 //
-// Per CTA (192 threads):
-//   warp 0     producer: fetches items, loads the G query rows into shared memory,
-//              and per tile issues 4 TMA boxes per block (K and V, two 64-column
-//              halves each, 128-byte swizzle) straight from the block's physical
-//              location -- the block-table gather.  kStages tiles in flight.
+// Per CTA (224 threads):
+//   warp 6     scheduler: takes items off the queue ahead of use and resolves the
+//              request, its lengths, its query row and the item's block ids (checked
+//              against the pool) into a ring in shared memory.
+//   warp 0     producer: only TMA -- the G query rows (one 3-D box per half) and,
+//              per tile, 4 boxes per block (K and V, two 64-column halves each,
+//              128-byte swizzle) straight from the block's physical location -- the
+//              block-table gather.  kStages tiles in flight.
 //   warp 1     MMA issuer (one lane): S^T = K Q^T with the 128 keys on M and the
 //              query-head group on N = 16, then O^T = V^T P^T with head_dim on M,
 //              both accumulating fp32 in TMEM.  V^T is read MN-major from the same
@@ -36,14 +39,15 @@
 namespace pkv {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;                 // 7 warps, see the role list above
 constexpr int kStages = 3;
 constexpr int kHalfBytes = 16384;             // one 64-column half of a 128-key tile
 constexpr int kKBytes = 2 * kHalfBytes;       // K tile: [2 halves][128 keys][128 B]
 constexpr int kStageBytes = 2 * kKBytes;      // K + V
 constexpr int kQBytes = 4096;                 // Q: [2 halves][16 rows][128 B]
 constexpr int kPBytes = 4096;                 // P^T: 128 keys x 16 heads, MN-major, no swizzle
-constexpr int kRing = 4;
+constexpr int kRing = 3;                      // ring of items prepared by the scheduler
+constexpr int kMaxIds = kSplitKeys / kBlock;  // block ids of one item
 constexpr uint32_t kTmemCols = 64;            // S^T x2 (cols 0, 16), O^T x2 (cols 32, 48)
 constexpr int kBlocksPerTile = kTileKeys / kBlock;
 
@@ -51,6 +55,7 @@ struct alignas(16) ItemInfo {
   int32_t idx;  // decode item index; -1 = queue exhausted
   int32_t seq, head, split;
   int32_t nsplit, key_start, key_end, valid;
+  int32_t trow, row_ok, pad0, pad1;  // the request's query row, and whether it is addressable
 };
 
 struct Ctl {
@@ -62,6 +67,7 @@ struct Ctl {
   uint64_t group_bar;  // the four softmax warps' exchange barrier
   ItemInfo ring[kRing];
   int bad[kRing];
+  int32_t ids[kRing][kMaxIds];  // physical block ids of each ring item, validated
   float red[2][4][16];
   uint32_t tmem_base;
   int abort_flag;
@@ -69,9 +75,9 @@ struct Ctl {
 };
 
 constexpr int kSmemBytes = kStages * kStageBytes + 2 * kQBytes + 2 * kPBytes + static_cast<int>(sizeof(Ctl)) + 1024;
+static_assert(kSmemBytes <= 232448, "decode shared memory");
 
 struct DecodeParams {
-  const __nv_bfloat16* q;
   __nv_bfloat16* out;
   const int32_t* bt;
   const int32_t* seq_lens;
@@ -85,7 +91,7 @@ struct DecodeParams {
   uint32_t* err;
   int64_t num_blocks;
   int64_t num_tokens;
-  int32_t num_seqs, max_blocks, hkv, group, hq, split_keys;
+  int32_t num_seqs, max_blocks, hkv, group, gp, hq, split_keys;
   float scale_log2;
 };
 
@@ -104,133 +110,160 @@ __device__ __forceinline__ bool group_sync(Ctl& c, uint32_t& phase) {
   return ok;
 }
 
-__device__ ItemInfo make_item(const DecodeParams& P, int idx, int total) {
-  ItemInfo r{};
-  if (idx >= total) {
-    r.idx = -1;
-    return r;
-  }
-  int lo = 0, hi = P.num_seqs - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (P.dec_prefix[mid] <= idx) lo = mid; else hi = mid - 1;
-  }
-  const int i = lo;
-  const int base = P.dec_prefix[i];
-  const int nsplit = (P.dec_prefix[i + 1] - base) / P.hkv;
-  if (nsplit <= 0) {  // cannot happen for a consistent plan; treat as an invalid item
-    r.idx = idx;
-    r.seq = i;
-    r.nsplit = 1;
-    return r;
-  }
-  const int local = idx - base;
-  r.idx = idx;
-  r.seq = i;
-  r.head = local / nsplit;
-  r.split = local % nsplit;
-  r.nsplit = nsplit;
-  const int64_t L = P.seq_lens[i];
-  const int64_t t = P.qsl[i];
-  const bool ok = L >= 1 && (L + kBlock - 1) / kBlock <= P.max_blocks &&
-                  static_cast<int64_t>(nsplit) == (L + P.split_keys - 1) / P.split_keys && t >= 0 &&
-                  t < P.num_tokens && P.qsl[i + 1] == t + 1;
-  r.valid = ok ? 1 : 0;
-  r.key_start = ok ? r.split * P.split_keys : 0;
-  const int64_t split_end = static_cast<int64_t>(r.key_start) + P.split_keys;
-  r.key_end = ok ? static_cast<int32_t>(L < split_end ? L : split_end) : 0;
-  return r;
-}
-
-// ------------------------------------------------------------------ producer warp
-__device__ void producer_warp(const DecodeParams& P, const CUtensorMap* kmap, const CUtensorMap* vmap, Ctl& c,
-                              uint8_t* stages, uint8_t* qbuf) {
+// ------------------------------------------------------------------ scheduler warp
+// Takes items off the queue ahead of use and resolves everything the other roles need
+// from global memory -- the request, its lengths and query row, and the item's block
+// ids (validated) -- into a ring in shared memory, so that the TMA producer never
+// waits on a global load.  The ring is short on purpose: an item taken off the queue
+// early is an item no idle CTA can take at the end.
+__device__ void scheduler_warp(const DecodeParams& P, Ctl& c) {
   const int lane = threadIdx.x & 31;
-  const int total = P.dec_prefix[P.num_seqs];
-  uint32_t it = 0, tc = 0, qc = 0;
   volatile int* abort_flag = &c.abort_flag;
-  while (true) {
+  const int total = P.dec_prefix[P.num_seqs];
+  for (uint32_t it = 0;; ++it) {
     const int slot = it % kRing;
     if (!mbar_wait(&c.item_empty[slot], ((it / kRing) & 1) ^ 1, abort_flag)) {
       if (!*abort_flag && lane == 0) raise_abort(c, P.err);
       break;
     }
+    int idx = 0;
+    if (lane == 0) idx = atomicAdd(P.queue, 1);
+    idx = __shfl_sync(0xffffffffu, idx, 0);
+    ItemInfo r{};
+    if (idx >= total) {
+      if (lane == 0) {
+        r.idx = -1;
+        c.ring[slot] = r;
+        mbar_arrive(&c.item_full[slot]);
+      }
+      break;
+    }
+    // the request owning the item: last i with dec_prefix[i] <= idx, by a 32-way
+    // search (each round the 32 lanes probe evenly spaced candidates)
+    int lo = 0, hi = P.num_seqs - 1;
+    while (hi > lo) {
+      const int step = (hi - lo + 32) / 32;
+      const int pos = lo + lane * step;
+      const bool le = pos <= hi && __ldg(P.dec_prefix + pos) <= idx;
+      const unsigned m = __ballot_sync(0xffffffffu, le);  // lane 0 always: dec_prefix[lo] <= idx
+      lo += (31 - __clz(m)) * step;
+      hi = min(hi, lo + step - 1);
+    }
+    const int i = lo;
+    const int base = __ldg(P.dec_prefix + i);
+    const int cnt = __ldg(P.dec_prefix + i + 1) - base;
+    const int64_t L = __ldg(P.seq_lens + i);
+    const int64_t t = __ldg(P.qsl + i), t1 = __ldg(P.qsl + i + 1);
+    const int nsplit = cnt / P.hkv;
+    r.idx = idx;
+    r.seq = i;
+    r.row_ok = (t >= 0 && t < P.num_tokens && t1 == t + 1) ? 1 : 0;
+    r.trow = r.row_ok ? static_cast<int32_t>(t) : 0;
+    r.nsplit = 1;
+    if (nsplit > 0) {  // always, for a consistent plan
+      const int local = idx - base;
+      r.head = local / nsplit;
+      r.split = local % nsplit;
+      r.nsplit = nsplit;
+      const bool ok = r.row_ok && L >= 1 && (L + kBlock - 1) / kBlock <= P.max_blocks &&
+                      static_cast<int64_t>(nsplit) == (L + P.split_keys - 1) / P.split_keys;
+      if (ok) {
+        r.valid = 1;
+        r.key_start = r.split * P.split_keys;
+        const int64_t split_end = static_cast<int64_t>(r.key_start) + P.split_keys;
+        r.key_end = static_cast<int32_t>(L < split_end ? L : split_end);
+      }
+    }
+    int bad = 0;
+    if (r.valid) {
+      const int nblk = (r.key_end - r.key_start + kBlock - 1) / kBlock;
+      const int32_t* row = P.bt + static_cast<int64_t>(i) * P.max_blocks + r.key_start / kBlock;
+      for (int b = lane; b < nblk; b += 32) {
+        int id = __ldg(row + b);
+        if (id < 0 || id >= P.num_blocks) {
+          bad = 1;
+          id = 0;
+        }
+        c.ids[slot][b] = id;
+      }
+    }
+    bad = __any_sync(0xffffffffu, bad);
     if (lane == 0) {
-      const int idx = atomicAdd(P.queue, 1);
-      c.ring[slot] = make_item(P, idx, total);
-      c.bad[slot] = 0;
-      mbar_arrive(&c.item_full[slot]);
+      if (bad) flag_error(P.err, kErrBlockId);
+      c.ring[slot] = r;
+      c.bad[slot] = bad;
     }
     __syncwarp();
+    if (lane == 0) mbar_arrive(&c.item_full[slot]);
+  }
+}
+
+// ------------------------------------------------------------------ producer warp
+// Only mbarrier waits and TMA issues: the G query rows of the item (one 3-D box per
+// 64-column half) and, per 128-key tile, four 16 x 64 boxes per block taken straight
+// from the block's physical location (the block-table gather).
+__device__ void producer_warp(const DecodeParams& P, const CUtensorMap* qmap, const CUtensorMap* kmap,
+                              const CUtensorMap* vmap, Ctl& c, uint8_t* stages, uint8_t* qbuf) {
+  const int lane = threadIdx.x & 31;
+  uint32_t it = 0, tc = 0, qc = 0;
+  volatile int* abort_flag = &c.abort_flag;
+  const uint64_t pol_q = l2_policy_evict_first();
+  bool ok = true;
+  while (ok) {
+    const int slot = it % kRing;
+    if (!mbar_wait(&c.item_full[slot], (it / kRing) & 1, abort_flag)) {
+      ok = false;
+      break;
+    }
     const ItemInfo info = c.ring[slot];
     ++it;
     if (info.idx < 0) break;
-    if (!info.valid) continue;
-
-    // the G query rows of this (token, kv head), K-major with the 128B swizzle
-    const int qb = qc & 1;
-    if (!mbar_wait(&c.q_free[qb], ((qc >> 1) & 1) ^ 1, abort_flag)) {
-      if (!*abort_flag && lane == 0) raise_abort(c, P.err);
-      break;
-    }
-    {
-      uint8_t* qs = qbuf + qb * kQBytes;
-      const int64_t trow = P.qsl[info.seq];
-      const uint4* src = reinterpret_cast<const uint4*>(P.q + (trow * P.hq + static_cast<int64_t>(info.head) * P.group) * 128);
-      for (int ch = lane; ch < P.group * 16; ch += 32) {
-        const int r = ch >> 4, cc = ch & 15, half = cc >> 3, c8 = cc & 7;
-        *reinterpret_cast<uint4*>(qs + half * 2048 + r * 128 + ((c8 ^ (r & 7)) << 4)) = __ldg(src + ch);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&c.q_full[qb]);
-      ++qc;
-    }
-
-    const int nt = (info.key_end - info.key_start + kTileKeys - 1) / kTileKeys;
-    const int32_t* btrow = P.bt + static_cast<int64_t>(info.seq) * P.max_blocks;
-    bool ok = true;
-    for (int j = 0; j < nt; ++j) {
-      const int st = tc % kStages;
-      if (!mbar_wait(&c.empty[st], ((tc / kStages) & 1) ^ 1, abort_flag)) {
-        if (!*abort_flag && lane == 0) raise_abort(c, P.err);
+    if (info.valid) {
+      const int qb = qc & 1;
+      if (!mbar_wait(&c.q_free[qb], ((qc >> 1) & 1) ^ 1, abort_flag)) {
         ok = false;
         break;
       }
-      const int t0 = info.key_start + j * kTileKeys;
-      const int nblk = min(kBlocksPerTile, (info.key_end - t0 + kBlock - 1) / kBlock);
-      int id = 0;
-      bool bad = false;
-      if (lane < nblk) {
-        id = __ldg(btrow + t0 / kBlock + lane);
-        if (id < 0 || id >= P.num_blocks) {
-          bad = true;
-          id = 0;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&c.q_full[qb], 2u * static_cast<uint32_t>(P.gp) * 128u);
+        const int32_t y = info.head * P.group;
+        tma_load_3d(qbuf + qb * kQBytes, qmap, &c.q_full[qb], 0, y, info.trow, pol_q);
+        tma_load_3d(qbuf + qb * kQBytes + 2048, qmap, &c.q_full[qb], 64, y, info.trow, pol_q);
+      }
+      ++qc;
+      const int nt = (info.key_end - info.key_start + kTileKeys - 1) / kTileKeys;
+      for (int j = 0; j < nt; ++j) {
+        const int st = tc % kStages;
+        if (!mbar_wait(&c.empty[st], ((tc / kStages) & 1) ^ 1, abort_flag)) {
+          ok = false;
+          break;
         }
+        const int t0 = info.key_start + j * kTileKeys;
+        const int nblk = min(kBlocksPerTile, (info.key_end - t0 + kBlock - 1) / kBlock);
+        const int id = lane < nblk ? c.ids[slot][j * kBlocksPerTile + lane] : 0;
+        if (lane == 0) mbar_arrive_expect_tx(&c.full[st], static_cast<uint32_t>(nblk) * 8192u);
+        __syncwarp();
+        if (lane < nblk) {
+          uint8_t* s = stages + st * kStageBytes + lane * 2048;
+          const int32_t row = (id * P.hkv + info.head) * kBlock;
+          tma_load_2d(s, kmap, &c.full[st], 0, row);
+          tma_load_2d(s + kHalfBytes, kmap, &c.full[st], 64, row);
+          tma_load_2d(s + kKBytes, vmap, &c.full[st], 0, row);
+          tma_load_2d(s + kKBytes + kHalfBytes, vmap, &c.full[st], 64, row);
+        }
+        ++tc;
       }
-      if (__any_sync(0xffffffffu, bad)) {
-        if (bad) flag_error(P.err, kErrBlockId);
-        if (lane == 0) c.bad[slot] = 1;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive_expect_tx(&c.full[st], static_cast<uint32_t>(nblk) * 8192u);
-      __syncwarp();
-      if (lane < nblk) {
-        uint8_t* s = stages + st * kStageBytes + lane * 2048;
-        const int32_t row = (id * P.hkv + info.head) * kBlock;
-        tma_load_2d(s, kmap, &c.full[st], 0, row);
-        tma_load_2d(s + kHalfBytes, kmap, &c.full[st], 64, row);
-        tma_load_2d(s + kKBytes, vmap, &c.full[st], 0, row);
-        tma_load_2d(s + kKBytes + kHalfBytes, vmap, &c.full[st], 64, row);
-      }
-      ++tc;
+      if (!ok) break;
     }
-    if (!ok) break;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&c.item_empty[slot]);
   }
+  if (!ok && !*abort_flag && lane == 0) raise_abort(c, P.err);
   if (*abort_flag) {
     // let copies already issued land before the CTA's shared memory goes away
     const uint32_t first = tc > static_cast<uint32_t>(kStages) ? tc - kStages : 0;
     for (uint32_t cnt = first; cnt < tc; ++cnt) mbar_wait(&c.full[cnt % kStages], (cnt / kStages) & 1, nullptr);
+    if (qc > 0) mbar_wait(&c.q_full[(qc - 1) & 1], ((qc - 1) >> 1) & 1, nullptr);
   }
 }
 
@@ -342,8 +375,8 @@ __device__ void softmax_warps(const DecodeParams& P, Ctl& c, uint8_t* stages, ui
     if (!info.valid) {
       // report once per request and zero what can be addressed
       if (info.split == 0 && info.head == 0 && r == 0) flag_error(P.err, kErrLength);
-      const int64_t trow = P.qsl[info.seq];
-      if (info.split == 0 && trow >= 0 && trow < P.num_tokens && P.qsl[info.seq + 1] == trow + 1)
+      const int64_t trow = info.trow;
+      if (info.split == 0 && info.row_ok)
         for (int g = 0; g < G; ++g)
           P.out[(trow * P.hq + static_cast<int64_t>(info.head) * G + g) * 128 + r] = __float2bfloat16_rn(0.f);
       __syncwarp();
@@ -497,7 +530,7 @@ __device__ void softmax_warps(const DecodeParams& P, Ctl& c, uint8_t* stages, ui
       for (int g = 0; g < GP; ++g) lt[g] = c.red[rb][0][g] + c.red[rb][1][g] + c.red[rb][2][g] + c.red[rb][3][g];
     }
     const bool bad = c.bad[slot] != 0;
-    const int64_t trow = P.qsl[info.seq];
+    const int64_t trow = info.trow;
     const int64_t unit = static_cast<int64_t>(info.seq) * P.hkv + info.head;
     __nv_bfloat16* orow = P.out + (trow * P.hq + static_cast<int64_t>(info.head) * G) * 128 + r;
     if (info.nsplit == 1) {
@@ -555,7 +588,8 @@ __device__ void softmax_warps(const DecodeParams& P, Ctl& c, uint8_t* stages, ui
 }
 
 template <int GP>
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ CUtensorMap kmap,
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ CUtensorMap qmap,
+                                                             const __grid_constant__ CUtensorMap kmap,
                                                              const __grid_constant__ CUtensorMap vmap,
                                                              const DecodeParams P) {
   extern __shared__ uint8_t smem_raw[];
@@ -584,13 +618,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     }
     for (int s = 0; s < kRing; ++s) {
       mbar_init(&c.item_full[s], 1);
-      mbar_init(&c.item_empty[s], 5);
+      mbar_init(&c.item_empty[s], 6);  // producer, MMA warp, four softmax warps
     }
     mbar_init(&c.drain, 1);
     mbar_init(&c.group_bar, 4);
     c.abort_flag = 0;
     c.merge_flag = 0;
     fence_mbar_init();
+    tma_prefetch_map(&qmap);
     tma_prefetch_map(&kmap);
     tma_prefetch_map(&vmap);
   }
@@ -604,9 +639,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   tc_fence_after();
   const uint32_t tmem = c.tmem_base;
 
-  if (warp == 0) producer_warp(P, &kmap, &vmap, c, stages, qbuf);
+  if (warp == 0) producer_warp(P, &qmap, &kmap, &vmap, c, stages, qbuf);
   else if (warp == 1) mma_warp(P, c, stages, qbuf, pbuf, tmem);
-  else softmax_warps<GP>(P, c, stages, pbuf, tmem);
+  else if (warp < 6) softmax_warps<GP>(P, c, stages, pbuf, tmem);
+  else scheduler_warp(P, c);
 
   tc_fence_before();
   __syncthreads();
@@ -618,10 +654,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
 }
 
 template <int GP>
-int launch_gp(const CUtensorMap& km, const CUtensorMap& vm, const DecodeParams& p, int grid, cudaStream_t s) {
+int launch_gp(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& vm, const DecodeParams& p, int grid,
+              cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(decode_kernel<GP>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return cuda_status(e);
-  decode_kernel<GP><<<grid, kThreads, kSmemBytes, s>>>(km, vm, p);
+  decode_kernel<GP><<<grid, kThreads, kSmemBytes, s>>>(qm, km, vm, p);
   return cuda_status(cudaGetLastError());
 }
 
@@ -633,13 +670,20 @@ int launch_decode_tc(const AttnArgs& a, const Workspace& ws, int num_sms, uint32
   if (group > 16 || a.cache.head_dim != 128 || a.cache.dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
   const uint64_t rows = static_cast<uint64_t>(a.cache.num_blocks) * hkv * kBlock;
   if (rows >= (1ull << 31)) return PKV_ERR_UNSUPPORTED;
-  CUtensorMap km, vm;
+  if (a.num_tokens >= (int64_t(1) << 31)) return PKV_ERR_UNSUPPORTED;
+  const int gp = group <= 4 ? 4 : (group <= 8 ? 8 : 16);
+  CUtensorMap qm, km, vm;
   int st = encode_tensor_map_2d(&km, a.k_cache, 128, rows, 256, 64, 16);
   if (st) return st;
   st = encode_tensor_map_2d(&vm, a.v_cache, 128, rows, 256, 64, 16);
   if (st) return st;
+  // q viewed as [token][head][128]: one box = the GP query heads of a kv head, one token
+  const uint64_t qdims[3] = {128, static_cast<uint64_t>(a.num_q_heads), static_cast<uint64_t>(a.num_tokens)};
+  const uint64_t qstrides[2] = {256, static_cast<uint64_t>(a.num_q_heads) * 256};
+  const uint32_t qbox[3] = {64, static_cast<uint32_t>(gp), 1};
+  st = encode_tensor_map_3d(&qm, a.q, qdims, qstrides, qbox);
+  if (st) return st;
   DecodeParams p;
-  p.q = static_cast<const __nv_bfloat16*>(a.q);
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.bt = a.block_tables;
   p.seq_lens = a.seq_lens;
@@ -657,13 +701,14 @@ int launch_decode_tc(const AttnArgs& a, const Workspace& ws, int num_sms, uint32
   p.max_blocks = a.max_blocks;
   p.hkv = hkv;
   p.group = group;
+  p.gp = gp;
   p.hq = a.num_q_heads;
   p.split_keys = kSplitKeys;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   TraceScope trace(kTraceDecode, s);
-  if (group <= 4) return launch_gp<4>(km, vm, p, num_sms, s);
-  if (group <= 8) return launch_gp<8>(km, vm, p, num_sms, s);
-  return launch_gp<16>(km, vm, p, num_sms, s);
+  if (gp == 4) return launch_gp<4>(qm, km, vm, p, num_sms, s);
+  if (gp == 8) return launch_gp<8>(qm, km, vm, p, num_sms, s);
+  return launch_gp<16>(qm, km, vm, p, num_sms, s);
 }
 
 }  // namespace pkv
