@@ -162,7 +162,8 @@ PKV_API int paged_attention(const void* q, const void* k_cache, const void* v_ca
  *    (the bits of pkv_peek_error_bits); NULL discards them.  The caller clears it.
  *  - A batch whose scratch need exceeds the array returns PKV_ERR_NO_MEMORY and
  *    launches nothing.  The need is about num_seqs * num_kv_heads *
- *    ceil(max_seq_len / 1024) * group * 520 bytes plus a few arrays per request.
+ *    ceil(max_seq_len / 1024) * GP * 520 bytes plus a few arrays per request, GP
+ *    being the query-head group size rounded up to 4, 8 or 16.
  *  - The first call on a device looks up the array's device address (with that
  *    device current); make it before any stream capture.
  *  - All calls share the array and the library re-zeroes what each call needs, but

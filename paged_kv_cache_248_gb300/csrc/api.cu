@@ -261,11 +261,11 @@ int paged_attention(const void* q, const void* k_cache, const void* v_cache, con
   const int64_t max_splits = (static_cast<int64_t>(max_seq_len) + kSplitKeys - 1) / kSplitKeys;
   const int64_t max_dec_items = static_cast<int64_t>(num_seqs) * hkv * max_splits;
   if (max_dec_items >= (int64_t(1) << 31)) return PKV_ERR_UNSUPPORTED;
-  const size_t need = layout_workspace(nullptr, num_seqs, hkv, group, cache->head_dim, max_dec_items, nullptr);
+  const size_t need = layout_workspace(nullptr, num_seqs, hkv, gp, cache->head_dim, max_dec_items, nullptr);
   st = ensure_workspace(ctx, need, s);
   if (st) return st;
   Workspace ws;
-  layout_workspace(ctx->ws, num_seqs, hkv, group, cache->head_dim, max_dec_items, &ws);
+  layout_workspace(ctx->ws, num_seqs, hkv, gp, cache->head_dim, max_dec_items, &ws);
   PlanArgs plan{seq_lens, query_start_loc, num_seqs, num_tokens, hkv, max_blocks_per_seq, max_seq_len,
                 kSplitKeys, kTileKeys / gp, ws.counters, ws.dec_prefix, ws.pre_prefix, ws.unit_arrive,
                 ws.unit_bad, ctx->err};

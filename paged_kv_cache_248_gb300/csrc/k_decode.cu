@@ -86,8 +86,8 @@ struct DecodeParams {
   int32_t* queue;
   int32_t* unit_arrive;
   int32_t* unit_bad;
-  float* part_o;   // [items][G][128]
-  float* part_ml;  // [items][G][2]
+  float* part_o;   // [items][128][GP]
+  float* part_ml;  // [items][GP][2]
   uint32_t* err;
   int64_t num_blocks;
   int64_t num_tokens;
@@ -108,6 +108,43 @@ __device__ __forceinline__ bool group_sync(Ctl& c, uint32_t& phase) {
   const bool ok = mbar_wait(&c.group_bar, phase & 1, &c.abort_flag);
   ++phase;
   return ok;
+}
+
+// Reduce GP per-lane values over the warp for every head at once.  Each halving
+// exchange sends half of the remaining values to the partner lane, so after log2(GP)
+// exchanges a lane holds one head's partial (head_of_lane), and the remaining lane
+// bits are folded with a plain butterfly: GP - 1 + 5 - log2(GP) shuffles in all,
+// instead of 5 per head.
+template <int GP, bool kMax>
+__device__ __forceinline__ float warp_reduce_scatter(float (&v)[GP]) {
+  const int lane = threadIdx.x & 31;
+  int o = 16;
+#pragma unroll
+  for (int n = GP; n > 1; n >>= 1, o >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int k = 0; k < n / 2; ++k) {
+      const float send = upper ? v[k] : v[k + n / 2];
+      const float keep = upper ? v[k + n / 2] : v[k];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, o);
+      v[k] = kMax ? fmaxf(keep, recv) : keep + recv;
+    }
+  }
+  float x = v[0];
+#pragma unroll
+  for (; o > 0; o >>= 1) {
+    const float recv = __shfl_xor_sync(0xffffffffu, x, o);
+    x = kMax ? fmaxf(x, recv) : x + recv;
+  }
+  return x;
+}
+// The head whose reduction warp_reduce_scatter<GP> leaves in this lane.
+template <int GP>
+__device__ __forceinline__ int head_of_lane(int lane) {
+  int g = 0, o = 16;
+#pragma unroll
+  for (int n = GP; n > 1; n >>= 1, o >>= 1) g = (g << 1) | ((lane & o) ? 1 : 0);
+  return g;
 }
 
 // ------------------------------------------------------------------ scheduler warp
@@ -429,16 +466,11 @@ __device__ void softmax_warps(const DecodeParams& P, Ctl& c, uint8_t* stages, ui
 #pragma unroll
       for (int g = 0; g < GP; ++g) {
         x[g] = valid_key ? __uint_as_float(sraw[g]) * P.scale_log2 : -INFINITY;
-        float v = x[g];
-#pragma unroll
-        for (int sh = 16; sh > 0; sh >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, sh));
-        tmax[g] = v;
+        tmax[g] = x[g];
       }
+      const float wmax = warp_reduce_scatter<GP, true>(tmax);
       const int rb = gph & 1;
-      if (lane == 0) {
-#pragma unroll
-        for (int g = 0; g < GP; ++g) c.red[rb][wq][g] = tmax[g];
-      }
+      if ((lane & (32 / GP - 1)) == 0) c.red[rb][wq][head_of_lane<GP>(lane)] = wmax;
       if (!group_sync(c, gph)) {
         ok = false;
         break;
@@ -509,19 +541,12 @@ __device__ void softmax_warps(const DecodeParams& P, Ctl& c, uint8_t* stages, ui
 
     // total softmax denominators: sum the per-thread partial sums over the 128 keys lanes
     float lt[GP];
-#pragma unroll
-    for (int g = 0; g < GP; ++g) {
-      float v = l_run[g];
-#pragma unroll
-      for (int sh = 16; sh > 0; sh >>= 1) v += __shfl_xor_sync(0xffffffffu, v, sh);
-      lt[g] = v;
-    }
     {
-      const int rb = gph & 1;
-      if (lane == 0) {
 #pragma unroll
-        for (int g = 0; g < GP; ++g) c.red[rb][wq][g] = lt[g];
-      }
+      for (int g = 0; g < GP; ++g) lt[g] = l_run[g];
+      const float wsum = warp_reduce_scatter<GP, false>(lt);
+      const int rb = gph & 1;
+      if ((lane & (32 / GP - 1)) == 0) c.red[rb][wq][head_of_lane<GP>(lane)] = wsum;
       if (!group_sync(c, gph)) {
         ok = false;
         break;
@@ -538,16 +563,16 @@ __device__ void softmax_warps(const DecodeParams& P, Ctl& c, uint8_t* stages, ui
       for (int g = 0; g < GP; ++g)
         if (g < G) orow[g * 128] = __float2bfloat16_rn(bad ? 0.f : acc[g] / lt[g]);
     } else {
-      float* po = P.part_o + static_cast<int64_t>(info.idx) * G * 128 + r;
-      float* pml = P.part_ml + static_cast<int64_t>(info.idx) * G * 2;
+      // partials: accumulators [item][d][GP] (one float4 run per thread), max and sum [item][GP][2]
+      float4* po = reinterpret_cast<float4*>(P.part_o + (static_cast<int64_t>(info.idx) * 128 + r) * GP);
+#pragma unroll
+      for (int k = 0; k < GP / 4; ++k) po[k] = make_float4(acc[4 * k], acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3]);
+      float* pml = P.part_ml + static_cast<int64_t>(info.idx) * GP * 2;
 #pragma unroll
       for (int g = 0; g < GP; ++g) {
-        if (g < G) {
-          po[g * 128] = acc[g];
-          if (r == g) {
-            pml[2 * g] = m_run[g];
-            pml[2 * g + 1] = lt[g];
-          }
+        if (r == g) {
+          pml[2 * g] = m_run[g];
+          pml[2 * g + 1] = lt[g];
         }
       }
       if (bad && r == 0) P.unit_bad[unit] = 1;
@@ -568,17 +593,48 @@ __device__ void softmax_warps(const DecodeParams& P, Ctl& c, uint8_t* stages, ui
         __threadfence();
         const bool any_bad = *reinterpret_cast<volatile int*>(P.unit_bad + unit) != 0;
         const int64_t base = info.idx - info.split;
-        for (int g = 0; g < G; ++g) {
-          float M = -INFINITY;
-          for (int s = 0; s < info.nsplit; ++s) M = fmaxf(M, __ldcg(P.part_ml + ((base + s) * G + g) * 2));
-          float num = 0.f, den = 0.f;
-          for (int s = 0; s < info.nsplit; ++s) {
-            const float f = exp2f(__ldcg(P.part_ml + ((base + s) * G + g) * 2) - M);
-            den = fmaf(__ldcg(P.part_ml + ((base + s) * G + g) * 2 + 1), f, den);
-            num = fmaf(__ldcg(P.part_o + ((base + s) * G + g) * 128 + r), f, num);
-          }
-          orow[g * 128] = __float2bfloat16_rn(any_bad ? 0.f : num / den);
+        // log-sum-exp merge in split order, one pass with a running maximum
+        float M[GP], num[GP], den[GP];
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
+          M[g] = -INFINITY;
+          num[g] = 0.f;
+          den[g] = 0.f;
         }
+#pragma unroll 4
+        for (int s = 0; s < info.nsplit; ++s) {
+          const float4* ml4 = reinterpret_cast<const float4*>(P.part_ml + (base + s) * GP * 2);
+          const float4* o4 = reinterpret_cast<const float4*>(P.part_o + ((base + s) * 128 + r) * GP);
+          float ml[2 * GP], ov[GP];
+#pragma unroll
+          for (int k = 0; k < GP / 2; ++k) {
+            const float4 t = __ldcg(ml4 + k);
+            ml[4 * k] = t.x;
+            ml[4 * k + 1] = t.y;
+            ml[4 * k + 2] = t.z;
+            ml[4 * k + 3] = t.w;
+          }
+#pragma unroll
+          for (int k = 0; k < GP / 4; ++k) {
+            const float4 t = __ldcg(o4 + k);
+            ov[4 * k] = t.x;
+            ov[4 * k + 1] = t.y;
+            ov[4 * k + 2] = t.z;
+            ov[4 * k + 3] = t.w;
+          }
+#pragma unroll
+          for (int g = 0; g < GP; ++g) {
+            const float m_new = fmaxf(M[g], ml[2 * g]);
+            const float a = exp2f(M[g] - m_new);
+            const float b = exp2f(ml[2 * g] - m_new);
+            den[g] = fmaf(den[g], a, ml[2 * g + 1] * b);
+            num[g] = fmaf(num[g], a, ov[g] * b);
+            M[g] = m_new;
+          }
+        }
+#pragma unroll
+        for (int g = 0; g < GP; ++g)
+          if (g < G) orow[g * 128] = __float2bfloat16_rn(any_bad ? 0.f : num[g] / den[g]);
       }
     }
     __syncwarp();

@@ -89,7 +89,7 @@ extern "C" PKV_API int paged_attention_noalloc(const void* q, const void* k_cach
   const int64_t max_splits = (static_cast<int64_t>(max_seq_len) + kSplitKeys - 1) / kSplitKeys;
   const int64_t max_dec_items = static_cast<int64_t>(num_seqs) * hkv * max_splits;
   if (max_dec_items >= (int64_t(1) << 31)) return PKV_ERR_NO_MEMORY;
-  const size_t need = layout_workspace(nullptr, num_seqs, hkv, group, cache->head_dim, max_dec_items, nullptr);
+  const size_t need = layout_workspace(nullptr, num_seqs, hkv, gp, cache->head_dim, max_dec_items, nullptr);
   if (need > kNoAllocScratchBytes - kErrSlotBytes) return PKV_ERR_NO_MEMORY;
 
   int dev = 0;
@@ -100,7 +100,7 @@ extern "C" PKV_API int paged_attention_noalloc(const void* q, const void* k_cach
   if (st) return st;
   uint32_t* err = error_bits ? error_bits : static_cast<uint32_t*>(scratch);
   Workspace ws;
-  layout_workspace(static_cast<uint8_t*>(scratch) + kErrSlotBytes, num_seqs, hkv, group, cache->head_dim,
+  layout_workspace(static_cast<uint8_t*>(scratch) + kErrSlotBytes, num_seqs, hkv, gp, cache->head_dim,
                    max_dec_items, &ws);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   AttnArgs a{q,        k_cache,    v_cache,       *cache,      block_tables, max_blocks_per_seq, seq_lens,

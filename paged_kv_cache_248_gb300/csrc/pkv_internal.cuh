@@ -125,10 +125,11 @@ struct Workspace {
   int32_t* pre_prefix;   // [num_seqs + 1] exclusive prefix of prefill items
   int32_t* unit_arrive;  // [num_seqs * hkv] split arrivals per (request, kv head)
   int32_t* unit_bad;     // [num_seqs * hkv] a split saw a bad block id
-  float* part_ml;        // [max_dec_items * G * 2] split running max and sum
-  float* part_o;         // [max_dec_items * G * head_dim] split accumulators
+  float* part_ml;        // [max_dec_items * GP * 2] split running max and sum
+  float* part_o;         // [max_dec_items * head_dim * GP] split accumulators
 };
-// Computes the layout at `base` (nullptr: only the size) and returns the bytes needed.
+// Computes the layout at `base` (nullptr: only the size) and returns the bytes needed;
+// `group` is the padded head-group width GP the decode partials are stored with.
 size_t layout_workspace(void* base, int32_t num_seqs, int32_t hkv, int32_t group, int32_t head_dim,
                         int64_t max_dec_items, Workspace* ws);
 
