@@ -47,7 +47,7 @@ METRIC = "decode KV-read GB/s (% of HBM peak); mixed-step tokens/sec at 1 GB300"
 NCU_TRAFFIC = {
     "decode": {"ratio": 511.19 / 503.62,
                "sources": ("k_decode.cu", "ptx.cuh", "pkv_internal.cuh"),
-               "sha256": "ea9223297054b588d56ddfcb10bc31a96c039f975cf9dbe88d7f51825bed5bdc"},
+               "sha256": "552c6b8a17fa5386fe1fc0bac9075f1911952956423f69ab9167021856cd5b1e"},
 }
 
 

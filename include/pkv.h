@@ -200,7 +200,7 @@ PKV_API void pkv_shutdown(void);
  * by CUDA events on its stream.  pkv_trace_read() synchronises the device and
  * returns, per kernel kind, the launch count and the summed device time in ms,
  * then resets the counters.  Kinds: 0 slot mapping, 1 write, 2 copy, 3 plan,
- * 4 decode, 5 prefill, 6 generic attention.  Arrays hold PKV_TRACE_KINDS entries.
+ * 4 decode, 5 prefill, 6 generic attention, 7 split merge.  Arrays hold PKV_TRACE_KINDS entries.
  */
 #define PKV_TRACE_KINDS 8
 PKV_API int pkv_trace_enable(int on);

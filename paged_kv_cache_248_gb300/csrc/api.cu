@@ -84,7 +84,6 @@ size_t layout_workspace(void* base, int32_t num_seqs, int32_t hkv, int32_t group
   w.counters = static_cast<int32_t*>(take(kNumQueueCounters * sizeof(int32_t)));
   w.dec_prefix = static_cast<int32_t*>(take((static_cast<size_t>(num_seqs) + 1) * sizeof(int32_t)));
   w.pre_prefix = static_cast<int32_t*>(take((static_cast<size_t>(num_seqs) + 1) * sizeof(int32_t)));
-  w.unit_arrive = static_cast<int32_t*>(take(static_cast<size_t>(num_seqs) * hkv * sizeof(int32_t)));
   w.unit_bad = static_cast<int32_t*>(take(static_cast<size_t>(num_seqs) * hkv * sizeof(int32_t)));
   w.part_ml = static_cast<float*>(take(static_cast<size_t>(max_dec_items) * group * 2 * sizeof(float)));
   w.part_o = static_cast<float*>(take(static_cast<size_t>(max_dec_items) * group * head_dim * sizeof(float)));
@@ -150,7 +149,7 @@ std::vector<int> g_pending_kind;  // kind per used slot
 int64_t g_launches[PKV_TRACE_KINDS] = {};
 double g_ms[PKV_TRACE_KINDS] = {};
 const char* kTraceNames[PKV_TRACE_KINDS] = {"slot_mapping", "write", "copy_blocks", "plan",
-                                            "decode", "prefill", "generic_attention", "other"};
+                                            "decode", "prefill", "generic_attention", "merge"};
 }  // namespace
 
 TraceScope::TraceScope(int k, cudaStream_t s) : kind(k), stream(s), slot(-1) {
@@ -267,8 +266,8 @@ int paged_attention(const void* q, const void* k_cache, const void* v_cache, con
   Workspace ws;
   layout_workspace(ctx->ws, num_seqs, hkv, gp, cache->head_dim, max_dec_items, &ws);
   PlanArgs plan{seq_lens, query_start_loc, num_seqs, num_tokens, hkv, max_blocks_per_seq, max_seq_len,
-                kSplitKeys, kTileKeys / gp, ws.counters, ws.dec_prefix, ws.pre_prefix, ws.unit_arrive,
-                ws.unit_bad, ctx->err};
+                kSplitKeys, kTileKeys / gp, ws.counters, ws.dec_prefix, ws.pre_prefix, ws.unit_bad,
+                ctx->err};
   st = launch_plan(plan, s);
   if (st) return st;
   st = launch_decode_tc(a, ws, ctx->num_sms, ctx->err, s);

@@ -10,9 +10,9 @@
 // (request, kv head, split) items handed out by an atomic queue to persistent CTAs,
 // one per SM.  A split walks 128-key tiles (8 blocks).  A split that is the whole
 // request writes the output directly; otherwise it stores its fp32 partial
-// (running max, sum, unnormalised accumulator) and the last split to arrive
-// merges all partials in split order (log-sum-exp merge), so results never depend
-// on scheduling.
+// (running max, sum, unnormalised accumulator) and merge_kernel, launched right
+// after on the same stream, combines the partials in split order (log-sum-exp
+// merge), so results never depend on scheduling.
 //
 // Per CTA (224 threads):
 //   warp 6     scheduler: takes items off the queue ahead of use and resolves the
@@ -71,7 +71,6 @@ struct Ctl {
   float red[2][4][16];
   uint32_t tmem_base;
   int abort_flag;
-  int merge_flag;
 };
 
 constexpr int kSmemBytes = kStages * kStageBytes + 2 * kQBytes + 2 * kPBytes + static_cast<int>(sizeof(Ctl)) + 1024;
@@ -84,7 +83,6 @@ struct DecodeParams {
   const int32_t* qsl;
   const int32_t* dec_prefix;
   int32_t* queue;
-  int32_t* unit_arrive;
   int32_t* unit_bad;
   float* part_o;   // [items][128][GP]
   float* part_ml;  // [items][GP][2]
@@ -313,27 +311,6 @@ __device__ void mma_warp(const DecodeParams& P, Ctl& c, uint8_t* stages, uint8_t
   volatile int* abort_flag = &c.abort_flag;
   uint32_t it = 0, tc = 0, qc = 0;
   bool issued = false;
-
-  auto pv = [&](uint32_t cnt) -> bool {
-    const int st = cnt % kStages, b = cnt & 1;
-    const uint32_t ph = (cnt >> 1) & 1;
-    if (!mbar_wait(&c.p_full[b], ph, abort_flag) || !mbar_wait(&c.o_free[b], ph ^ 1, abort_flag)) return false;
-    tc_fence_after();
-    if (lane == 0) {
-      const uint64_t a = umma_smem_desc(smem_u32(stages + st * kStageBytes + kKBytes), kHalfBytes, 1024, kLayout128B);
-      const uint64_t bd = umma_smem_desc(smem_u32(pbuf + b * kPBytes), 128, 2048, kLayoutNone);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        umma_f16_ss(tmem + 32 + 16 * b, umma_desc_advance(a, kk * 2048), umma_desc_advance(bd, kk * 256), idesc_o,
-                    kk > 0);
-      umma_commit(&c.o_full[b]);
-      umma_commit(&c.p_free[b]);
-      umma_commit(&c.empty[st]);
-    }
-    __syncwarp();
-    return true;
-  };
-
   bool ok = true;
   while (ok) {
     const int slot = it % kRing;
@@ -350,31 +327,71 @@ __device__ void mma_warp(const DecodeParams& P, Ctl& c, uint8_t* stages, uint8_t
         ok = false;
         break;
       }
+      // Issue S^T(j) as soon as tile j has landed and its TMEM buffer is free, and
+      // O^T(j) = V^T P^T as soon as the softmax has written P(j): polled, so that neither
+      // kind of MMA waits behind the other (a late tile must not hold back the P V
+      // that frees an earlier stage).
       const int nt = (info.key_end - info.key_start + kTileKeys - 1) / kTileKeys;
-      for (int j = 0; j < nt && ok; ++j) {
-        const int st = tc % kStages, sb = tc & 1;
-        if (!mbar_wait(&c.full[st], (tc / kStages) & 1, abort_flag) ||
-            !mbar_wait(&c.s_free[sb], ((tc >> 1) & 1) ^ 1, abort_flag)) {
+      int ns = 0, npv = 0;
+      uint64_t t_last = globaltimer_ns();
+      while (npv < nt) {
+        bool progress = false;
+        if (ns < nt) {
+          const uint32_t cnt = tc + ns;
+          const int st = cnt % kStages, sb = cnt & 1;
+          bool ready = mbar_test(&c.full[st], (cnt / kStages) & 1) && mbar_test(&c.s_free[sb], ((cnt >> 1) & 1) ^ 1);
+          ready = __shfl_sync(0xffffffffu, ready, 0);
+          if (ready) {
+            tc_fence_after();
+            if (lane == 0) {
+              const uint64_t a = umma_smem_desc(smem_u32(stages + st * kStageBytes), 16, 1024, kLayout128B);
+              const uint64_t b = umma_smem_desc(smem_u32(qbuf + qb * kQBytes), 16, 1024, kLayout128B);
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk)
+                umma_f16_ss(tmem + 16 * sb, umma_desc_advance(a, (kk >> 2) * kHalfBytes + (kk & 3) * 32),
+                            umma_desc_advance(b, (kk >> 2) * 2048 + (kk & 3) * 32), idesc_s, kk > 0);
+              umma_commit(&c.s_full[sb]);
+              if (ns == nt - 1) umma_commit(&c.q_free[qb]);
+              issued = true;
+            }
+            __syncwarp();
+            ++ns;
+            progress = true;
+          }
+        }
+        if (npv < ns) {
+          const uint32_t cnt = tc + npv;
+          const int st = cnt % kStages, b = cnt & 1;
+          const uint32_t ph = (cnt >> 1) & 1;
+          bool ready = mbar_test(&c.p_full[b], ph) && mbar_test(&c.o_free[b], ph ^ 1);
+          ready = __shfl_sync(0xffffffffu, ready, 0);
+          if (ready) {
+            tc_fence_after();
+            if (lane == 0) {
+              const uint64_t a =
+                  umma_smem_desc(smem_u32(stages + st * kStageBytes + kKBytes), kHalfBytes, 1024, kLayout128B);
+              const uint64_t bd = umma_smem_desc(smem_u32(pbuf + b * kPBytes), 128, 2048, kLayoutNone);
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk)
+                umma_f16_ss(tmem + 32 + 16 * b, umma_desc_advance(a, kk * 2048), umma_desc_advance(bd, kk * 256),
+                            idesc_o, kk > 0);
+              umma_commit(&c.o_full[b]);
+              umma_commit(&c.p_free[b]);
+              umma_commit(&c.empty[st]);
+            }
+            __syncwarp();
+            ++npv;
+            progress = true;
+          }
+        }
+        if (progress) {
+          t_last = globaltimer_ns();
+        } else if (*abort_flag || globaltimer_ns() - t_last > kWaitTimeoutNs) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        if (lane == 0) {
-          const uint64_t a = umma_smem_desc(smem_u32(stages + st * kStageBytes), 16, 1024, kLayout128B);
-          const uint64_t b = umma_smem_desc(smem_u32(qbuf + qb * kQBytes), 16, 1024, kLayout128B);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_f16_ss(tmem + 16 * sb, umma_desc_advance(a, (kk >> 2) * kHalfBytes + (kk & 3) * 32),
-                        umma_desc_advance(b, (kk >> 2) * 2048 + (kk & 3) * 32), idesc_s, kk > 0);
-          umma_commit(&c.s_full[sb]);
-          if (j == nt - 1) umma_commit(&c.q_free[qb]);
-          issued = true;
-        }
-        __syncwarp();
-        if (j > 0 && !pv(tc - 1)) ok = false;
-        ++tc;
       }
-      if (ok && !pv(tc - 1)) ok = false;
+      tc += nt;
       ++qc;
     }
     if (!ok) break;
@@ -563,7 +580,8 @@ __device__ void softmax_warps(const DecodeParams& P, Ctl& c, uint8_t* stages, ui
       for (int g = 0; g < GP; ++g)
         if (g < G) orow[g * 128] = __float2bfloat16_rn(bad ? 0.f : acc[g] / lt[g]);
     } else {
-      // partials: accumulators [item][d][GP] (one float4 run per thread), max and sum [item][GP][2]
+      // partials: accumulators [item][d][GP] (one float4 run per thread), max and sum
+      // [item][GP][2]; the merge kernel that runs after this one combines them
       float4* po = reinterpret_cast<float4*>(P.part_o + (static_cast<int64_t>(info.idx) * 128 + r) * GP);
 #pragma unroll
       for (int k = 0; k < GP / 4; ++k) po[k] = make_float4(acc[4 * k], acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3]);
@@ -576,66 +594,6 @@ __device__ void softmax_warps(const DecodeParams& P, Ctl& c, uint8_t* stages, ui
         }
       }
       if (bad && r == 0) P.unit_bad[unit] = 1;
-      __threadfence();
-      if (!group_sync(c, gph)) {
-        ok = false;
-        break;
-      }
-      if (r == 0) {
-        const int old = atomicAdd(P.unit_arrive + unit, 1);
-        c.merge_flag = old == info.nsplit - 1;
-      }
-      if (!group_sync(c, gph)) {
-        ok = false;
-        break;
-      }
-      if (c.merge_flag) {
-        __threadfence();
-        const bool any_bad = *reinterpret_cast<volatile int*>(P.unit_bad + unit) != 0;
-        const int64_t base = info.idx - info.split;
-        // log-sum-exp merge in split order, one pass with a running maximum
-        float M[GP], num[GP], den[GP];
-#pragma unroll
-        for (int g = 0; g < GP; ++g) {
-          M[g] = -INFINITY;
-          num[g] = 0.f;
-          den[g] = 0.f;
-        }
-#pragma unroll 4
-        for (int s = 0; s < info.nsplit; ++s) {
-          const float4* ml4 = reinterpret_cast<const float4*>(P.part_ml + (base + s) * GP * 2);
-          const float4* o4 = reinterpret_cast<const float4*>(P.part_o + ((base + s) * 128 + r) * GP);
-          float ml[2 * GP], ov[GP];
-#pragma unroll
-          for (int k = 0; k < GP / 2; ++k) {
-            const float4 t = __ldcg(ml4 + k);
-            ml[4 * k] = t.x;
-            ml[4 * k + 1] = t.y;
-            ml[4 * k + 2] = t.z;
-            ml[4 * k + 3] = t.w;
-          }
-#pragma unroll
-          for (int k = 0; k < GP / 4; ++k) {
-            const float4 t = __ldcg(o4 + k);
-            ov[4 * k] = t.x;
-            ov[4 * k + 1] = t.y;
-            ov[4 * k + 2] = t.z;
-            ov[4 * k + 3] = t.w;
-          }
-#pragma unroll
-          for (int g = 0; g < GP; ++g) {
-            const float m_new = fmaxf(M[g], ml[2 * g]);
-            const float a = exp2f(M[g] - m_new);
-            const float b = exp2f(ml[2 * g] - m_new);
-            den[g] = fmaf(den[g], a, ml[2 * g + 1] * b);
-            num[g] = fmaf(num[g], a, ov[g] * b);
-            M[g] = m_new;
-          }
-        }
-#pragma unroll
-        for (int g = 0; g < GP; ++g)
-          if (g < G) orow[g * 128] = __float2bfloat16_rn(any_bad ? 0.f : num[g] / den[g]);
-      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&c.item_empty[slot]);
@@ -679,7 +637,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     mbar_init(&c.drain, 1);
     mbar_init(&c.group_bar, 4);
     c.abort_flag = 0;
-    c.merge_flag = 0;
     fence_mbar_init();
     tma_prefetch_map(&qmap);
     tma_prefetch_map(&kmap);
@@ -709,12 +666,95 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   }
 }
 
+// ------------------------------------------------------------------ split merge
+// Combines the partials of every (request, kv head) that was cut into several key
+// splits: log-sum-exp merge in split order, one CTA per unit (thread d = head element),
+// one pass with a running maximum and float4 loads.  Units of one split were written
+// by the decode kernel directly and are skipped.
+struct MergeParams {
+  __nv_bfloat16* out;
+  const int32_t* dec_prefix;
+  const int32_t* qsl;
+  const int32_t* unit_bad;
+  const float* part_o;
+  const float* part_ml;
+  int32_t num_seqs, hkv, group, hq;
+};
+
+template <int GP>
+__global__ void __launch_bounds__(128) merge_kernel(const MergeParams P) {
+  const int d = threadIdx.x;
+  const int64_t n_units = static_cast<int64_t>(P.num_seqs) * P.hkv;
+  for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
+    const int i = static_cast<int>(u / P.hkv), h = static_cast<int>(u % P.hkv);
+    const int base_i = __ldg(P.dec_prefix + i);
+    const int ns = (__ldg(P.dec_prefix + i + 1) - base_i) / P.hkv;
+    if (ns <= 1) continue;
+    const int64_t base = base_i + static_cast<int64_t>(h) * ns;
+    float M[GP], num[GP], den[GP];
+#pragma unroll
+    for (int g = 0; g < GP; ++g) {
+      M[g] = -INFINITY;
+      num[g] = 0.f;
+      den[g] = 0.f;
+    }
+#pragma unroll 4
+    for (int s = 0; s < ns; ++s) {
+      const float4* ml4 = reinterpret_cast<const float4*>(P.part_ml + (base + s) * GP * 2);
+      const float4* o4 = reinterpret_cast<const float4*>(P.part_o + ((base + s) * 128 + d) * GP);
+      float ml[2 * GP], ov[GP];
+#pragma unroll
+      for (int k = 0; k < GP / 2; ++k) {
+        const float4 t = __ldg(ml4 + k);
+        ml[4 * k] = t.x;
+        ml[4 * k + 1] = t.y;
+        ml[4 * k + 2] = t.z;
+        ml[4 * k + 3] = t.w;
+      }
+#pragma unroll
+      for (int k = 0; k < GP / 4; ++k) {
+        const float4 t = __ldg(o4 + k);
+        ov[4 * k] = t.x;
+        ov[4 * k + 1] = t.y;
+        ov[4 * k + 2] = t.z;
+        ov[4 * k + 3] = t.w;
+      }
+#pragma unroll
+      for (int g = 0; g < GP; ++g) {
+        const float m_new = fmaxf(M[g], ml[2 * g]);
+        const float a = exp2f(M[g] - m_new);
+        const float b = exp2f(ml[2 * g] - m_new);
+        den[g] = fmaf(den[g], a, ml[2 * g + 1] * b);
+        num[g] = fmaf(num[g], a, ov[g] * b);
+        M[g] = m_new;
+      }
+    }
+    const bool bad = __ldg(P.unit_bad + u) != 0;
+    const int64_t trow = __ldg(P.qsl + i);
+    __nv_bfloat16* orow = P.out + (trow * P.hq + static_cast<int64_t>(h) * P.group) * 128 + d;
+#pragma unroll
+    for (int g = 0; g < GP; ++g)
+      if (g < P.group) orow[g * 128] = __float2bfloat16_rn(bad ? 0.f : num[g] / den[g]);
+  }
+}
+
 template <int GP>
 int launch_gp(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& vm, const DecodeParams& p, int grid,
               cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(decode_kernel<GP>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return cuda_status(e);
-  decode_kernel<GP><<<grid, kThreads, kSmemBytes, s>>>(qm, km, vm, p);
+  {
+    TraceScope trace(kTraceDecode, s);
+    decode_kernel<GP><<<grid, kThreads, kSmemBytes, s>>>(qm, km, vm, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  MergeParams m{p.out, p.dec_prefix, p.qsl, p.unit_bad, p.part_o, p.part_ml, p.num_seqs, p.hkv, p.group, p.hq};
+  const int64_t n_units = static_cast<int64_t>(p.num_seqs) * p.hkv;
+  const int64_t cap = static_cast<int64_t>(grid) * 8;
+  const int mgrid = static_cast<int>(n_units < cap ? n_units : cap);
+  TraceScope trace(kTraceMerge, s);
+  merge_kernel<GP><<<mgrid, 128, 0, s>>>(m);
   return cuda_status(cudaGetLastError());
 }
 
@@ -746,7 +786,6 @@ int launch_decode_tc(const AttnArgs& a, const Workspace& ws, int num_sms, uint32
   p.qsl = a.qsl;
   p.dec_prefix = ws.dec_prefix;
   p.queue = ws.counters + 0;
-  p.unit_arrive = ws.unit_arrive;
   p.unit_bad = ws.unit_bad;
   p.part_o = ws.part_o;
   p.part_ml = ws.part_ml;
@@ -761,7 +800,6 @@ int launch_decode_tc(const AttnArgs& a, const Workspace& ws, int num_sms, uint32
   p.hq = a.num_q_heads;
   p.split_keys = kSplitKeys;
   p.scale_log2 = a.scale * 1.4426950408889634f;
-  TraceScope trace(kTraceDecode, s);
   if (gp == 4) return launch_gp<4>(qm, km, vm, p, num_sms, s);
   if (gp == 8) return launch_gp<8>(qm, km, vm, p, num_sms, s);
   return launch_gp<16>(qm, km, vm, p, num_sms, s);

@@ -9,8 +9,8 @@
 //                    ceil(q_len / rows_per_tile) (kv head, query tile) items.
 // Split boundaries depend only on a request's own length and a library constant,
 // so a request's result does not depend on what else is in the batch.  It also
-// zeroes the work-queue counters and the per-(request, kv head) arrival counters
-// and bad-block flags used by the split merge.  Lengths that contradict the host
+// zeroes the work-queue counters and the per-(request, kv head) bad-block flags
+// used by the split merge.  Lengths that contradict the host
 // bounds become a single item that reports the error and zeroes its output.
 #include "pkv_internal.cuh"
 
@@ -58,7 +58,6 @@ __device__ void block_scan2(int a, int b, int& ex_a, int& ex_b, int& tot_a, int&
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs p) {
   const int64_t n_units = static_cast<int64_t>(p.num_seqs) * p.hkv;
   for (int64_t u = threadIdx.x; u < n_units; u += blockDim.x) {
-    p.unit_arrive[u] = 0;
     p.unit_bad[u] = 0;
   }
   if (threadIdx.x < kNumQueueCounters) p.counters[threadIdx.x] = 0;

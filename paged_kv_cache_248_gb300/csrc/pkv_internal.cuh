@@ -5,7 +5,7 @@
 #include <cuda_runtime.h>
 #include <cstdint>
 
-#include "../../include/pkv.h"
+#include "pkv.h"
 
 namespace pkv {
 
@@ -32,6 +32,7 @@ enum TraceKind : int {
   kTraceDecode = 4,
   kTracePrefill = 5,
   kTraceGeneric = 6,
+  kTraceMerge = 7,
 };
 
 __device__ __forceinline__ void flag_error(uint32_t* err, uint32_t bits) {
@@ -123,7 +124,6 @@ struct Workspace {
   int32_t* counters;     // [kNumQueueCounters] work-queue heads
   int32_t* dec_prefix;   // [num_seqs + 1] exclusive prefix of decode items
   int32_t* pre_prefix;   // [num_seqs + 1] exclusive prefix of prefill items
-  int32_t* unit_arrive;  // [num_seqs * hkv] split arrivals per (request, kv head)
   int32_t* unit_bad;     // [num_seqs * hkv] a split saw a bad block id
   float* part_ml;        // [max_dec_items * GP * 2] split running max and sum
   float* part_o;         // [max_dec_items * head_dim * GP] split accumulators
@@ -146,7 +146,6 @@ struct PlanArgs {
   int32_t* counters;
   int32_t* dec_prefix;
   int32_t* pre_prefix;
-  int32_t* unit_arrive;
   int32_t* unit_bad;
   uint32_t* err;
 };
