@@ -40,14 +40,14 @@ METRIC = "decode KV-read GB/s (% of HBM peak); mixed-step tokens/sec at 1 GB300"
 
 
 # DRAM traffic of the decode kernel per algorithmic byte, from one ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum = 505.63 MB + 5.56 MB for 503.62 MB of
+# (dram__bytes_read.sum + dram__bytes_write.sum = 505.31 MB + 5.19 MB for 503.62 MB of
 # algorithmic bytes, batched-decode workload; profiles/decode_kernel_batched_decode.md).
 # It scales to other workloads by the bytes processed, and it is reported only while
 # the profiled sources are unchanged.
 NCU_TRAFFIC = {
-    "decode": {"ratio": 511.19 / 503.62,
+    "decode": {"ratio": 510.50 / 503.62,
                "sources": ("k_decode.cu", "ptx.cuh", "pkv_internal.cuh"),
-               "sha256": "552c6b8a17fa5386fe1fc0bac9075f1911952956423f69ab9167021856cd5b1e"},
+               "sha256": "59edfe19fc3bb1292c7558d47427b60f6cf693d0f3623158fdf56f7882102d40"},
 }
 
 

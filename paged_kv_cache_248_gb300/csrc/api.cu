@@ -85,6 +85,7 @@ size_t layout_workspace(void* base, int32_t num_seqs, int32_t hkv, int32_t group
   w.dec_prefix = static_cast<int32_t*>(take((static_cast<size_t>(num_seqs) + 1) * sizeof(int32_t)));
   w.pre_prefix = static_cast<int32_t*>(take((static_cast<size_t>(num_seqs) + 1) * sizeof(int32_t)));
   w.unit_bad = static_cast<int32_t*>(take(static_cast<size_t>(num_seqs) * hkv * sizeof(int32_t)));
+  w.merge_list = static_cast<int32_t*>(take(static_cast<size_t>(num_seqs) * sizeof(int32_t)));
   w.part_ml = static_cast<float*>(take(static_cast<size_t>(max_dec_items) * group * 2 * sizeof(float)));
   w.part_o = static_cast<float*>(take(static_cast<size_t>(max_dec_items) * group * head_dim * sizeof(float)));
   if (ws) *ws = w;
@@ -267,7 +268,7 @@ int paged_attention(const void* q, const void* k_cache, const void* v_cache, con
   layout_workspace(ctx->ws, num_seqs, hkv, gp, cache->head_dim, max_dec_items, &ws);
   PlanArgs plan{seq_lens, query_start_loc, num_seqs, num_tokens, hkv, max_blocks_per_seq, max_seq_len,
                 kSplitKeys, kTileKeys / gp, ws.counters, ws.dec_prefix, ws.pre_prefix, ws.unit_bad,
-                ctx->err};
+                ws.merge_list, ctx->err};
   st = launch_plan(plan, s);
   if (st) return st;
   st = launch_decode_tc(a, ws, ctx->num_sms, ctx->err, s);

@@ -5,8 +5,9 @@
 // 16-token blocks live): for a decode request i (one query token at position
 // seq_len - 1) and kv head h, the G query heads of h attend to all seq_len keys.
 //
-// Work decomposition.  Each (request, kv head) is cut into key splits of
-// kSplitKeys keys (a function of the request's own length only), giving
+// Work decomposition.  Each (request, kv head) is cut into key splits
+// (decode_splits: none up to kNoSplitKeys keys, else kSplitKeys-key pieces -- a
+// function of the request's own length only), giving
 // (request, kv head, split) items handed out by an atomic queue to persistent CTAs,
 // one per SM.  A split walks 128-key tiles (8 blocks).  A split that is the whole
 // request writes the output directly; otherwise it stores its fp32 partial
@@ -47,7 +48,7 @@ constexpr int kStageBytes = 2 * kKBytes;      // K + V
 constexpr int kQBytes = 4096;                 // Q: [2 halves][16 rows][128 B]
 constexpr int kPBytes = 4096;                 // P^T: 128 keys x 16 heads, MN-major, no swizzle
 constexpr int kRing = 3;                      // ring of items prepared by the scheduler
-constexpr int kMaxIds = kSplitKeys / kBlock;  // block ids of one item
+constexpr int kMaxIds = kNoSplitKeys / kBlock;  // block ids of one item (the longest item is unsplit)
 constexpr uint32_t kTmemCols = 64;            // S^T x2 (cols 0, 16), O^T x2 (cols 32, 48)
 constexpr int kBlocksPerTile = kTileKeys / kBlock;
 
@@ -201,12 +202,17 @@ __device__ void scheduler_warp(const DecodeParams& P, Ctl& c) {
       r.split = local % nsplit;
       r.nsplit = nsplit;
       const bool ok = r.row_ok && L >= 1 && (L + kBlock - 1) / kBlock <= P.max_blocks &&
-                      static_cast<int64_t>(nsplit) == (L + P.split_keys - 1) / P.split_keys;
+                      static_cast<int64_t>(nsplit) == decode_splits(L);
       if (ok) {
         r.valid = 1;
-        r.key_start = r.split * P.split_keys;
-        const int64_t split_end = static_cast<int64_t>(r.key_start) + P.split_keys;
-        r.key_end = static_cast<int32_t>(L < split_end ? L : split_end);
+        if (nsplit == 1) {
+          r.key_start = 0;
+          r.key_end = static_cast<int32_t>(L);
+        } else {
+          r.key_start = r.split * P.split_keys;
+          const int64_t split_end = static_cast<int64_t>(r.key_start) + P.split_keys;
+          r.key_end = static_cast<int32_t>(L < split_end ? L : split_end);
+        }
       }
     }
     int bad = 0;
@@ -668,11 +674,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
 
 // ------------------------------------------------------------------ split merge
 // Combines the partials of every (request, kv head) that was cut into several key
-// splits: log-sum-exp merge in split order, one CTA per unit (thread d = head element),
-// one pass with a running maximum and float4 loads.  Units of one split were written
-// by the decode kernel directly and are skipped.
+// splits -- the planner lists those requests -- by a log-sum-exp merge in split
+// order, one CTA per unit (thread d = head element), one pass with a running
+// maximum and float4 loads.  Requests of one split were written by the decode kernel.
 struct MergeParams {
   __nv_bfloat16* out;
+  const int32_t* counters;
+  const int32_t* merge_list;
   const int32_t* dec_prefix;
   const int32_t* qsl;
   const int32_t* unit_bad;
@@ -684,9 +692,10 @@ struct MergeParams {
 template <int GP>
 __global__ void __launch_bounds__(128) merge_kernel(const MergeParams P) {
   const int d = threadIdx.x;
-  const int64_t n_units = static_cast<int64_t>(P.num_seqs) * P.hkv;
-  for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x) {
-    const int i = static_cast<int>(u / P.hkv), h = static_cast<int>(u % P.hkv);
+  const int64_t n_units = static_cast<int64_t>(P.counters[kMergeCountSlot]) * P.hkv;
+  for (int64_t e = blockIdx.x; e < n_units; e += gridDim.x) {
+    const int i = __ldg(P.merge_list + e / P.hkv), h = static_cast<int>(e % P.hkv);
+    const int64_t u = static_cast<int64_t>(i) * P.hkv + h;
     const int base_i = __ldg(P.dec_prefix + i);
     const int ns = (__ldg(P.dec_prefix + i + 1) - base_i) / P.hkv;
     if (ns <= 1) continue;
@@ -740,7 +749,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeParams P) {
 
 template <int GP>
 int launch_gp(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& vm, const DecodeParams& p, int grid,
-              cudaStream_t s) {
+              const int32_t* counters, const int32_t* merge_list, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(decode_kernel<GP>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return cuda_status(e);
   {
@@ -749,9 +758,12 @@ int launch_gp(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& v
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_status(e);
   }
-  MergeParams m{p.out, p.dec_prefix, p.qsl, p.unit_bad, p.part_o, p.part_ml, p.num_seqs, p.hkv, p.group, p.hq};
+  MergeParams m{p.out,       counters,  merge_list, p.dec_prefix, p.qsl,    p.unit_bad,
+                p.part_o,    p.part_ml, p.num_seqs, p.hkv,        p.group,  p.hq};
+  // the list length is only known on the device: enough CTAs for every unit of a
+  // full list, each exiting at once when the list is shorter
   const int64_t n_units = static_cast<int64_t>(p.num_seqs) * p.hkv;
-  const int64_t cap = static_cast<int64_t>(grid) * 8;
+  const int64_t cap = static_cast<int64_t>(grid) * 4;
   const int mgrid = static_cast<int>(n_units < cap ? n_units : cap);
   TraceScope trace(kTraceMerge, s);
   merge_kernel<GP><<<mgrid, 128, 0, s>>>(m);
@@ -800,9 +812,9 @@ int launch_decode_tc(const AttnArgs& a, const Workspace& ws, int num_sms, uint32
   p.hq = a.num_q_heads;
   p.split_keys = kSplitKeys;
   p.scale_log2 = a.scale * 1.4426950408889634f;
-  if (gp == 4) return launch_gp<4>(qm, km, vm, p, num_sms, s);
-  if (gp == 8) return launch_gp<8>(qm, km, vm, p, num_sms, s);
-  return launch_gp<16>(qm, km, vm, p, num_sms, s);
+  if (gp == 4) return launch_gp<4>(qm, km, vm, p, num_sms, ws.counters, ws.merge_list, s);
+  if (gp == 8) return launch_gp<8>(qm, km, vm, p, num_sms, ws.counters, ws.merge_list, s);
+  return launch_gp<16>(qm, km, vm, p, num_sms, ws.counters, ws.merge_list, s);
 }
 
 }  // namespace pkv

@@ -4,13 +4,13 @@
 // computed / total tokens, and one step mixes decodes and prefill chunks) and
 // writes two work lists as exclusive prefix sums over the requests:
 //   decode items  -- requests with exactly one query token: num_kv_heads x
-//                    ceil(seq_len / split_keys) (kv head, key split) items;
+//                    decode_splits(seq_len) (kv head, key split) items;
 //   prefill items -- requests with more query tokens: num_kv_heads x
 //                    ceil(q_len / rows_per_tile) (kv head, query tile) items.
 // Split boundaries depend only on a request's own length and a library constant,
 // so a request's result does not depend on what else is in the batch.  It also
 // zeroes the work-queue counters and the per-(request, kv head) bad-block flags
-// used by the split merge.  Lengths that contradict the host
+// used by the split merge, and lists the requests whose splits need merging.  Lengths that contradict the host
 // bounds become a single item that reports the error and zeroes its output.
 #include "pkv_internal.cuh"
 
@@ -29,29 +29,30 @@ __device__ __forceinline__ int warp_inclusive_scan(int v) {
   return v;
 }
 
-// Block-wide exclusive scan of two counters at once.
-__device__ void block_scan2(int a, int b, int& ex_a, int& ex_b, int& tot_a, int& tot_b) {
-  __shared__ int wa[32], wb[32];
+// Block-wide exclusive scan of three counters at once.
+__device__ void block_scan3(const int (&v)[3], int (&ex)[3], int (&tot)[3]) {
+  __shared__ int ws[3][32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-  const int ia = warp_inclusive_scan(a), ib = warp_inclusive_scan(b);
-  if (lane == 31) {
-    wa[warp] = ia;
-    wb[warp] = ib;
+  int inc[3];
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    inc[k] = warp_inclusive_scan(v[k]);
+    if (lane == 31) ws[k][warp] = inc[k];
   }
   __syncthreads();
   if (warp == 0) {
-    int x = lane < nwarps ? wa[lane] : 0;
-    int y = lane < nwarps ? wb[lane] : 0;
-    x = warp_inclusive_scan(x);
-    y = warp_inclusive_scan(y);
-    wa[lane] = x;
-    wb[lane] = y;
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+      int x = lane < nwarps ? ws[k][lane] : 0;
+      ws[k][lane] = warp_inclusive_scan(x);
+    }
   }
   __syncthreads();
-  ex_a = (warp ? wa[warp - 1] : 0) + ia - a;
-  ex_b = (warp ? wb[warp - 1] : 0) + ib - b;
-  tot_a = wa[nwarps - 1];
-  tot_b = wb[nwarps - 1];
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    ex[k] = (warp ? ws[k][warp - 1] : 0) + inc[k] - v[k];
+    tot[k] = ws[k][nwarps - 1];
+  }
   __syncthreads();
 }
 
@@ -61,10 +62,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs p) {
     p.unit_bad[u] = 0;
   }
   if (threadIdx.x < kNumQueueCounters) p.counters[threadIdx.x] = 0;
-  int carry_d = 0, carry_p = 0;
+  __syncthreads();
+  int carry_d = 0, carry_p = 0, carry_m = 0;
   for (int base = 0; base < p.num_seqs; base += blockDim.x) {
     const int i = base + threadIdx.x;
-    int nd = 0, np = 0;
+    int nd = 0, np = 0, nm = 0;
     if (i < p.num_seqs) {
       const int64_t q0 = p.qsl[i], q1 = p.qsl[i + 1];
       const int64_t L = p.seq_lens[i];
@@ -74,23 +76,29 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs p) {
         flag_error(p.err, kErrLength);  // rows cannot be addressed: no item
       } else if (q_len == 1) {
         const bool ok = L >= 1 && L <= p.max_seq_len && (L + kBlock - 1) / kBlock <= p.max_blocks;
-        nd = p.hkv * (ok ? static_cast<int>((L + p.split_keys - 1) / p.split_keys) : 1);
+        const int ns = ok ? static_cast<int>(decode_splits(L)) : 1;
+        nd = p.hkv * ns;
+        nm = ns > 1 ? 1 : 0;  // its partials need the split merge
       } else if (q_len > 1) {
         np = p.hkv * static_cast<int>((q_len + p.rows_per_tile - 1) / p.rows_per_tile);
       }
     }
-    int ed, ep, td, tp;
-    block_scan2(nd, np, ed, ep, td, tp);
+    const int v[3] = {nd, np, nm};
+    int ex[3], tot[3];
+    block_scan3(v, ex, tot);
     if (i < p.num_seqs) {
-      p.dec_prefix[i] = carry_d + ed;
-      p.pre_prefix[i] = carry_p + ep;
+      p.dec_prefix[i] = carry_d + ex[0];
+      p.pre_prefix[i] = carry_p + ex[1];
+      if (nm) p.merge_list[carry_m + ex[2]] = i;
     }
-    carry_d += td;
-    carry_p += tp;
+    carry_d += tot[0];
+    carry_p += tot[1];
+    carry_m += tot[2];
   }
   if (threadIdx.x == 0) {
     p.dec_prefix[p.num_seqs] = carry_d;
     p.pre_prefix[p.num_seqs] = carry_p;
+    p.counters[kMergeCountSlot] = carry_m;
   }
 }
 

@@ -21,7 +21,15 @@ enum : uint32_t {
 
 constexpr int kTileKeys = 128;       // keys per tensor-core tile (8 blocks)
 constexpr int kSplitKeys = 1024;     // decode key-split length (a multiple of kTileKeys)
+constexpr int kNoSplitKeys = 2048;   // decode contexts up to this length are never split
+
+// Key splits of a decode request of context length L: a function of L alone, so
+// a request's result does not depend on the rest of the batch.
+__host__ __device__ inline int64_t decode_splits(int64_t L) {
+  return L <= kNoSplitKeys ? 1 : (L + kSplitKeys - 1) / kSplitKeys;
+}
 constexpr int kNumQueueCounters = 8; // work-queue counters in the workspace
+constexpr int kMergeCountSlot = 2;   // counters[2]: number of requests in the merge list
 
 // Trace kinds (pkv_trace_read).
 enum TraceKind : int {
@@ -125,6 +133,7 @@ struct Workspace {
   int32_t* dec_prefix;   // [num_seqs + 1] exclusive prefix of decode items
   int32_t* pre_prefix;   // [num_seqs + 1] exclusive prefix of prefill items
   int32_t* unit_bad;     // [num_seqs * hkv] a split saw a bad block id
+  int32_t* merge_list;   // [num_seqs] decode requests cut into several splits
   float* part_ml;        // [max_dec_items * GP * 2] split running max and sum
   float* part_o;         // [max_dec_items * head_dim * GP] split accumulators
 };
@@ -147,6 +156,7 @@ struct PlanArgs {
   int32_t* dec_prefix;
   int32_t* pre_prefix;
   int32_t* unit_bad;
+  int32_t* merge_list;
   uint32_t* err;
 };
 int launch_plan(const PlanArgs& p, cudaStream_t s);

@@ -60,7 +60,8 @@ def test_random_mixed_bf16(pkv, seed, group, hkv):
     run_pair(pkv, w)
 
 
-@pytest.mark.parametrize("lens", [[1], [16], [17], [128], [129], [255, 256, 257], [1024, 1, 2049]])
+@pytest.mark.parametrize("lens", [[1], [16], [17], [128], [129], [255, 256, 257], [1024, 1, 2049],
+                                  [2047, 2048, 4097, 3073]])
 def test_decode_edge_lengths_bf16(pkv, lens):
     w = wl.sized_case(21, lens, [1] * len(lens), 32, 8, 128, "bf16")
     run_pair(pkv, w)
