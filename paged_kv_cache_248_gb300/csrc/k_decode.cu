@@ -405,8 +405,10 @@ __device__ void mma_warp(const DecodeParams& P, Ctl& c, uint8_t* stages, uint8_t
     if (lane == 0) mbar_arrive(&c.item_empty[slot]);
   }
   if (!ok && !*abort_flag && lane == 0) raise_abort(c, P.err);
-  if (!ok && issued && lane == 0) {
-    umma_commit(&c.drain);  // wait for every MMA issued so far before TMEM is freed
+  if (issued && lane == 0) {
+    // every MMA issued so far, and the barrier arrivals its commits trigger, must be
+    // complete before TMEM is freed and the CTA's shared memory goes away
+    umma_commit(&c.drain);
     mbar_wait(&c.drain, 0, nullptr);
   }
   __syncwarp();

@@ -22,7 +22,8 @@
 //   warps 2-5  softmax: thread r owns row r.  It loads its S row from TMEM, applies
 //              the causal mask, and keeps a per-row reference maximum; only when a
 //              row's maximum grows by more than 2^8 does the warp rescale its O rows
-//              in TMEM (after the previous P V has landed).  P is written as bf16 into
+//              in TMEM.  It observes every P V completion in order (mbarrier parity
+//              waits must not skip a phase) before handing over the next P.  P is written as bf16 into
 //              a swizzled K-major operand.  The final O / l is stored per row.
 // All waits are bounded (see ptx.cuh); a timeout raises the CTA abort flag.
 #include "ptx.cuh"
@@ -285,7 +286,9 @@ __device__ void mma_warp(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uint8_t*
     if (lane == 0) mbar_arrive(&c.item_empty[slot]);
   }
   if (!ok && !*abort_flag && lane == 0) raise_abort(c, P.err);
-  if (!ok && issued && lane == 0) {
+  if (issued && lane == 0) {
+    // every MMA issued so far, and the barrier arrivals its commits trigger, must be
+    // complete before TMEM is freed and the CTA's shared memory goes away
     umma_commit(&c.drain);
     mbar_wait(&c.drain, 0, nullptr);
   }
@@ -366,13 +369,16 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* stages, u
       if (j == 0) {
         m_ref = tmax;  // key 0 is visible to every row, so this is finite
       } else {
+        // Observe P V(j-1) complete before handing over P(j).  Every phase of o_full
+        // must be waited for in order: a parity wait that skips a phase could match
+        // the parity of an older completed phase and return before the MMA is done.
+        if (!mbar_wait(&c.o_full, (tc - 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
         const bool need = tmax > m_ref + kRescaleThreshold;
         if (__any_sync(0xffffffffu, need)) {
-          // rescale this warp's O rows once the previous P V has landed
-          if (!mbar_wait(&c.o_full, (tc - 1) & 1, abort_flag)) {
-            ok = false;
-            break;
-          }
+          // rescale this warp's O rows (P V(j-1) has landed)
           tc_fence_after();
           const float m_new = need ? tmax : m_ref;
           const float alpha = exp2f(m_ref - m_new);

@@ -67,7 +67,14 @@ def compare(got: torch.Tensor, ref: np.ndarray, dtype: str, what: str = ""):
     assert g.shape == ref.shape, (g.shape, ref.shape)
     err = np.abs(g - ref)
     max_tol, mean_tol = TOL[dtype]
-    assert np.isfinite(g).all(), f"{what}: non-finite output"
-    assert err.max() <= max_tol, f"{what}: max-abs {err.max():.3e} > {max_tol}"
+
+    def where():
+        rows = err.reshape(err.shape[0], -1).max(axis=1) if err.ndim > 1 else err
+        bad = np.nonzero(rows > max_tol)[0]
+        heads = sorted(set(np.nonzero(err[bad].max(axis=-1) > max_tol)[1].tolist())) if err.ndim == 3 and len(bad) else []
+        return f" ({len(bad)} rows over tolerance, first {bad[:12].tolist()}, heads {heads[:16]})"
+
+    assert np.isfinite(g).all(), f"{what}: non-finite output" + where()
+    assert err.max() <= max_tol, f"{what}: max-abs {err.max():.3e} > {max_tol}" + where()
     assert err.mean() <= mean_tol, f"{what}: mean-abs {err.mean():.3e} > {mean_tol}"
     return float(err.max()), float(err.mean())

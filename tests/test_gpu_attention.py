@@ -240,6 +240,23 @@ def test_mixed_batch_equals_separate_calls_bitwise(pkv):
         assert torch.equal(one, whole[qsl[i]:qsl[i + 1]]), i
 
 
+@pytest.mark.parametrize("seed,group,hkv", [(13, 1, 4), (14, 2, 2), (16, 4, 8), (17, 8, 2)])
+def test_repeated_calls_match_oracle_and_each_other(pkv, seed, group, hkv):
+    # Which CTA runs which item, and when, changes from call to call; the results must
+    # not.  Repetition also exposes ordering races inside a CTA's pipeline.
+    w = wl.random_case(seed, num_seqs=10, max_ctx=1500, max_q=300, group=group, num_kv_heads=hkv,
+                       head_dim=128, dtype="bf16")
+    t_cpu = w.make_tensors("cpu")
+    t = {k: v.cuda() for k, v in t_cpu.items()}
+    _, slots, st = gpu_step(pkv, w, t)
+    assert st == 0
+    ref, _, kc, vc = oracle_step(w, t_cpu)
+    outs = [_attention_only(pkv, w, t) for _ in range(6)]
+    for o in outs:
+        compare(o, ref, "bf16", w.name)
+        assert torch.equal(o, outs[0])
+
+
 # --------------------------------------------------------------------------- device errors
 
 def test_bad_block_id_zeroes_only_that_request(pkv):
