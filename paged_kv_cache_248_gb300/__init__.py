@@ -213,3 +213,101 @@ def pkv_umma_selftest(params, a_img: torch.Tensor, b_img: torch.Tensor, d_out: t
 def pkv_tma_selftest(src: torch.Tensor, row0: int, dump: torch.Tensor, stream=None) -> None:
     _check(lib().pkv_tma_selftest(_dev(src, "src", torch.bfloat16), src.shape[0], int(row0), _dev(dump, "dump"),
                                   _stream(stream)), "pkv_tma_selftest")
+
+
+# ----------------------------------------------------------------------------- block manager
+class BlockManager:
+    """Host-side KV block manager in libpkv (C ABI in include/pkv_blocks.h): a pool of
+    16-token blocks with a free queue, reference counts, chained hashing of full blocks
+    for prefix reuse, fork and copy-on-write.  Argument marshalling only."""
+
+    def __init__(self, num_blocks: int, enable_prefix_cache: bool = True):
+        L = lib()
+        if not getattr(L, "_bm_ready", False):
+            P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+            I32P = ctypes.POINTER(ctypes.c_int32)
+            I64P = ctypes.POINTER(ctypes.c_int64)
+            L.pkv_bm_create.argtypes, L.pkv_bm_create.restype = [i64, i32], P
+            L.pkv_bm_destroy.argtypes, L.pkv_bm_destroy.restype = [P], None
+            L.pkv_bm_num_free.argtypes, L.pkv_bm_num_free.restype = [P], i64
+            L.pkv_bm_get_computed_blocks.argtypes = [P, i64, I32P, i64]
+            L.pkv_bm_allocate_slots.argtypes = [P, i64, i64]
+            L.pkv_bm_cache_full_blocks.argtypes = [P, i64, I32P, i64]
+            L.pkv_bm_block_table.argtypes = [P, i64, I32P, i32]
+            L.pkv_bm_free.argtypes = [P, i64]
+            L.pkv_bm_fork.argtypes = [P, i64, i64]
+            L.pkv_bm_cow.argtypes = [P, i64, i32, I32P, I32P]
+            L.pkv_bm_usage.argtypes = [P, I64P, I64P, I64P]
+            L.pkv_bm_block_hash.argtypes, L.pkv_bm_block_hash.restype = [ctypes.c_uint64, I32P, ctypes.c_uint64], \
+                ctypes.c_uint64
+            for f in ("pkv_bm_get_computed_blocks", "pkv_bm_allocate_slots", "pkv_bm_cache_full_blocks",
+                      "pkv_bm_block_table", "pkv_bm_free", "pkv_bm_fork", "pkv_bm_cow", "pkv_bm_usage"):
+                getattr(L, f).restype = ctypes.c_int32
+            L._bm_ready = True
+        self._L = L
+        self._h = L.pkv_bm_create(int(num_blocks), 1 if enable_prefix_cache else 0)
+        if not self._h:
+            raise ValueError("bad block manager arguments")
+
+    def __del__(self):
+        h, self._h = getattr(self, "_h", None), None
+        if h:
+            self._L.pkv_bm_destroy(h)
+
+    @staticmethod
+    def _i32(tokens):
+        import numpy as np
+        a = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+        return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+    def _ok(self, rc: int, what: str) -> int:
+        if rc in (-2, -3):
+            raise ValueError(f"{what}: {'unknown or duplicate request' if rc == -2 else 'bad argument'}")
+        return rc
+
+    @property
+    def num_free(self) -> int:
+        return int(self._L.pkv_bm_num_free(self._h))
+
+    def get_computed_blocks(self, req: int, tokens) -> int:
+        a, p = self._i32(tokens)
+        return self._ok(self._L.pkv_bm_get_computed_blocks(self._h, req, p, a.size), "get_computed_blocks")
+
+    def allocate_slots(self, req: int, total_tokens: int):
+        """Number of blocks added, or None when the pool cannot cover the tokens."""
+        rc = self._ok(self._L.pkv_bm_allocate_slots(self._h, req, int(total_tokens)), "allocate_slots")
+        return None if rc == -1 else rc
+
+    def cache_full_blocks(self, req: int, tokens) -> int:
+        a, p = self._i32(tokens)
+        return self._ok(self._L.pkv_bm_cache_full_blocks(self._h, req, p, a.size), "cache_full_blocks")
+
+    def block_table(self, req: int) -> list:
+        n = self._ok(self._L.pkv_bm_block_table(self._h, req, None, 0), "block_table")
+        out = (ctypes.c_int32 * max(n, 1))()
+        self._L.pkv_bm_block_table(self._h, req, out, n)
+        return list(out[:n])
+
+    def free(self, req: int) -> None:
+        self._ok(self._L.pkv_bm_free(self._h, req), "free")
+
+    def fork(self, parent: int, child: int) -> None:
+        self._ok(self._L.pkv_bm_fork(self._h, parent, child), "fork")
+
+    def cow(self, req: int, logical_block: int):
+        """(src, dst) when the block was shared and is now a private copy, () when it was
+        already exclusive, None when no block is free."""
+        s, d = ctypes.c_int32(0), ctypes.c_int32(0)
+        rc = self._ok(self._L.pkv_bm_cow(self._h, req, int(logical_block), ctypes.byref(s), ctypes.byref(d)), "cow")
+        return None if rc == -1 else ((s.value, d.value) if rc == 1 else ())
+
+    def usage(self) -> dict:
+        b, t, u = ctypes.c_int64(0), ctypes.c_int64(0), ctypes.c_int64(0)
+        self._L.pkv_bm_usage(self._h, ctypes.byref(b), ctypes.byref(t), ctypes.byref(u))
+        return {"blocks_in_use": b.value, "tokens_held": t.value, "unused_slots": u.value}
+
+    def block_hash(self, parent: int, tokens16, extra: int = 0) -> int:
+        a, p = self._i32(tokens16)
+        if a.size != BLOCK_SIZE:
+            raise ValueError("a block holds 16 tokens")
+        return int(self._L.pkv_bm_block_hash(ctypes.c_uint64(parent), p, ctypes.c_uint64(extra)))

@@ -32,13 +32,16 @@ def _nvcc() -> str:
     return cand
 
 
+CXX_FLAGS = ["-O2", "-std=c++17", "-fPIC", "-fvisibility=hidden", f"-I{INCLUDE}"]
+
+
 def sources() -> list[str]:
-    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
+    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cu", ".cpp")))
 
 
 def _headers_mtime() -> float:
     hs = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
-    hs.append(os.path.join(INCLUDE, "pkv.h"))
+    hs += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")]
     return max(os.path.getmtime(h) for h in hs)
 
 
@@ -50,11 +53,14 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
     flags = NVCC_FLAGS + (extra_flags or [])
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(OUT_DIR, os.path.splitext(os.path.basename(src))[0] + ".o")
         if (not force and os.path.exists(obj) and os.path.getmtime(obj) >= os.path.getmtime(src)
                 and os.path.getmtime(obj) >= hdr):
             return obj
-        cmd = [nvcc, *ARCH, *flags, "-c", src, "-o", obj + ".tmp"]
+        if src.endswith(".cpp"):  # host-only C++ (block manager)
+            cmd = [shutil.which("g++") or "g++", *CXX_FLAGS, "-c", src, "-o", obj + ".tmp"]
+        else:
+            cmd = [nvcc, *ARCH, *flags, "-c", src, "-o", obj + ".tmp"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {os.path.basename(src)}:\n{r.stdout}\n{r.stderr}")

@@ -8,6 +8,7 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "pkv.h")
+BLOCKS_HEADER = os.path.join(ROOT, "include", "pkv_blocks.h")
 
 
 @pytest.fixture(scope="module")
@@ -18,9 +19,9 @@ def lib():
     return pkv.lib()
 
 
-def declared_symbols():
-    text = open(HEADER).read()
-    return sorted(set(re.findall(r"^PKV_API\s+[\w\s\*]+?\b(\w+)\(", text, flags=re.M)))
+def declared_symbols(header=HEADER, macro="PKV_API"):
+    text = open(header).read()
+    return sorted(set(re.findall(rf"^{macro}\s+[\w\s\*]+?\b(\w+)\(", text, flags=re.M)))
 
 
 def test_header_declares_the_hot_path_calls():
@@ -31,7 +32,9 @@ def test_header_declares_the_hot_path_calls():
 
 
 def test_every_declared_symbol_is_exported(lib):
-    for name in declared_symbols():
+    names = declared_symbols() + declared_symbols(BLOCKS_HEADER, "PKV_BM_API")
+    assert "pkv_bm_allocate_slots" in names and "pkv_bm_cow" in names
+    for name in names:
         assert hasattr(lib, name), f"libpkv does not export {name}"
 
 

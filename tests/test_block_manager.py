@@ -1,0 +1,175 @@
+"""Host block manager (libpkv, include/pkv_blocks.h) against what the pages state.
+
+"vLLM's PagedAttention" teardown, section "PagedAttention: the KV cache is paged":
+  * allocate_slots takes ceil(new tokens / 16) blocks, or returns None when the pool
+    cannot cover them;
+  * full blocks are hashed by chaining the parent block's hash with the block's token
+    ids, so equal prefixes give equal hashes and a new request with the same prompt
+    prefix reuses the physical blocks (reference count + 1, no copy);
+  * a block returns to the free pool at reference count zero, and cached-but-free
+    blocks sit at the tail of the free queue so they are evicted last.
+Section "What happens when the blocks run out": freeing evicts a request's tail
+blocks first, so its prompt prefix tends to survive.
+"The 1960s Operating System Trick ..." page, Technical Details: samples share blocks
+until they diverge; copy-on-write duplicates only the block that changes.
+"""
+import numpy as np
+import pytest
+
+BLOCK = 16
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    from paged_kv_cache_248_gb300 import _build
+    _build.build()
+    import paged_kv_cache_248_gb300 as m
+    return m
+
+
+def toks(seed, n):
+    return np.random.default_rng(seed).integers(0, 50000, size=n).astype(np.int32)
+
+
+@pytest.mark.parametrize("n", [1, 15, 16, 17, 31, 32, 33, 2000])
+def test_allocate_takes_ceil_tokens_over_16(pkv, n):
+    bm = pkv.BlockManager(200)
+    assert bm.get_computed_blocks(1, toks(0, n)) == 0
+    assert bm.allocate_slots(1, n) == (n + BLOCK - 1) // BLOCK
+    assert len(bm.block_table(1)) == (n + BLOCK - 1) // BLOCK
+    assert bm.num_free == 200 - (n + BLOCK - 1) // BLOCK
+    # growing within the last block takes nothing; crossing a boundary takes one
+    last = (n + BLOCK - 1) // BLOCK * BLOCK
+    assert bm.allocate_slots(1, last) == 0
+    assert bm.allocate_slots(1, last + 1) == 1
+
+
+def test_allocate_returns_none_and_takes_nothing_when_short(pkv):
+    bm = pkv.BlockManager(5)
+    bm.get_computed_blocks(1, [])
+    assert bm.allocate_slots(1, 3 * BLOCK) == 3
+    bm.get_computed_blocks(2, [])
+    assert bm.allocate_slots(2, 3 * BLOCK) is None        # needs 3, only 2 free
+    assert bm.num_free == 2 and bm.block_table(2) == []
+    assert bm.allocate_slots(2, 2 * BLOCK) == 2
+    assert bm.num_free == 0
+
+
+def test_shared_prefix_reuses_physical_blocks(pkv):
+    bm = pkv.BlockManager(64)
+    system = toks(1, 3 * BLOCK)
+    a = np.concatenate([system, toks(2, 10)])
+    assert bm.get_computed_blocks(1, a) == 0
+    bm.allocate_slots(1, a.size)
+    assert bm.cache_full_blocks(1, a) == 3                 # three full blocks hashed
+    free_before = bm.num_free
+    b = np.concatenate([system, toks(3, 25)])
+    assert bm.get_computed_blocks(2, b) == 3               # the system prompt is a hit
+    assert bm.block_table(2) == bm.block_table(1)[:3]      # the same physical blocks
+    assert bm.num_free == free_before                       # no copy, nothing taken
+    bm.allocate_slots(2, b.size)
+    assert bm.block_table(2)[:3] == bm.block_table(1)[:3]
+    assert set(bm.block_table(2)[3:]).isdisjoint(bm.block_table(1))
+
+
+def test_hash_chains_the_whole_prefix(pkv):
+    bm = pkv.BlockManager(64)
+    x, y, z = toks(4, BLOCK), toks(5, BLOCK), toks(6, BLOCK)
+    h_x = bm.block_hash(0, x)
+    assert bm.block_hash(0, x) == h_x                       # deterministic
+    assert bm.block_hash(h_x, z) != bm.block_hash(bm.block_hash(0, y), z)  # same block, other parent
+    assert bm.block_hash(h_x, z, 1) != bm.block_hash(h_x, z, 0)            # extra key counts
+    # a request whose third block matches but whose first does not gets no hit
+    a = np.concatenate([x, y, z])
+    bm.get_computed_blocks(1, a)
+    bm.allocate_slots(1, a.size)
+    bm.cache_full_blocks(1, a)
+    b = np.concatenate([toks(7, BLOCK), y, z])
+    assert bm.get_computed_blocks(2, b) == 0
+    c = np.concatenate([x, y, toks(8, BLOCK)])
+    assert bm.get_computed_blocks(3, c) == 2
+
+
+def test_block_returns_to_pool_at_refcount_zero(pkv):
+    bm = pkv.BlockManager(32)
+    p = toks(9, 2 * BLOCK)
+    bm.get_computed_blocks(1, p)
+    bm.allocate_slots(1, p.size)
+    bm.cache_full_blocks(1, p)
+    bm.get_computed_blocks(2, p)                            # shares both blocks
+    assert bm.num_free == 30
+    bm.free(1)
+    assert bm.num_free == 30                                # still referenced by request 2
+    bm.free(2)
+    assert bm.num_free == 32
+
+
+def test_cached_free_blocks_revive_and_tail_evicted_first(pkv):
+    n = 8
+    bm = pkv.BlockManager(n)
+    p = toks(10, 4 * BLOCK)
+    bm.get_computed_blocks(1, p)
+    bm.allocate_slots(1, p.size)                            # blocks 0..3
+    table = bm.block_table(1)
+    bm.cache_full_blocks(1, p)
+    bm.free(1)                                              # cached-but-free, tail first into the queue
+    assert bm.num_free == n
+    # a new request with the same prompt revives them without any copy
+    assert bm.get_computed_blocks(2, p) == 4 and bm.block_table(2) == table
+    bm.free(2)
+    # never-used blocks are taken first; then the freed request's tail before its prefix
+    bm.get_computed_blocks(3, [])
+    bm.allocate_slots(3, (n - 4) * BLOCK)                   # the 4 never-used blocks
+    assert set(bm.block_table(3)).isdisjoint(table)
+    bm.allocate_slots(3, (n - 4 + 1) * BLOCK)               # evicts one cached block
+    assert bm.block_table(3)[-1] == table[-1]               # the request's last block went first
+    q = np.concatenate([p[:3 * BLOCK], toks(11, BLOCK)])
+    assert bm.get_computed_blocks(4, q) == 3                # the prefix survived
+
+
+def test_fork_and_copy_on_write(pkv):
+    bm = pkv.BlockManager(16)
+    p = toks(12, 40)                                        # 3 blocks, the last partial
+    bm.get_computed_blocks(1, p)
+    bm.allocate_slots(1, p.size)
+    parent = bm.block_table(1)
+    bm.fork(1, 2)                                           # a parallel sample: shares everything
+    assert bm.block_table(2) == parent and bm.num_free == 13
+    src_dst = bm.cow(2, 2)                                  # the sample writes into the shared last block
+    assert src_dst[0] == parent[2] and src_dst[1] not in parent
+    assert bm.block_table(2) == parent[:2] + [src_dst[1]]
+    assert bm.block_table(1) == parent                      # the parent keeps its block
+    assert bm.cow(2, 2) == ()                               # now private: no further copy
+    assert bm.cow(1, 2) == ()                               # and the parent's is private again
+    assert bm.cow(2, 0) != ()                               # the first block is still shared
+    full = pkv.BlockManager(3)
+    full.get_computed_blocks(1, [])
+    full.allocate_slots(1, 48)
+    full.fork(1, 2)
+    assert full.cow(2, 1) is None                           # no free block for the copy
+
+
+def test_waste_is_only_the_last_partial_block(pkv):
+    # paging wastes at most the tail of each request's last block (< 16 slots)
+    rng = np.random.default_rng(13)
+    bm = pkv.BlockManager(100000)
+    lens = rng.integers(1, 5000, size=200)
+    for i, L in enumerate(lens):
+        bm.get_computed_blocks(i, [])
+        bm.allocate_slots(i, int(L))
+    u = bm.usage()
+    assert u["tokens_held"] == lens.sum()
+    assert u["unused_slots"] == int(sum((-L) % BLOCK for L in lens))
+    assert u["unused_slots"] < BLOCK * len(lens)
+    assert u["blocks_in_use"] == sum((int(L) + BLOCK - 1) // BLOCK for L in lens)
+
+
+def test_errors(pkv):
+    bm = pkv.BlockManager(4)
+    with pytest.raises(ValueError):
+        bm.allocate_slots(7, 10)                            # unknown request
+    bm.get_computed_blocks(1, [])
+    with pytest.raises(ValueError):
+        bm.get_computed_blocks(1, [])                       # already exists
+    with pytest.raises(ValueError):
+        pkv.BlockManager(0)
