@@ -405,6 +405,24 @@ def main():
         "work": {"bytes": work_b, "flops": work_f},
     }
 
+    # the same step captured once into a CUDA graph and replayed (one launch per step)
+    try:
+        gs = torch.cuda.Stream()
+        gs.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(gs):
+            step.run()
+        gs.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=gs):
+            step.run()
+        ms_graph = timed(graph.replay, args.steps, args.warmup, barrier)
+        if pkv.pkv_get_last_error() != 0:
+            raise RuntimeError("device error during graph replay")
+        res["graph_replay"] = {"ms_per_step": ms_graph, "value": tokens / (ms_graph / 1e3), "unit": "tokens/s"}
+        del graph
+    except RuntimeError as e:  # capture not possible here: report why, keep the eager numbers
+        res["graph_replay"] = {"error": str(e)[:200]}
+
     if not args.no_e2e:
         e2e = E2EStep(step)
         ms_e2e = timed(e2e.run, max(3, args.steps // 2), 3, barrier)
