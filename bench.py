@@ -45,9 +45,9 @@ METRIC = "decode KV-read GB/s (% of HBM peak); mixed-step tokens/sec at 1 GB300"
 # It scales to other workloads by the bytes processed, and it is reported only while
 # the profiled sources are unchanged.
 NCU_TRAFFIC = {
-    "decode": {"ratio": 510.50 / 503.62,
+    "decode": {"ratio": 510.65 / 503.62,
                "sources": ("k_decode.cu", "ptx.cuh", "pkv_internal.cuh"),
-               "sha256": "59edfe19fc3bb1292c7558d47427b60f6cf693d0f3623158fdf56f7882102d40"},
+               "sha256": "c574056f5615eed041ee45edf5b04def0a387bc45f0b77b50be6896217fc5efb"},
 }
 
 
@@ -171,7 +171,7 @@ class ClockSampler:
 class Step:
     """Device-resident inputs of one workload and the three C-ABI calls of a step."""
 
-    def __init__(self, pkv, w, device):
+    def __init__(self, pkv, w, device, cascade: bool = True):
         self.pkv, self.w = pkv, w
         t = w.make_tensors(device)
         self.t = t
@@ -180,6 +180,21 @@ class Step:
         self.slots = torch.empty(w.num_tokens, dtype=torch.int64, device=device)
         self.out = torch.empty_like(t["q"])
         self.cow = (dev(w.cow_src), dev(w.cow_dst)) if w.cow_src is not None else None
+        # the shared prefix, when the workload has one, is handed over as a group hint
+        self.groups = None
+        if cascade and "shared_prefix_ids" in w.notes:
+            pid = np.asarray(w.notes["shared_prefix_ids"], np.int32)
+            self.groups = (dev(pid[None, :]), dev(np.array([pid.size], np.int32)),
+                           dev(np.array([0, w.num_seqs], np.int32)), dev(np.arange(w.num_seqs, dtype=np.int32)))
+
+    def attend(self, q, out):
+        p, w, t = self.pkv, self.w, self.t
+        if self.groups is not None:
+            p.paged_attention_cascade(q, t["k_cache"], t["v_cache"], self.bt, self.sl, self.qsl, w.scale,
+                                      w.max_query_len, w.max_seq_len, *self.groups, out=out)
+        else:
+            p.paged_attention(q, t["k_cache"], t["v_cache"], self.bt, self.sl, self.qsl, w.scale,
+                              w.max_query_len, w.max_seq_len, out=out)
 
     def run(self):
         p, w, t = self.pkv, self.w, self.t
@@ -187,13 +202,10 @@ class Step:
             p.pkv_copy_blocks(self.cow[0], self.cow[1], t["k_cache"], t["v_cache"])
         p.pkv_slot_mapping(self.bt, self.sl, self.qsl, w.num_tokens, out=self.slots)
         p.pkv_write(t["k_new"], t["v_new"], self.slots, t["k_cache"], t["v_cache"])
-        p.paged_attention(t["q"], t["k_cache"], t["v_cache"], self.bt, self.sl, self.qsl, w.scale,
-                          w.max_query_len, w.max_seq_len, out=self.out)
+        self.attend(t["q"], self.out)
 
     def attention_only(self):
-        p, w, t = self.pkv, self.w, self.t
-        p.paged_attention(t["q"], t["k_cache"], t["v_cache"], self.bt, self.sl, self.qsl, w.scale,
-                          w.max_query_len, w.max_seq_len, out=self.out)
+        self.attend(self.t["q"], self.out)
 
 
 class E2EStep:
@@ -221,8 +233,7 @@ class E2EStep:
         s.qsl.copy_(self.h_qsl, non_blocking=True)
         p.pkv_slot_mapping(s.bt, s.sl, s.qsl, w.num_tokens, out=s.slots)
         p.pkv_write(self.d["k_new"], self.d["v_new"], s.slots, t["k_cache"], t["v_cache"])
-        p.paged_attention(self.d["q"], t["k_cache"], t["v_cache"], s.bt, s.sl, s.qsl, w.scale, w.max_query_len,
-                          w.max_seq_len, out=s.out)
+        s.attend(self.d["q"], s.out)
         self.h_out.copy_(s.out, non_blocking=True)
 
 
@@ -322,6 +333,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-decode-line", action="store_true")
+    ap.add_argument("--no-cascade", action="store_true",
+                    help="attend a shared prefix per request instead of once per group")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -343,7 +356,7 @@ def main():
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     pk = peaks()
-    step = Step(pkv, w, device)
+    step = Step(pkv, w, device, cascade=not args.no_cascade)
     work_b = algorithmic_bytes(w)
     work_f = algorithmic_flops(w)
 
@@ -377,6 +390,12 @@ def main():
     # dominant kernel of the step and its roofline
     dom = max(kernel_ms, key=lambda k: kernel_ms[k][1])
     n_dom, t_dom = kernel_ms[dom]
+    if "cascade" in kernel_ms:
+        # shared-prefix groups: the cascade kernel reads the prefix, the decode kernel each
+        # member's own keys, the merge joins them; the roofline covers that whole pass
+        parts = [k for k in ("cascade", "decode", "merge") if k in kernel_ms]
+        dom = "+".join(parts)
+        n_dom, t_dom = kernel_ms["decode"][0], sum(kernel_ms[k][1] for k in parts)
     per_launch_ms = t_dom / n_dom
     if dom == "prefill":
         flops = work_f["prefill"]
@@ -384,7 +403,7 @@ def main():
         roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops_sustained"],
                 "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops_sustained"], "traffic": None}
     else:
-        b = work_b["decode"] if dom == "decode" else work_b["total"]
+        b = work_b["decode"] if dom.startswith(("decode", "cascade")) else work_b["total"]
         ach = b / (per_launch_ms / 1e3) / 1e9
         ratio = traffic_ratio(dom)
         roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",

@@ -148,6 +148,54 @@ PKV_API int paged_attention(const void* q, const void* k_cache, const void* v_ca
                     int32_t max_query_len, int32_t max_seq_len, float scale, void* out, void* stream);
 
 /*
+ * Shared-prefix groups for paged_attention_cascade (host struct of device arrays).
+ * Requests that share a prompt prefix point at the same physical blocks ("vLLM's
+ * PagedAttention" teardown, section "PagedAttention": a new request whose prefix
+ * hashes match reuses the cached blocks), so those blocks need to be read only once
+ * per step for all of them.  Group g is a prefix of prefix_num_blocks[g] full blocks
+ * (P_g = 16 x that many tokens) whose physical ids are row g of prefix_block_tables;
+ * its members are the request indices member_seqs[member_start[g] ..
+ * member_start[g + 1]).
+ *   prefix_block_tables  device int32 [num_groups][max_prefix_blocks]
+ *   prefix_num_blocks    device int32 [num_groups], each in [1, max_prefix_blocks]
+ *   member_start         device int32 [num_groups + 1], 0 = first <= ... <= last = num_members
+ *   member_seqs          device int32 [num_members]
+ */
+typedef struct {
+  const int32_t* prefix_block_tables;
+  int32_t max_prefix_blocks;
+  const int32_t* prefix_num_blocks;
+  const int32_t* member_start;
+  const int32_t* member_seqs;
+  int32_t num_groups;
+  int32_t num_members;
+} pkv_prefix_groups;
+
+/*
+ * paged_attention_cascade -- paged_attention() with shared-prefix groups as a hint.
+ * The output is paged_attention()'s (up to fp32 rounding order): the groups only
+ * change how the work is done.  A member whose request is a decode (one query
+ * token), whose context goes past the prefix (seq_len > P_g), which is listed once
+ * in all groups, and whose block table starts with the group's prefix blocks has
+ * its first P_g keys attended together with the other members of its group: one
+ * tensor-core pass per (group, kv head) reads the prefix once and leaves a partial
+ * softmax state per member, which the split merge folds with the member's own keys
+ * (log-sum-exp merge, prefix first).  Any other listed request -- a prefill chunk,
+ * a shorter context, a duplicate, a table that does not match, a malformed group --
+ * is attended the ordinary way.  No counterpart on the pages beyond the sharing
+ * itself; this is the cascade reading of it.
+ * groups: NULL or num_groups == 0 or num_members == 0 = paged_attention().  The fp32
+ * path ignores the groups.  Host errors as paged_attention(), plus PKV_ERR_INVALID_ARG
+ * for negative counts, null group arrays or max_prefix_blocks < 1.
+ */
+PKV_API int paged_attention_cascade(const void* q, const void* k_cache, const void* v_cache,
+                                    const pkv_cache_desc* cache, const int32_t* block_tables,
+                                    int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                    const int32_t* query_start_loc, int32_t num_seqs, int32_t num_q_heads,
+                                    int64_t num_tokens, int32_t max_query_len, int32_t max_seq_len, float scale,
+                                    const pkv_prefix_groups* groups, void* out, void* stream);
+
+/*
  * paged_attention_noalloc -- paged_attention() for callers that cannot let a library
  * allocate device memory.  The pages have no counterpart for this call; it exists
  * for deployment.  paged_attention() grows a workspace with cudaMalloc when a batch
@@ -200,9 +248,10 @@ PKV_API void pkv_shutdown(void);
  * by CUDA events on its stream.  pkv_trace_read() synchronises the device and
  * returns, per kernel kind, the launch count and the summed device time in ms,
  * then resets the counters.  Kinds: 0 slot mapping, 1 write, 2 copy, 3 plan,
- * 4 decode, 5 prefill, 6 generic attention, 7 split merge.  Arrays hold PKV_TRACE_KINDS entries.
+ * 4 decode, 5 prefill, 6 generic attention, 7 split merge, 8 shared-prefix (cascade)
+ * pass.  Arrays hold PKV_TRACE_KINDS entries.
  */
-#define PKV_TRACE_KINDS 8
+#define PKV_TRACE_KINDS 9
 PKV_API int pkv_trace_enable(int on);
 PKV_API int pkv_trace_read(int64_t* launches, double* total_ms);
 PKV_API const char* pkv_trace_kind_name(int kind);

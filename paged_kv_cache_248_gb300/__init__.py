@@ -8,7 +8,7 @@ Every computation runs in the library's CUDA kernels; there is no CPU path.
 If the library has not been built, importing a function raises immediately.
 
 Functions carry the C names:
-  pkv_slot_mapping, pkv_write, pkv_copy_blocks, paged_attention,
+  pkv_slot_mapping, pkv_write, pkv_copy_blocks, paged_attention, paged_attention_cascade,
   pkv_get_last_error, pkv_peek_error_bits, pkv_trace_enable, pkv_trace_read,
   pkv_num_workers, pkv_shutdown, pkv_umma_selftest, pkv_tma_selftest.
 """
@@ -27,7 +27,7 @@ PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_INDEX = 0, 1, 2, 3
 PKV_ERR_CUDA, PKV_ERR_NO_MEMORY, PKV_ERR_TIMEOUT = 4, 5, 6
 PKV_F32, PKV_BF16 = 0, 1
 BLOCK_SIZE = 16
-TRACE_KINDS = 8
+TRACE_KINDS = 9
 
 _lib = None
 _lock = threading.Lock()
@@ -42,6 +42,12 @@ class PkvError(RuntimeError):
 class _CacheDesc(ctypes.Structure):
     _fields_ = [("num_blocks", ctypes.c_int64), ("block_size", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+class _PrefixGroups(ctypes.Structure):
+    _fields_ = [("prefix_block_tables", ctypes.c_void_p), ("max_prefix_blocks", ctypes.c_int32),
+                ("prefix_num_blocks", ctypes.c_void_p), ("member_start", ctypes.c_void_p),
+                ("member_seqs", ctypes.c_void_p), ("num_groups", ctypes.c_int32), ("num_members", ctypes.c_int32)]
 
 
 def lib():
@@ -60,6 +66,8 @@ def lib():
                 "pkv_write": [P, P, P, i64, P, P, D, P],
                 "pkv_copy_blocks": [P, P, i64, P, P, D, P],
                 "paged_attention": [P, P, P, D, P, i32, P, P, i32, i32, i64, i32, i32, f32, P, P],
+                "paged_attention_cascade": [P, P, P, D, P, i32, P, P, i32, i32, i64, i32, i32, f32,
+                                            ctypes.POINTER(_PrefixGroups), P, P],
                 "pkv_get_last_error": [P],
                 "pkv_peek_error_bits": [P, ctypes.POINTER(ctypes.c_uint32)],
                 "pkv_num_workers": [ctypes.POINTER(ctypes.c_int32)],
@@ -168,6 +176,39 @@ def paged_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tenso
                                  _dev(query_start_loc, "query_start_loc", torch.int32), seq_lens.shape[0], hq, T,
                                  int(max_query_len), int(max_seq_len), float(scale),
                                  _dev(out, "out", k_cache.dtype), _stream(stream)), "paged_attention")
+    return out
+
+
+def paged_attention_cascade(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                            block_tables: torch.Tensor, seq_lens: torch.Tensor, query_start_loc: torch.Tensor,
+                            scale: float, max_query_len: int, max_seq_len: int, prefix_block_tables: torch.Tensor,
+                            prefix_num_blocks: torch.Tensor, member_start: torch.Tensor, member_seqs: torch.Tensor,
+                            out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """paged_attention with shared-prefix groups as a hint: group g's prefix is the
+    first prefix_num_blocks[g] blocks of row g of prefix_block_tables, shared by the
+    requests member_seqs[member_start[g]:member_start[g + 1]].  Same result."""
+    desc = _cache_desc(k_cache, v_cache)
+    if out is None:
+        out = torch.empty_like(q)
+    T, hq, d = q.shape
+    if prefix_block_tables.dim() != 2:
+        raise ValueError("prefix_block_tables must be [num_groups, max_prefix_blocks]")
+    G, M = prefix_num_blocks.shape[0], member_seqs.shape[0]
+    if prefix_block_tables.shape[0] != G or member_start.shape[0] != G + 1:
+        raise ValueError("prefix group arrays disagree on the number of groups")
+    groups = _PrefixGroups(_dev(prefix_block_tables, "prefix_block_tables", torch.int32),
+                           prefix_block_tables.shape[1],
+                           _dev(prefix_num_blocks, "prefix_num_blocks", torch.int32),
+                           _dev(member_start, "member_start", torch.int32),
+                           _dev(member_seqs, "member_seqs", torch.int32) if M else None, G, M)
+    _check(lib().paged_attention_cascade(_dev(q, "q", k_cache.dtype), _dev(k_cache, "k_cache"),
+                                         _dev(v_cache, "v_cache"), ctypes.byref(desc),
+                                         _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+                                         _dev(seq_lens, "seq_lens", torch.int32),
+                                         _dev(query_start_loc, "query_start_loc", torch.int32), seq_lens.shape[0],
+                                         hq, T, int(max_query_len), int(max_seq_len), float(scale),
+                                         ctypes.byref(groups), _dev(out, "out", k_cache.dtype), _stream(stream)),
+           "paged_attention_cascade")
     return out
 
 

@@ -73,7 +73,7 @@ int ensure_workspace(DeviceCtx* ctx, size_t bytes, cudaStream_t stream) {
 }
 
 size_t layout_workspace(void* base, int32_t num_seqs, int32_t hkv, int32_t group, int32_t head_dim,
-                        int64_t max_dec_items, Workspace* ws) {
+                        int64_t max_dec_items, Workspace* ws, const CascadeArgs* cas) {
   size_t off = 0;
   auto take = [&](size_t bytes) -> void* {
     void* p = base ? static_cast<char*>(base) + off : nullptr;
@@ -88,6 +88,17 @@ size_t layout_workspace(void* base, int32_t num_seqs, int32_t hkv, int32_t group
   w.merge_list = static_cast<int32_t*>(take(static_cast<size_t>(num_seqs) * sizeof(int32_t)));
   w.part_ml = static_cast<float*>(take(static_cast<size_t>(max_dec_items) * group * 2 * sizeof(float)));
   w.part_o = static_cast<float*>(take(static_cast<size_t>(max_dec_items) * group * head_dim * sizeof(float)));
+  if (cas && cas->num_groups > 0 && cas->num_members > 0) {
+    const size_t nm = static_cast<size_t>(cas->num_members);
+    w.cas_np_max = static_cast<int32_t>(cascade_splits(static_cast<int64_t>(cas->max_blocks) * kBlock));
+    const size_t slots = nm * hkv * w.cas_np_max;
+    w.seq_prefix = static_cast<int32_t*>(take(static_cast<size_t>(num_seqs) * sizeof(int32_t)));
+    w.seq_entry = static_cast<int32_t*>(take(static_cast<size_t>(num_seqs) * sizeof(int32_t)));
+    w.member_ok = static_cast<int32_t*>(take(nm * sizeof(int32_t)));
+    w.cas_prefix = static_cast<int32_t*>(take((static_cast<size_t>(cas->num_groups) + 1) * sizeof(int32_t)));
+    w.cas_ml = static_cast<float*>(take(slots * group * 2 * sizeof(float)));
+    w.cas_o = static_cast<float*>(take(slots * group * head_dim * sizeof(float)));
+  }
   if (ws) *ws = w;
   return off;
 }
@@ -150,7 +161,8 @@ std::vector<int> g_pending_kind;  // kind per used slot
 int64_t g_launches[PKV_TRACE_KINDS] = {};
 double g_ms[PKV_TRACE_KINDS] = {};
 const char* kTraceNames[PKV_TRACE_KINDS] = {"slot_mapping", "write", "copy_blocks", "plan",
-                                            "decode", "prefill", "generic_attention", "merge"};
+                                            "decode", "prefill", "generic_attention", "merge",
+                                            "cascade"};
 }  // namespace
 
 TraceScope::TraceScope(int k, cudaStream_t s) : kind(k), stream(s), slot(-1) {
@@ -233,15 +245,33 @@ int pkv_copy_blocks(const int32_t* src, const int32_t* dst, int64_t n, void* k_c
   return launch_copy_blocks(src, dst, n, k_cache, v_cache, *cache, ctx->err, as_stream(stream));
 }
 
-int paged_attention(const void* q, const void* k_cache, const void* v_cache, const pkv_cache_desc* cache,
-                    const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
-                    const int32_t* query_start_loc, int32_t num_seqs, int32_t num_q_heads, int64_t num_tokens,
-                    int32_t max_query_len, int32_t max_seq_len, float scale, void* out, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// paged_attention and paged_attention_cascade: `groups` null = no shared prefixes.
+int attention_impl(const void* q, const void* k_cache, const void* v_cache, const pkv_cache_desc* cache,
+                   const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                   const int32_t* query_start_loc, int32_t num_seqs, int32_t num_q_heads, int64_t num_tokens,
+                   int32_t max_query_len, int32_t max_seq_len, float scale, const pkv_prefix_groups* groups,
+                   void* out, void* stream) {
   int st = check_cache(cache);
   if (st) return st;
   if (num_tokens < 0 || num_seqs < 0 || num_q_heads <= 0 || num_q_heads % cache->num_kv_heads != 0)
     return PKV_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
+  CascadeArgs cas{};
+  if (groups) {
+    if (groups->num_groups < 0 || groups->num_members < 0) return PKV_ERR_INVALID_ARG;
+    if (groups->num_groups > 0 && groups->num_members > 0) {
+      if (!groups->prefix_block_tables || !groups->prefix_num_blocks || !groups->member_start ||
+          !groups->member_seqs || groups->max_prefix_blocks < 1)
+        return PKV_ERR_INVALID_ARG;
+      cas = CascadeArgs{groups->prefix_block_tables, groups->max_prefix_blocks, groups->prefix_num_blocks,
+                        groups->member_start,        groups->member_seqs,       groups->num_groups,
+                        groups->num_members};
+    }
+  }
   if (num_tokens == 0) return PKV_OK;
   if (num_seqs == 0 || max_blocks_per_seq <= 0 || max_query_len <= 0 || max_seq_len <= 0) return PKV_ERR_INVALID_ARG;
   if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !query_start_loc || !out)
@@ -252,7 +282,7 @@ int paged_attention(const void* q, const void* k_cache, const void* v_cache, con
   AttnArgs a{q,        k_cache,    v_cache,       *cache,      block_tables, max_blocks_per_seq, seq_lens,
              query_start_loc, num_seqs, num_q_heads, num_tokens, max_query_len, max_seq_len, scale, out};
   cudaStream_t s = as_stream(stream);
-  if (cache->dtype == PKV_F32) return launch_generic_attention(a, ctx->err, s);
+  if (cache->dtype == PKV_F32) return launch_generic_attention(a, ctx->err, s);  // groups do not change results
   // bf16, head_dim 128: tensor-core path
   const int32_t hkv = cache->num_kv_heads;
   const int32_t group = num_q_heads / hkv;
@@ -261,20 +291,60 @@ int paged_attention(const void* q, const void* k_cache, const void* v_cache, con
   const int64_t max_splits = (static_cast<int64_t>(max_seq_len) + kSplitKeys - 1) / kSplitKeys;
   const int64_t max_dec_items = static_cast<int64_t>(num_seqs) * hkv * max_splits;
   if (max_dec_items >= (int64_t(1) << 31)) return PKV_ERR_UNSUPPORTED;
-  const size_t need = layout_workspace(nullptr, num_seqs, hkv, gp, cache->head_dim, max_dec_items, nullptr);
+  if (cas.num_groups > 0) {
+    const int64_t slots = static_cast<int64_t>(cas.num_members) * hkv *
+                          cascade_splits(static_cast<int64_t>(cas.max_blocks) * kBlock);
+    if (slots * gp >= (int64_t(1) << 31)) return PKV_ERR_UNSUPPORTED;
+  }
+  const CascadeArgs* casp = cas.num_groups > 0 ? &cas : nullptr;
+  const size_t need = layout_workspace(nullptr, num_seqs, hkv, gp, cache->head_dim, max_dec_items, nullptr, casp);
   st = ensure_workspace(ctx, need, s);
   if (st) return st;
   Workspace ws;
-  layout_workspace(ctx->ws, num_seqs, hkv, gp, cache->head_dim, max_dec_items, &ws);
+  layout_workspace(ctx->ws, num_seqs, hkv, gp, cache->head_dim, max_dec_items, &ws, casp);
   PlanArgs plan{seq_lens, query_start_loc, num_seqs, num_tokens, hkv, max_blocks_per_seq, max_seq_len,
                 kSplitKeys, kTileKeys / gp, ws.counters, ws.dec_prefix, ws.pre_prefix, ws.unit_bad,
                 ws.merge_list, ctx->err};
+  if (casp) {
+    plan.bt = block_tables;
+    plan.cas = cas;
+    plan.cas_rows = kTileKeys / gp;
+    plan.seq_prefix = ws.seq_prefix;
+    plan.seq_entry = ws.seq_entry;
+    plan.member_ok = ws.member_ok;
+    plan.cas_prefix = ws.cas_prefix;
+  }
   st = launch_plan(plan, s);
   if (st) return st;
+  if (casp) {
+    st = launch_cascade_tc(a, cas, ws, ctx->num_sms, ctx->err, s);
+    if (st) return st;
+  }
   st = launch_decode_tc(a, ws, ctx->num_sms, ctx->err, s);
   if (st) return st;
   if (max_query_len > 1) st = launch_prefill_tc(a, ws, ctx->num_sms, ctx->err, s);
   return st;
+}
+
+}  // namespace
+
+extern "C" {
+
+int paged_attention(const void* q, const void* k_cache, const void* v_cache, const pkv_cache_desc* cache,
+                    const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                    const int32_t* query_start_loc, int32_t num_seqs, int32_t num_q_heads, int64_t num_tokens,
+                    int32_t max_query_len, int32_t max_seq_len, float scale, void* out, void* stream) {
+  return attention_impl(q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq, seq_lens, query_start_loc,
+                        num_seqs, num_q_heads, num_tokens, max_query_len, max_seq_len, scale, nullptr, out, stream);
+}
+
+int paged_attention_cascade(const void* q, const void* k_cache, const void* v_cache, const pkv_cache_desc* cache,
+                            const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                            const int32_t* query_start_loc, int32_t num_seqs, int32_t num_q_heads,
+                            int64_t num_tokens, int32_t max_query_len, int32_t max_seq_len, float scale,
+                            const pkv_prefix_groups* groups, void* out, void* stream) {
+  return attention_impl(q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq, seq_lens, query_start_loc,
+                        num_seqs, num_q_heads, num_tokens, max_query_len, max_seq_len, scale, groups, out, stream);
 }
 
 int pkv_peek_error_bits(void* stream, uint32_t* bits) {

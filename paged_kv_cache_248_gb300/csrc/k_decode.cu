@@ -56,7 +56,8 @@ struct alignas(16) ItemInfo {
   int32_t idx;  // decode item index; -1 = queue exhausted
   int32_t seq, head, split;
   int32_t nsplit, key_start, key_end, valid;
-  int32_t trow, row_ok, pad0, pad1;  // the request's query row, and whether it is addressable
+  int32_t trow, row_ok, member, pad1;  // the request's query row, whether it is addressable, and
+                                       // whether a shared prefix was attended by the cascade kernel
 };
 
 struct Ctl {
@@ -87,6 +88,7 @@ struct DecodeParams {
   int32_t* unit_bad;
   float* part_o;   // [items][128][GP]
   float* part_ml;  // [items][GP][2]
+  const int32_t* seq_prefix;  // [num_seqs] keys before this many are the cascade kernel's; null: none
   uint32_t* err;
   int64_t num_blocks;
   int64_t num_tokens;
@@ -191,6 +193,7 @@ __device__ void scheduler_warp(const DecodeParams& P, Ctl& c) {
     const int64_t L = __ldg(P.seq_lens + i);
     const int64_t t = __ldg(P.qsl + i), t1 = __ldg(P.qsl + i + 1);
     const int nsplit = cnt / P.hkv;
+    const int64_t pre = P.seq_prefix ? __ldg(P.seq_prefix + i) : 0;  // shared-prefix keys, done elsewhere
     r.idx = idx;
     r.seq = i;
     r.row_ok = (t >= 0 && t < P.num_tokens && t1 == t + 1) ? 1 : 0;
@@ -201,15 +204,16 @@ __device__ void scheduler_warp(const DecodeParams& P, Ctl& c) {
       r.head = local / nsplit;
       r.split = local % nsplit;
       r.nsplit = nsplit;
-      const bool ok = r.row_ok && L >= 1 && (L + kBlock - 1) / kBlock <= P.max_blocks &&
-                      static_cast<int64_t>(nsplit) == decode_splits(L);
+      const bool ok = r.row_ok && L >= 1 && (L + kBlock - 1) / kBlock <= P.max_blocks && pre >= 0 && pre < L &&
+                      static_cast<int64_t>(nsplit) == decode_splits(L - pre);
       if (ok) {
         r.valid = 1;
+        r.member = pre > 0 ? 1 : 0;
         if (nsplit == 1) {
-          r.key_start = 0;
+          r.key_start = static_cast<int32_t>(pre);
           r.key_end = static_cast<int32_t>(L);
         } else {
-          r.key_start = r.split * P.split_keys;
+          r.key_start = static_cast<int32_t>(pre) + r.split * P.split_keys;
           const int64_t split_end = static_cast<int64_t>(r.key_start) + P.split_keys;
           r.key_end = static_cast<int32_t>(L < split_end ? L : split_end);
         }
@@ -583,7 +587,7 @@ __device__ void softmax_warps(const DecodeParams& P, Ctl& c, uint8_t* stages, ui
     const int64_t trow = info.trow;
     const int64_t unit = static_cast<int64_t>(info.seq) * P.hkv + info.head;
     __nv_bfloat16* orow = P.out + (trow * P.hq + static_cast<int64_t>(info.head) * G) * 128 + r;
-    if (info.nsplit == 1) {
+    if (info.nsplit == 1 && !info.member) {
 #pragma unroll
       for (int g = 0; g < GP; ++g)
         if (g < G) orow[g * 128] = __float2bfloat16_rn(bad ? 0.f : acc[g] / lt[g]);
@@ -679,6 +683,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
 // splits -- the planner lists those requests -- by a log-sum-exp merge in split
 // order, one CTA per unit (thread d = head element), one pass with a running
 // maximum and float4 loads.  Requests of one split were written by the decode kernel.
+// A shared-prefix member's prefix partials (the cascade kernel's, stored [GP][128]
+// per split) come first, then its own key splits.
 struct MergeParams {
   __nv_bfloat16* out;
   const int32_t* counters;
@@ -688,8 +694,28 @@ struct MergeParams {
   const int32_t* unit_bad;
   const float* part_o;
   const float* part_ml;
+  const int32_t* seq_prefix;  // null: no shared-prefix groups
+  const int32_t* seq_entry;
+  const float* cas_o;
+  const float* cas_ml;
+  int32_t cas_np_max;
   int32_t num_seqs, hkv, group, hq;
 };
+
+// Folds one partial (running max m, sum l, accumulator o, per head) into the merge.
+template <int GP>
+__device__ __forceinline__ void merge_fold(float (&M)[GP], float (&num)[GP], float (&den)[GP], const float (&ml)[2 * GP],
+                                           const float (&ov)[GP]) {
+#pragma unroll
+  for (int g = 0; g < GP; ++g) {
+    const float m_new = fmaxf(M[g], ml[2 * g]);
+    const float a = exp2f(M[g] - m_new);
+    const float b = exp2f(ml[2 * g] - m_new);
+    den[g] = fmaf(den[g], a, ml[2 * g + 1] * b);
+    num[g] = fmaf(num[g], a, ov[g] * b);
+    M[g] = m_new;
+  }
+}
 
 template <int GP>
 __global__ void __launch_bounds__(128) merge_kernel(const MergeParams P) {
@@ -700,7 +726,8 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeParams P) {
     const int64_t u = static_cast<int64_t>(i) * P.hkv + h;
     const int base_i = __ldg(P.dec_prefix + i);
     const int ns = (__ldg(P.dec_prefix + i + 1) - base_i) / P.hkv;
-    if (ns <= 1) continue;
+    const int pre = P.seq_prefix ? __ldg(P.seq_prefix + i) : 0;
+    if (ns <= 1 && pre == 0) continue;
     const int64_t base = base_i + static_cast<int64_t>(h) * ns;
     float M[GP], num[GP], den[GP];
 #pragma unroll
@@ -708,6 +735,20 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeParams P) {
       M[g] = -INFINITY;
       num[g] = 0.f;
       den[g] = 0.f;
+    }
+    if (pre > 0) {
+      const int npre = static_cast<int>(cascade_splits(pre));
+      const int64_t cbase = (static_cast<int64_t>(__ldg(P.seq_entry + i)) * P.hkv + h) * P.cas_np_max;
+      for (int s = 0; s < npre; ++s) {
+        const float* ml_p = P.cas_ml + (cbase + s) * GP * 2;
+        const float* o_p = P.cas_o + (cbase + s) * GP * 128 + d;
+        float ml[2 * GP], ov[GP];
+#pragma unroll
+        for (int k = 0; k < 2 * GP; ++k) ml[k] = __ldg(ml_p + k);
+#pragma unroll
+        for (int g = 0; g < GP; ++g) ov[g] = __ldg(o_p + g * 128);
+        merge_fold<GP>(M, num, den, ml, ov);
+      }
     }
 #pragma unroll 4
     for (int s = 0; s < ns; ++s) {
@@ -730,15 +771,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeParams P) {
         ov[4 * k + 2] = t.z;
         ov[4 * k + 3] = t.w;
       }
-#pragma unroll
-      for (int g = 0; g < GP; ++g) {
-        const float m_new = fmaxf(M[g], ml[2 * g]);
-        const float a = exp2f(M[g] - m_new);
-        const float b = exp2f(ml[2 * g] - m_new);
-        den[g] = fmaf(den[g], a, ml[2 * g + 1] * b);
-        num[g] = fmaf(num[g], a, ov[g] * b);
-        M[g] = m_new;
-      }
+      merge_fold<GP>(M, num, den, ml, ov);
     }
     const bool bad = __ldg(P.unit_bad + u) != 0;
     const int64_t trow = __ldg(P.qsl + i);
@@ -751,7 +784,9 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeParams P) {
 
 template <int GP>
 int launch_gp(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& vm, const DecodeParams& p, int grid,
-              const int32_t* counters, const int32_t* merge_list, cudaStream_t s) {
+              const Workspace& ws, cudaStream_t s) {
+  const int32_t* counters = ws.counters;
+  const int32_t* merge_list = ws.merge_list;
   cudaError_t e = cudaFuncSetAttribute(decode_kernel<GP>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return cuda_status(e);
   {
@@ -760,8 +795,9 @@ int launch_gp(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& v
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_status(e);
   }
-  MergeParams m{p.out,       counters,  merge_list, p.dec_prefix, p.qsl,    p.unit_bad,
-                p.part_o,    p.part_ml, p.num_seqs, p.hkv,        p.group,  p.hq};
+  MergeParams m{p.out,          counters,  merge_list, p.dec_prefix,  p.qsl,     p.unit_bad,    p.part_o,
+                p.part_ml,      p.seq_prefix, ws.seq_entry, ws.cas_o, ws.cas_ml, ws.cas_np_max, p.num_seqs,
+                p.hkv,          p.group,   p.hq};
   // the list length is only known on the device: enough CTAs for every unit of a
   // full list, each exiting at once when the list is shorter
   const int64_t n_units = static_cast<int64_t>(p.num_seqs) * p.hkv;
@@ -803,6 +839,7 @@ int launch_decode_tc(const AttnArgs& a, const Workspace& ws, int num_sms, uint32
   p.unit_bad = ws.unit_bad;
   p.part_o = ws.part_o;
   p.part_ml = ws.part_ml;
+  p.seq_prefix = ws.seq_prefix;
   p.err = err;
   p.num_blocks = a.cache.num_blocks;
   p.num_tokens = a.num_tokens;
@@ -814,9 +851,9 @@ int launch_decode_tc(const AttnArgs& a, const Workspace& ws, int num_sms, uint32
   p.hq = a.num_q_heads;
   p.split_keys = kSplitKeys;
   p.scale_log2 = a.scale * 1.4426950408889634f;
-  if (gp == 4) return launch_gp<4>(qm, km, vm, p, num_sms, ws.counters, ws.merge_list, s);
-  if (gp == 8) return launch_gp<8>(qm, km, vm, p, num_sms, ws.counters, ws.merge_list, s);
-  return launch_gp<16>(qm, km, vm, p, num_sms, ws.counters, ws.merge_list, s);
+  if (gp == 4) return launch_gp<4>(qm, km, vm, p, num_sms, ws, s);
+  if (gp == 8) return launch_gp<8>(qm, km, vm, p, num_sms, ws, s);
+  return launch_gp<16>(qm, km, vm, p, num_sms, ws, s);
 }
 
 }  // namespace pkv

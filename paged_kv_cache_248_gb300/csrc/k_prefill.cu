@@ -26,6 +26,16 @@
 //              waits must not skip a phase) before handing over the next P.  P is written as bf16 into
 //              a swizzled K-major operand.  The final O / l is stored per row.
 // All waits are bounded (see ptx.cuh); a timeout raises the CTA abort flag.
+//
+// Shared-prefix (cascade) mode, kCas = true.  The same pipeline attends the member
+// decodes of a prefix group to the group's shared prefix: an item is (group, tile of
+// R member requests, kv head, key split of kCascadeSplitKeys prefix keys), its 128
+// rows are (member, head) pairs whose query rows the softmax warps gather with plain
+// loads into the swizzled Q tile (members are scattered over the batch), every key of
+// the split is visible to every row (all members sit past the prefix), and each row
+// leaves its unnormalised accumulator, reference maximum and sum as a partial for the
+// split merge instead of a final output.  The prefix's K/V are read once per
+// (group, kv head, split) for all its members.
 #include "ptx.cuh"
 #include "pkv_internal.cuh"
 
@@ -45,9 +55,10 @@ constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale O when a row 
 
 struct alignas(16) PItem {
   int32_t idx;  // -1: queue exhausted
-  int32_t seq, head, qt;
-  int32_t q_len, ctx, j0, nq;
-  int32_t nt, valid, t0, kend;
+  int32_t seq, head, qt;  // seq: the request (cascade: the prefix group)
+  int32_t q_len, ctx, j0, nq;  // j0: first query of the tile (cascade: first member entry)
+  int32_t nt, valid, t0, kend;  // keys [ks, kend) in nt tiles
+  int32_t ks, split, pad0, pad1;
 };
 
 struct Ctl {
@@ -79,6 +90,18 @@ struct PrefillParams {
   int64_t num_tokens;
   int32_t num_seqs, max_blocks, hkv, group, gp, rows_q, hq;
   float scale_log2;
+  // shared-prefix mode
+  const __nv_bfloat16* q;
+  const int32_t* cas_tables;
+  const int32_t* cas_blocks;
+  const int32_t* cas_start;
+  const int32_t* cas_members;
+  const int32_t* cas_prefix;
+  const int32_t* member_ok;
+  float* cas_o;
+  float* cas_ml;
+  int32_t* unit_bad;
+  int32_t cas_max_blocks, cas_groups, cas_np_max;
 };
 
 __device__ __forceinline__ void raise_abort(Ctl& c, uint32_t* err) {
@@ -126,11 +149,43 @@ __device__ PItem make_item(const PrefillParams& P, int idx, int total) {
   return r;
 }
 
+// A cascade item: group g by its item prefix, then (member tile, kv head, key split).
+__device__ PItem make_cas_item(const PrefillParams& P, int idx, int total) {
+  PItem r{};
+  if (idx >= total) {
+    r.idx = -1;
+    return r;
+  }
+  int lo = 0, hi = P.cas_groups - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (P.cas_prefix[mid] <= idx) lo = mid; else hi = mid - 1;
+  }
+  r.idx = idx;
+  r.seq = lo;
+  const int pb = P.cas_blocks[lo];
+  const int e0 = P.cas_start[lo], e1 = P.cas_start[lo + 1];
+  if (pb < 1 || pb > P.cas_max_blocks || e1 <= e0) return r;  // inconsistent plan: invalid item
+  const int np = static_cast<int>(cascade_splits(int64_t(pb) * kBlock));
+  const int local = idx - P.cas_prefix[lo];
+  r.split = local % np;
+  r.head = (local / np) % P.hkv;
+  r.qt = local / np / P.hkv;
+  r.j0 = e0 + r.qt * P.rows_q;
+  r.nq = min(P.rows_q, e1 - r.j0);
+  r.ks = r.split * kCascadeSplitKeys;
+  r.kend = min(pb * kBlock, r.ks + kCascadeSplitKeys);
+  r.nt = (r.kend - r.ks + kTileKeys - 1) / kTileKeys;
+  r.valid = (r.nq > 0 && r.ks < r.kend) ? 1 : 0;
+  return r;
+}
+
 // ------------------------------------------------------------------ producer warp
+template <bool kCas>
 __device__ void producer_warp(const PrefillParams& P, const CUtensorMap* qmap, const CUtensorMap* kmap,
                               const CUtensorMap* vmap, Ctl& c, uint8_t* qbuf, uint8_t* stages) {
   const int lane = threadIdx.x & 31;
-  const int total = P.pre_prefix[P.num_seqs];
+  const int total = kCas ? P.cas_prefix[P.cas_groups] : P.pre_prefix[P.num_seqs];
   volatile int* abort_flag = &c.abort_flag;
   uint32_t it = 0, tc = 0, qc = 0;
   bool ok = true;
@@ -142,7 +197,7 @@ __device__ void producer_warp(const PrefillParams& P, const CUtensorMap* qmap, c
     }
     if (lane == 0) {
       const int idx = atomicAdd(P.queue, 1);
-      c.ring[slot] = make_item(P, idx, total);
+      c.ring[slot] = kCas ? make_cas_item(P, idx, total) : make_item(P, idx, total);
       c.bad[slot] = 0;
       mbar_arrive(&c.item_full[slot]);
     }
@@ -151,25 +206,28 @@ __device__ void producer_warp(const PrefillParams& P, const CUtensorMap* qmap, c
     ++it;
     if (info.idx < 0) break;
     if (!info.valid) continue;
-    if (!mbar_wait(&c.q_free, (qc & 1) ^ 1, abort_flag)) {
-      ok = false;
-      break;
+    if (!kCas) {  // (cascade: the softmax warps gather Q)
+      if (!mbar_wait(&c.q_free, (qc & 1) ^ 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&c.q_full, kTileBytes);
+        const int32_t y = info.head * P.group, z = info.t0 + info.j0;
+        tma_load_3d(qbuf, qmap, &c.q_full, 0, y, z, l2_policy_evict_first());
+        tma_load_3d(qbuf + kHalfBytes, qmap, &c.q_full, 64, y, z, l2_policy_evict_first());
+      }
+      ++qc;
     }
-    if (lane == 0) {
-      mbar_arrive_expect_tx(&c.q_full, kTileBytes);
-      const int32_t y = info.head * P.group, z = info.t0 + info.j0;
-      tma_load_3d(qbuf, qmap, &c.q_full, 0, y, z, l2_policy_evict_first());
-      tma_load_3d(qbuf + kHalfBytes, qmap, &c.q_full, 64, y, z, l2_policy_evict_first());
-    }
-    ++qc;
-    const int32_t* btrow = P.bt + static_cast<int64_t>(info.seq) * P.max_blocks;
+    const int32_t* btrow = kCas ? P.cas_tables + static_cast<int64_t>(info.seq) * P.cas_max_blocks
+                                : P.bt + static_cast<int64_t>(info.seq) * P.max_blocks;
     for (int j = 0; j < info.nt; ++j) {
       const int st = tc % kStages;
       if (!mbar_wait(&c.empty[st], ((tc / kStages) & 1) ^ 1, abort_flag)) {
         ok = false;
         break;
       }
-      const int t0 = j * kTileKeys;
+      const int t0 = info.ks + j * kTileKeys;
       const int nblk = min(kBlocksPerTile, (info.kend - t0 + kBlock - 1) / kBlock);
       int id = 0;
       bool bad = false;
@@ -296,13 +354,15 @@ __device__ void mma_warp(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uint8_t*
 }
 
 // ------------------------------------------------------------------ softmax warps
-__device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* stages, uint8_t* pbuf, uint32_t tmem) {
+template <bool kCas>
+__device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uint8_t* stages, uint8_t* pbuf,
+                              uint32_t tmem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wq = warp & 3;
   const int r = wq * 32 + lane;  // tile row
   const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
   volatile int* abort_flag = &c.abort_flag;
-  uint32_t it = 0, tc = 0;
+  uint32_t it = 0, tc = 0, qc = 0;
   bool ok = true;
   const int rj = r / P.gp, rg = r % P.gp;  // query offset and head of this row within a tile
 
@@ -319,6 +379,12 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* stages, u
     const bool row_out = info.nq > 0 && rj < info.nq && rg < P.group;  // a real (token, head) row
     __nv_bfloat16* orow = P.out + ((static_cast<int64_t>(info.t0) + j_row) * P.hq +
                                    static_cast<int64_t>(info.head) * P.group + rg) * 128;
+    if (kCas && !info.valid) {
+      if (r == 0) flag_error(P.err, kErrLength);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&c.item_empty[slot]);
+      continue;
+    }
     if (!info.valid) {
       if (r == 0 && info.head == 0) flag_error(P.err, kErrLength);
       const int64_t q0 = P.qsl[info.seq], q1 = P.qsl[info.seq + 1];
@@ -331,17 +397,46 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* stages, u
       if (lane == 0) mbar_arrive(&c.item_empty[slot]);
       continue;
     }
+    // this row's member entry (cascade) and whether it is stored
+    const int entry = info.j0 + rj;
+    const bool cas_live = kCas && rj < info.nq && P.member_ok[entry] != 0;
+    if (kCas) {
+      // gather the query row of (member, head) into the swizzled K-major Q tile once
+      // the previous item's last S = Q K^T has read it
+      if (!mbar_wait(&c.q_free, (qc & 1) ^ 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      uint4 qv[16];
+      if (cas_live && rg < P.group) {
+        const int64_t t = P.qsl[P.cas_members[entry]];
+        const uint4* src = reinterpret_cast<const uint4*>(
+            P.q + (t * P.hq + static_cast<int64_t>(info.head) * P.group + rg) * 128);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) qv[k] = __ldg(src + k);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) qv[k] = make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        *reinterpret_cast<uint4*>(qbuf + (k >> 3) * kHalfBytes + r * 128 + (((k & 7) ^ (r & 7)) << 4)) = qv[k];
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&c.q_full);
+      ++qc;
+    }
     // causal bound of this row (padding rows borrow the last real query's bound)
     const int pos = info.ctx + min(j_row, info.q_len - 1);
     const int L = info.ctx + info.q_len;
     // V rows from here on are either past the context or not loaded this item:
     // they are zeroed so that 0-weight keys cannot carry non-finite bytes into P V
-    const int zero_from = min(L, ((info.kend + kBlock - 1) / kBlock) * kBlock);
+    const int zero_from = kCas ? info.kend : min(L, ((info.kend + kBlock - 1) / kBlock) * kBlock);
     float m_ref = -INFINITY, l_sum = 0.f;
 
     for (int j = 0; j < info.nt && ok; ++j) {
       const int st = tc % kStages, sb = tc & 1, pb = tc & 1;
-      const int k0 = j * kTileKeys;
+      const int k0 = info.ks + j * kTileKeys;
       if (!mbar_wait(&c.s_full[sb], (tc >> 1) & 1, abort_flag)) {
         ok = false;
         break;
@@ -360,7 +455,8 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* stages, u
       __syncwarp();
       if (lane == 0) mbar_arrive(&c.s_free[sb]);
       float tmax = -INFINITY;
-      const int nvis = pos - k0 + 1;  // keys k0 .. k0 + nvis - 1 are visible to this row
+      // keys k0 .. k0 + nvis - 1 are visible to this row (cascade: the whole split)
+      const int nvis = kCas ? info.kend - k0 : pos - k0 + 1;
 #pragma unroll
       for (int k = 0; k < 128; ++k) {
         s[k] = k < nvis ? s[k] * P.scale_log2 : -INFINITY;
@@ -442,6 +538,35 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* stages, u
     }
     tc_fence_after();
     const bool bad = c.bad[slot] != 0;
+    if (kCas) {
+      // the row's partial: accumulator [slot][head][128], then max and sum
+      const int64_t cslot = (static_cast<int64_t>(entry) * P.hkv + info.head) * P.cas_np_max + info.split;
+      float4* dst = reinterpret_cast<float4*>(P.cas_o + (cslot * P.gp + rg) * 128);
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        uint32_t v[16];
+        tmem_ld16(tmem + lane_off + kOCol + 16 * ch, v);
+        tmem_ld_wait();
+        if (cas_live) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            dst[4 * ch + q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                          __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+        }
+      }
+      if (cas_live) {
+        P.cas_ml[(cslot * P.gp + rg) * 2] = m_ref;
+        P.cas_ml[(cslot * P.gp + rg) * 2 + 1] = l_sum;
+        if (bad && rg == 0) P.unit_bad[static_cast<int64_t>(P.cas_members[entry]) * P.hkv + info.head] = 1;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&c.o_free);
+        mbar_arrive(&c.item_empty[slot]);
+      }
+      continue;
+    }
     const float inv = bad ? 0.f : 1.f / l_sum;
 #pragma unroll
     for (int ch = 0; ch < 8; ++ch) {
@@ -469,6 +594,7 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* stages, u
   if (!ok && !*abort_flag && lane == 0) raise_abort(c, P.err);
 }
 
+template <bool kCas>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                                                               const __grid_constant__ CUtensorMap kmap,
                                                               const __grid_constant__ CUtensorMap vmap,
@@ -494,7 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     }
     mbar_init(&c.o_full, 1);
     mbar_init(&c.o_free, 4);
-    mbar_init(&c.q_full, 1);
+    mbar_init(&c.q_full, kCas ? 4 : 1);  // cascade: the four softmax warps gather Q
     mbar_init(&c.q_free, 1);
     for (int s = 0; s < kRing; ++s) {
       mbar_init(&c.item_full[s], 1);
@@ -512,9 +638,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = c.tmem_base;
-  if (warp == 0) producer_warp(P, &qmap, &kmap, &vmap, c, qbuf, stages);
+  if (warp == 0) producer_warp<kCas>(P, &qmap, &kmap, &vmap, c, qbuf, stages);
   else if (warp == 1) mma_warp(P, c, qbuf, stages, pbuf, tmem);
-  else softmax_warps(P, c, stages, pbuf, tmem);
+  else softmax_warps<kCas>(P, c, qbuf, stages, pbuf, tmem);
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -562,9 +688,62 @@ int launch_prefill_tc(const AttnArgs& a, const Workspace& ws, int num_sms, uint3
   p.hq = a.num_q_heads;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   TraceScope trace(kTracePrefill, s);
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  cudaError_t e =
+      cudaFuncSetAttribute(prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return cuda_status(e);
-  prefill_kernel<<<num_sms, kThreads, kSmemBytes, s>>>(qm, km, vm, p);
+  prefill_kernel<false><<<num_sms, kThreads, kSmemBytes, s>>>(qm, km, vm, p);
+  return cuda_status(cudaGetLastError());
+}
+
+int launch_cascade_tc(const AttnArgs& a, const CascadeArgs& cas, const Workspace& ws, int num_sms, uint32_t* err,
+                      cudaStream_t s) {
+  const int hkv = a.cache.num_kv_heads;
+  const int group = a.num_q_heads / hkv;
+  if (group > 16 || a.cache.head_dim != 128 || a.cache.dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+  if (cas.num_groups <= 0 || cas.num_members <= 0 || !ws.cas_o) return PKV_OK;
+  const int gp = group <= 4 ? 4 : (group <= 8 ? 8 : 16);
+  const uint64_t rows = static_cast<uint64_t>(a.cache.num_blocks) * hkv * kBlock;
+  if (rows >= (1ull << 31) || a.num_tokens >= (int64_t(1) << 31)) return PKV_ERR_UNSUPPORTED;
+  CUtensorMap km, vm;
+  int st = encode_tensor_map_2d(&km, a.k_cache, 128, rows, 256, 64, 16);
+  if (st) return st;
+  st = encode_tensor_map_2d(&vm, a.v_cache, 128, rows, 256, 64, 16);
+  if (st) return st;
+  PrefillParams p{};
+  p.bt = a.block_tables;
+  p.seq_lens = a.seq_lens;
+  p.qsl = a.qsl;
+  p.queue = ws.counters + kCascadeQueueSlot;
+  p.err = err;
+  p.num_blocks = a.cache.num_blocks;
+  p.num_tokens = a.num_tokens;
+  p.num_seqs = a.num_seqs;
+  p.max_blocks = a.max_blocks;
+  p.hkv = hkv;
+  p.group = group;
+  p.gp = gp;
+  p.rows_q = kTileKeys / gp;
+  p.hq = a.num_q_heads;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.q = static_cast<const __nv_bfloat16*>(a.q);
+  p.cas_tables = cas.tables;
+  p.cas_blocks = cas.blocks;
+  p.cas_start = cas.start;
+  p.cas_members = cas.members;
+  p.cas_prefix = ws.cas_prefix;
+  p.member_ok = ws.member_ok;
+  p.cas_o = ws.cas_o;
+  p.cas_ml = ws.cas_ml;
+  p.unit_bad = ws.unit_bad;
+  p.cas_max_blocks = cas.max_blocks;
+  p.cas_groups = cas.num_groups;
+  p.cas_np_max = ws.cas_np_max;
+  TraceScope trace(kTraceCascade, s);
+  cudaError_t e =
+      cudaFuncSetAttribute(prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return cuda_status(e);
+  // the Q tensor map is unused in this mode (Q rows are gathered); K's stands in
+  prefill_kernel<true><<<num_sms, kThreads, kSmemBytes, s>>>(km, km, vm, p);
   return cuda_status(cudaGetLastError());
 }
 

@@ -30,6 +30,14 @@ __host__ __device__ inline int64_t decode_splits(int64_t L) {
 }
 constexpr int kNumQueueCounters = 8; // work-queue counters in the workspace
 constexpr int kMergeCountSlot = 2;   // counters[2]: number of requests in the merge list
+constexpr int kCascadeQueueSlot = 3; // counters[3]: the shared-prefix kernel's work queue
+
+// Shared-prefix (cascade) key splits: a prefix of P tokens is attended in pieces of
+// kCascadeSplitKeys keys, a function of P alone.
+constexpr int kCascadeSplitKeys = 512;
+__host__ __device__ inline int64_t cascade_splits(int64_t P) {
+  return (P + kCascadeSplitKeys - 1) / kCascadeSplitKeys;
+}
 
 // Trace kinds (pkv_trace_read).
 enum TraceKind : int {
@@ -41,6 +49,7 @@ enum TraceKind : int {
   kTracePrefill = 5,
   kTraceGeneric = 6,
   kTraceMerge = 7,
+  kTraceCascade = 8,
 };
 
 __device__ __forceinline__ void flag_error(uint32_t* err, uint32_t bits) {
@@ -136,11 +145,32 @@ struct Workspace {
   int32_t* merge_list;   // [num_seqs] decode requests cut into several splits
   float* part_ml;        // [max_dec_items * GP * 2] split running max and sum
   float* part_o;         // [max_dec_items * head_dim * GP] split accumulators
+  // shared-prefix (cascade) state; all null without prefix groups
+  int32_t* seq_prefix;   // [num_seqs] prefix tokens attended by the cascade kernel (0: none)
+  int32_t* seq_entry;    // [num_seqs] the request's member-list entry (-1: none)
+  int32_t* member_ok;    // [num_members] the entry passed the planner's checks
+  int32_t* cas_prefix;   // [num_groups + 1] exclusive prefix of cascade work items
+  float* cas_ml;         // [num_members * hkv * cas_np_max * GP * 2] prefix partial max and sum
+  float* cas_o;          // [num_members * hkv * cas_np_max * GP * head_dim] prefix accumulators
+  int32_t cas_np_max;    // key splits of the longest prefix
 };
+
+// Shared-prefix groups of one call (the device arrays of pkv_prefix_groups).
+struct CascadeArgs {
+  const int32_t* tables;   // [num_groups][max_blocks] physical ids of each prefix
+  int32_t max_blocks;
+  const int32_t* blocks;   // [num_groups] prefix length in blocks
+  const int32_t* start;    // [num_groups + 1] CSR offsets into members
+  const int32_t* members;  // [num_members] request indices
+  int32_t num_groups;
+  int32_t num_members;
+};
+
 // Computes the layout at `base` (nullptr: only the size) and returns the bytes needed;
 // `group` is the padded head-group width GP the decode partials are stored with.
+// With `cas`, also the shared-prefix arrays.
 size_t layout_workspace(void* base, int32_t num_seqs, int32_t hkv, int32_t group, int32_t head_dim,
-                        int64_t max_dec_items, Workspace* ws);
+                        int64_t max_dec_items, Workspace* ws, const CascadeArgs* cas = nullptr);
 
 struct PlanArgs {
   const int32_t* seq_lens;
@@ -158,9 +188,21 @@ struct PlanArgs {
   int32_t* unit_bad;
   int32_t* merge_list;
   uint32_t* err;
+  // shared-prefix groups (cas.num_groups == 0: none)
+  const int32_t* bt = nullptr;
+  CascadeArgs cas{};
+  int32_t cas_rows = 0;  // member requests per cascade tile
+  int32_t* seq_prefix = nullptr;
+  int32_t* seq_entry = nullptr;
+  int32_t* member_ok = nullptr;
+  int32_t* cas_prefix = nullptr;
 };
 int launch_plan(const PlanArgs& p, cudaStream_t s);
 int launch_decode_tc(const AttnArgs& a, const Workspace& ws, int num_sms, uint32_t* err, cudaStream_t s);
+// Attends the member decodes of every prefix group to the group's shared prefix,
+// writing per-split partials for the merge (after launch_plan, before launch_decode_tc).
+int launch_cascade_tc(const AttnArgs& a, const CascadeArgs& cas, const Workspace& ws, int num_sms, uint32_t* err,
+                      cudaStream_t s);
 int launch_prefill_tc(const AttnArgs& a, const Workspace& ws, int num_sms, uint32_t* err, cudaStream_t s);
 int encode_tensor_map_3d(CUtensorMap* map, const void* base, const uint64_t dims[3], const uint64_t strides[2],
                          const uint32_t box[3]);

@@ -89,3 +89,19 @@ def test_binding_refuses_cpu_tensors(lib):
     with pytest.raises(ValueError):
         pkv.pkv_write(torch.zeros(1, 1, 64), torch.zeros(1, 1, 64), torch.zeros(1, dtype=torch.int64), kc,
                       kc.clone())
+
+
+def test_cascade_host_checks_fail_without_launching(lib):
+    import paged_kv_cache_248_gb300 as pkv
+    P = ctypes.c_void_p
+    fake = P(0x1000)  # never dereferenced: each call below fails its host checks first
+    desc = _desc(pkv, d=128, dt=1)
+    args = (fake, fake, fake, ctypes.byref(desc), fake, 4, fake, fake, 2, 8, 2, 1, 64, ctypes.c_float(0.1))
+    g = pkv._PrefixGroups(fake, 4, fake, fake, fake, -1, 3)
+    assert lib.paged_attention_cascade(*args, ctypes.byref(g), fake, None) == pkv.PKV_ERR_INVALID_ARG
+    g = pkv._PrefixGroups(None, 4, fake, fake, fake, 2, 3)       # a group array missing
+    assert lib.paged_attention_cascade(*args, ctypes.byref(g), fake, None) == pkv.PKV_ERR_INVALID_ARG
+    g = pkv._PrefixGroups(fake, 0, fake, fake, fake, 2, 3)       # max_prefix_blocks < 1
+    assert lib.paged_attention_cascade(*args, ctypes.byref(g), fake, None) == pkv.PKV_ERR_INVALID_ARG
+    bad_scale = args[:-1] + (ctypes.c_float(float("nan")),)
+    assert lib.paged_attention_cascade(*bad_scale, None, fake, None) == pkv.PKV_ERR_INVALID_ARG

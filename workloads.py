@@ -212,6 +212,81 @@ def make(name: str, seed: int | None = None) -> Workload:
     raise KeyError(name)
 
 
+def shared_prefix_case(seed: int, prefix_blocks=(5, 33, 70), members=(9, 40, 3), num_kv_heads: int = 2,
+                       group: int = 4, max_suffix: int = 300, bystanders: int = 6, bad_hints: bool = True,
+                       long_suffix: int = 0) -> tuple[Workload, dict]:
+    """A decode batch with shared-prefix groups, and the group hints for it.
+
+    Group g's ``members[g]`` decode requests all start with the same
+    ``prefix_blocks[g]`` physical blocks, then a suffix of U[1, max_suffix] tokens in
+    blocks of their own (``long_suffix`` > 0 gives the first member of each group that
+    many suffix tokens instead).  ``bystanders`` more requests -- decodes and
+    prefill chunks -- have tables of their own.  Requests are shuffled.  With
+    ``bad_hints`` the hint lists also name requests that must not be treated as
+    members: a prefill chunk and a decode whose context ends inside the prefix (both
+    with tables that start with the prefix), a request listed in two groups, and a
+    decode whose table does not start with the prefix.  Returns the workload and
+    ``{"prefix_block_tables", "prefix_num_blocks", "member_start", "member_seqs"}``.
+    """
+    rng = np.random.default_rng(seed)
+    G = len(prefix_blocks)
+    reqs = []  # (q_len, L, group or -1, table_is_prefixed, hint_groups)
+    for g in range(G):
+        P = prefix_blocks[g] * BLOCK
+        for m in range(members[g]):
+            sfx = long_suffix if (long_suffix and m == 0) else int(rng.integers(1, max_suffix, endpoint=True))
+            reqs.append((1, P + sfx, g, True, [g]))
+    for b in range(bystanders):
+        if b % 2 == 0:
+            reqs.append((1, int(rng.integers(1, 1500, endpoint=True)), -1, False, []))
+        else:
+            q = int(rng.integers(2, 150, endpoint=True))
+            reqs.append((q, q + int(rng.integers(0, 400, endpoint=True)), -1, False, []))
+    if bad_hints:
+        P0 = prefix_blocks[0] * BLOCK
+        reqs.append((37, P0 + 60, 0, True, [0]))                    # a prefill chunk after the prefix
+        reqs.append((1, max(1, P0 - 3), 0, True, [0]))             # context ends inside the prefix
+        g1 = 1 % G
+        reqs.append((1, prefix_blocks[g1] * BLOCK + 20, g1, True, [g1, 0]))  # listed in two groups
+        reqs.append((1, prefix_blocks[g1] * BLOCK + 50, -1, False, [g1]))   # its table is its own
+    order = rng.permutation(len(reqs))
+    reqs = [reqs[k] for k in order]
+    n = len(reqs)
+    q_lens = np.array([r[0] for r in reqs], np.int32)
+    L = np.array([r[1] for r in reqs], np.int32)
+    need_own = sum((int(r[1]) + BLOCK - 1) // BLOCK for r in reqs)
+    pool = sum(prefix_blocks) + need_own + 11
+    ids = rng.permutation(pool).astype(np.int32)
+    prefix_ids, pos = [], 0
+    for g in range(G):
+        prefix_ids.append(ids[pos:pos + prefix_blocks[g]])
+        pos += prefix_blocks[g]
+    mb = max((int(x) + BLOCK - 1) // BLOCK for x in L) + 1
+    bt = np.full((n, mb), -1, np.int32)
+    for i, (q, Li, g, prefixed, _) in enumerate(reqs):
+        nb = (Li + BLOCK - 1) // BLOCK
+        k = 0
+        if prefixed:
+            k = min(nb, prefix_blocks[g])
+            bt[i, :k] = prefix_ids[g][:k]
+        bt[i, k:nb] = ids[pos:pos + nb - k]
+        pos += nb - k
+    lists = [[] for _ in range(G)]
+    for i, r in enumerate(reqs):
+        for g in r[4]:
+            lists[g].append(i)
+    member_start = np.concatenate([[0], np.cumsum([len(x) for x in lists])]).astype(np.int32)
+    member_seqs = np.array([i for x in lists for i in x], np.int32)
+    mpb = max(prefix_blocks)
+    ptab = np.full((G, mpb), -1, np.int32)
+    for g in range(G):
+        ptab[g, :prefix_blocks[g]] = prefix_ids[g]
+    w = Workload(f"shared{seed}", "bf16", group * num_kv_heads, num_kv_heads, 128, pool, 1.0 / math.sqrt(128), L,
+                 _qsl(q_lens), bt, seed)
+    return w, {"prefix_block_tables": ptab, "prefix_num_blocks": np.array(prefix_blocks, np.int32),
+               "member_start": member_start, "member_seqs": member_seqs}
+
+
 def random_case(seed: int, num_seqs: int = 5, max_ctx: int = 80, max_q: int = 40,
                 group: int = 2, num_kv_heads: int = 2, head_dim: int = 64, dtype: str = "f32",
                 decode_frac: float = 0.4, pool_slack: int = 7, extra_table_cols: int = 2) -> Workload:
