@@ -45,9 +45,9 @@ METRIC = "decode KV-read GB/s (% of HBM peak); mixed-step tokens/sec at 1 GB300"
 # It scales to other workloads by the bytes processed, and it is reported only while
 # the profiled sources are unchanged.
 NCU_TRAFFIC = {
-    "decode": {"ratio": 510.65 / 503.62,
+    "decode": {"ratio": 510.84 / 503.62,
                "sources": ("k_decode.cu", "ptx.cuh", "pkv_internal.cuh"),
-               "sha256": "c574056f5615eed041ee45edf5b04def0a387bc45f0b77b50be6896217fc5efb"},
+               "sha256": "ea73d0a9971d1649a3c4d47fffb59371cd8e67c914792b674e20e49901272f01"},
 }
 
 
@@ -171,8 +171,8 @@ class ClockSampler:
 class Step:
     """Device-resident inputs of one workload and the three C-ABI calls of a step."""
 
-    def __init__(self, pkv, w, device, cascade: bool = True):
-        self.pkv, self.w = pkv, w
+    def __init__(self, pkv, w, device, cascade: bool = True, fused: bool = True):
+        self.pkv, self.w, self.fused = pkv, w, fused
         t = w.make_tensors(device)
         self.t = t
         dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)  # noqa: E731
@@ -196,13 +196,21 @@ class Step:
             p.paged_attention(q, t["k_cache"], t["v_cache"], self.bt, self.sl, self.qsl, w.scale,
                               w.max_query_len, w.max_seq_len, out=out)
 
-    def run(self):
+    def write_and_attend(self, q, k_new, v_new, out):
         p, w, t = self.pkv, self.w, self.t
+        if self.fused:  # slot mapping, scatter and attention in one call
+            p.paged_attention_step(q, k_new, v_new, t["k_cache"], t["v_cache"], self.bt, self.sl, self.qsl, w.scale,
+                                   w.max_query_len, w.max_seq_len, prefix_groups=self.groups, out=out)
+        else:
+            p.pkv_slot_mapping(self.bt, self.sl, self.qsl, w.num_tokens, out=self.slots)
+            p.pkv_write(k_new, v_new, self.slots, t["k_cache"], t["v_cache"])
+            self.attend(q, out)
+
+    def run(self):
+        p, t = self.pkv, self.t
         if self.cow is not None:
             p.pkv_copy_blocks(self.cow[0], self.cow[1], t["k_cache"], t["v_cache"])
-        p.pkv_slot_mapping(self.bt, self.sl, self.qsl, w.num_tokens, out=self.slots)
-        p.pkv_write(t["k_new"], t["v_new"], self.slots, t["k_cache"], t["v_cache"])
-        self.attend(t["q"], self.out)
+        self.write_and_attend(t["q"], t["k_new"], t["v_new"], self.out)
 
     def attention_only(self):
         self.attend(self.t["q"], self.out)
@@ -210,7 +218,8 @@ class Step:
 
 class E2EStep:
     """The same step from pinned HOST buffers: H2D of the step's inputs (q, new K/V,
-    block tables, lengths), the three calls, D2H of the attention output."""
+    block tables, lengths, copy-on-write pairs), the library calls, D2H of the
+    attention output."""
 
     def __init__(self, step: Step):
         self.s = step
@@ -218,10 +227,12 @@ class E2EStep:
         pin = lambda x: x.detach().to("cpu").pin_memory()  # noqa: E731
         self.h = {k: pin(t[k]) for k in ("q", "k_new", "v_new")}
         self.h_bt, self.h_sl, self.h_qsl = pin(step.bt), pin(step.sl), pin(step.qsl)
+        self.h_cow = tuple(pin(x) for x in step.cow) if step.cow is not None else ()
         self.h_out = torch.empty(t["q"].shape, dtype=t["q"].dtype).pin_memory()
         self.d = {k: torch.empty_like(t[k]) for k in ("q", "k_new", "v_new")}
         self.h2d = sum(x.numel() * x.element_size() for x in list(self.h.values()) + [self.h_bt, self.h_sl,
-                                                                                           self.h_qsl])
+                                                                                           self.h_qsl] +
+                       list(self.h_cow))
         self.d2h = self.h_out.numel() * self.h_out.element_size()
 
     def run(self):
@@ -231,9 +242,11 @@ class E2EStep:
         s.bt.copy_(self.h_bt, non_blocking=True)
         s.sl.copy_(self.h_sl, non_blocking=True)
         s.qsl.copy_(self.h_qsl, non_blocking=True)
-        p.pkv_slot_mapping(s.bt, s.sl, s.qsl, w.num_tokens, out=s.slots)
-        p.pkv_write(self.d["k_new"], self.d["v_new"], s.slots, t["k_cache"], t["v_cache"])
-        s.attend(self.d["q"], s.out)
+        if s.cow is not None:
+            for dst, src in zip(s.cow, self.h_cow):
+                dst.copy_(src, non_blocking=True)
+            p.pkv_copy_blocks(s.cow[0], s.cow[1], t["k_cache"], t["v_cache"])
+        s.write_and_attend(self.d["q"], self.d["k_new"], self.d["v_new"], s.out)
         self.h_out.copy_(s.out, non_blocking=True)
 
 
@@ -335,6 +348,8 @@ def main():
     ap.add_argument("--no-decode-line", action="store_true")
     ap.add_argument("--no-cascade", action="store_true",
                     help="attend a shared prefix per request instead of once per group")
+    ap.add_argument("--unfused", action="store_true",
+                    help="separate slot-mapping, write and attention calls instead of paged_attention_step")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -356,7 +371,7 @@ def main():
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     pk = peaks()
-    step = Step(pkv, w, device, cascade=not args.no_cascade)
+    step = Step(pkv, w, device, cascade=not args.no_cascade, fused=not args.unfused)
     work_b = algorithmic_bytes(w)
     work_f = algorithmic_flops(w)
 

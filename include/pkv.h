@@ -15,6 +15,8 @@
  *   paged_attention   attention for one continuously-batched step: split-KV GQA
  *                     decode with online softmax and a cross-split merge, plus
  *                     causal chunked prefill, gathering K/V through block tables
+ *   paged_attention_cascade  the same, reading each shared prompt prefix once
+ *   paged_attention_step     slot mapping + K/V scatter + attention in one call
  *
  * Conventions for every call
  *  - Pointers named as device pointers must point to device memory of the current
@@ -194,6 +196,28 @@ PKV_API int paged_attention_cascade(const void* q, const void* k_cache, const vo
                                     const int32_t* query_start_loc, int32_t num_seqs, int32_t num_q_heads,
                                     int64_t num_tokens, int32_t max_query_len, int32_t max_seq_len, float scale,
                                     const pkv_prefix_groups* groups, void* out, void* stream);
+
+/*
+ * paged_attention_step -- the new tokens' slot mapping and K/V scatter, then
+ * attention, in one call: pkv_slot_mapping + pkv_write + paged_attention_cascade
+ * with the same results, bit for bit ("vLLM's PagedAttention" teardown, section
+ * "Continuous batching": every step appends each running request's new tokens to
+ * its blocks and attends over them).  On the bf16 path the mapping and the scatter
+ * run in extra CTAs of the planning launch, so the step has two launches fewer and
+ * no slot array round trip; the kernel boundary orders the writes before every
+ * attention read.  Copy-on-write copies (pkv_copy_blocks) go before this call.
+ * k_new, v_new    device [num_tokens][num_kv_heads][head_dim], cache dtype, required
+ * k_cache, v_cache  written at the new tokens' slots, then read
+ * groups          NULL for none (see paged_attention_cascade)
+ * slot_mapping    optional device int64 [num_tokens]: receives the slots (NULL: not stored)
+ * Everything else and the errors: as paged_attention() and pkv_write().
+ */
+PKV_API int paged_attention_step(const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                                 const pkv_cache_desc* cache, const int32_t* block_tables,
+                                 int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                 const int32_t* query_start_loc, int32_t num_seqs, int32_t num_q_heads,
+                                 int64_t num_tokens, int32_t max_query_len, int32_t max_seq_len, float scale,
+                                 const pkv_prefix_groups* groups, int64_t* slot_mapping, void* out, void* stream);
 
 /*
  * paged_attention_noalloc -- paged_attention() for callers that cannot let a library

@@ -9,6 +9,7 @@ If the library has not been built, importing a function raises immediately.
 
 Functions carry the C names:
   pkv_slot_mapping, pkv_write, pkv_copy_blocks, paged_attention, paged_attention_cascade,
+  paged_attention_step,
   pkv_get_last_error, pkv_peek_error_bits, pkv_trace_enable, pkv_trace_read,
   pkv_num_workers, pkv_shutdown, pkv_umma_selftest, pkv_tma_selftest.
 """
@@ -68,6 +69,8 @@ def lib():
                 "paged_attention": [P, P, P, D, P, i32, P, P, i32, i32, i64, i32, i32, f32, P, P],
                 "paged_attention_cascade": [P, P, P, D, P, i32, P, P, i32, i32, i64, i32, i32, f32,
                                             ctypes.POINTER(_PrefixGroups), P, P],
+                "paged_attention_step": [P, P, P, P, P, D, P, i32, P, P, i32, i32, i64, i32, i32, f32,
+                                         ctypes.POINTER(_PrefixGroups), P, P, P],
                 "pkv_get_last_error": [P],
                 "pkv_peek_error_bits": [P, ctypes.POINTER(ctypes.c_uint32)],
                 "pkv_num_workers": [ctypes.POINTER(ctypes.c_int32)],
@@ -191,16 +194,7 @@ def paged_attention_cascade(q: torch.Tensor, k_cache: torch.Tensor, v_cache: tor
     if out is None:
         out = torch.empty_like(q)
     T, hq, d = q.shape
-    if prefix_block_tables.dim() != 2:
-        raise ValueError("prefix_block_tables must be [num_groups, max_prefix_blocks]")
-    G, M = prefix_num_blocks.shape[0], member_seqs.shape[0]
-    if prefix_block_tables.shape[0] != G or member_start.shape[0] != G + 1:
-        raise ValueError("prefix group arrays disagree on the number of groups")
-    groups = _PrefixGroups(_dev(prefix_block_tables, "prefix_block_tables", torch.int32),
-                           prefix_block_tables.shape[1],
-                           _dev(prefix_num_blocks, "prefix_num_blocks", torch.int32),
-                           _dev(member_start, "member_start", torch.int32),
-                           _dev(member_seqs, "member_seqs", torch.int32) if M else None, G, M)
+    groups = _groups((prefix_block_tables, prefix_num_blocks, member_start, member_seqs))
     _check(lib().paged_attention_cascade(_dev(q, "q", k_cache.dtype), _dev(k_cache, "k_cache"),
                                          _dev(v_cache, "v_cache"), ctypes.byref(desc),
                                          _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
@@ -209,6 +203,51 @@ def paged_attention_cascade(q: torch.Tensor, k_cache: torch.Tensor, v_cache: tor
                                          hq, T, int(max_query_len), int(max_seq_len), float(scale),
                                          ctypes.byref(groups), _dev(out, "out", k_cache.dtype), _stream(stream)),
            "paged_attention_cascade")
+    return out
+
+
+def _groups(prefix_groups):
+    """(prefix_block_tables, prefix_num_blocks, member_start, member_seqs) -> struct, or None."""
+    if prefix_groups is None:
+        return None
+    tables, nblocks, start, members = prefix_groups
+    if tables.dim() != 2:
+        raise ValueError("prefix_block_tables must be [num_groups, max_prefix_blocks]")
+    G, M = nblocks.shape[0], members.shape[0]
+    if tables.shape[0] != G or start.shape[0] != G + 1:
+        raise ValueError("prefix group arrays disagree on the number of groups")
+    return _PrefixGroups(_dev(tables, "prefix_block_tables", torch.int32), tables.shape[1],
+                         _dev(nblocks, "prefix_num_blocks", torch.int32), _dev(start, "member_start", torch.int32),
+                         _dev(members, "member_seqs", torch.int32) if M else None, G, M)
+
+
+def paged_attention_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
+                         v_cache: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                         query_start_loc: torch.Tensor, scale: float, max_query_len: int, max_seq_len: int,
+                         prefix_groups=None, slot_mapping: torch.Tensor | None = None,
+                         out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Slot mapping, K/V scatter and attention of one step in one call (same results as
+    pkv_slot_mapping + pkv_write + paged_attention[_cascade]).  ``prefix_groups`` is
+    None or (prefix_block_tables, prefix_num_blocks, member_start, member_seqs);
+    ``slot_mapping``, if given, receives the int64 slots."""
+    desc = _cache_desc(k_cache, v_cache)
+    if out is None:
+        out = torch.empty_like(q)
+    T, hq, d = q.shape
+    if k_new.shape != (T, k_cache.shape[1], d) or v_new.shape != k_new.shape:
+        raise ValueError("k_new and v_new must be [num_tokens, num_kv_heads, head_dim]")
+    g = _groups(prefix_groups)
+    _check(lib().paged_attention_step(_dev(q, "q", k_cache.dtype), _dev(k_new, "k_new", k_cache.dtype),
+                                      _dev(v_new, "v_new", k_cache.dtype), _dev(k_cache, "k_cache"),
+                                      _dev(v_cache, "v_cache"), ctypes.byref(desc),
+                                      _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+                                      _dev(seq_lens, "seq_lens", torch.int32),
+                                      _dev(query_start_loc, "query_start_loc", torch.int32), seq_lens.shape[0],
+                                      hq, T, int(max_query_len), int(max_seq_len), float(scale),
+                                      ctypes.byref(g) if g is not None else None,
+                                      _dev(slot_mapping, "slot_mapping", torch.int64) if slot_mapping is not None
+                                      else None, _dev(out, "out", k_cache.dtype), _stream(stream)),
+           "paged_attention_step")
     return out
 
 

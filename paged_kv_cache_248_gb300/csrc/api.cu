@@ -249,14 +249,17 @@ int pkv_copy_blocks(const int32_t* src, const int32_t* dst, int64_t n, void* k_c
 
 namespace {
 
-// paged_attention and paged_attention_cascade: `groups` null = no shared prefixes.
-int attention_impl(const void* q, const void* k_cache, const void* v_cache, const pkv_cache_desc* cache,
-                   const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
-                   const int32_t* query_start_loc, int32_t num_seqs, int32_t num_q_heads, int64_t num_tokens,
-                   int32_t max_query_len, int32_t max_seq_len, float scale, const pkv_prefix_groups* groups,
-                   void* out, void* stream) {
+// paged_attention, paged_attention_cascade and paged_attention_step: `groups` null =
+// no shared prefixes; `k_new` null = no new tokens to write first.
+int attention_impl(const void* q, const void* k_new, const void* v_new, const void* k_cache, const void* v_cache,
+                   const pkv_cache_desc* cache, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                   const int32_t* seq_lens, const int32_t* query_start_loc, int32_t num_seqs, int32_t num_q_heads,
+                   int64_t num_tokens, int32_t max_query_len, int32_t max_seq_len, float scale,
+                   const pkv_prefix_groups* groups, int64_t* slots_out, void* out, void* stream) {
   int st = check_cache(cache);
   if (st) return st;
+  const bool write = k_new != nullptr;
+  if (write && (!v_new || !aligned16(k_new) || !aligned16(v_new))) return PKV_ERR_INVALID_ARG;
   if (num_tokens < 0 || num_seqs < 0 || num_q_heads <= 0 || num_q_heads % cache->num_kv_heads != 0)
     return PKV_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
@@ -282,7 +285,23 @@ int attention_impl(const void* q, const void* k_cache, const void* v_cache, cons
   AttnArgs a{q,        k_cache,    v_cache,       *cache,      block_tables, max_blocks_per_seq, seq_lens,
              query_start_loc, num_seqs, num_q_heads, num_tokens, max_query_len, max_seq_len, scale, out};
   cudaStream_t s = as_stream(stream);
-  if (cache->dtype == PKV_F32) return launch_generic_attention(a, ctx->err, s);  // groups do not change results
+  if (cache->dtype == PKV_F32) {  // groups do not change results
+    if (write) {
+      int64_t* slots = slots_out;
+      if (!slots) {  // scratch for the slots between the two kernels
+        st = ensure_workspace(ctx, static_cast<size_t>(num_tokens) * sizeof(int64_t), s);
+        if (st) return st;
+        slots = static_cast<int64_t*>(ctx->ws);
+      }
+      st = launch_slot_mapping(block_tables, max_blocks_per_seq, seq_lens, query_start_loc, num_seqs, num_tokens,
+                               slots, ctx->err, s);
+      if (st) return st;
+      st = launch_write(k_new, v_new, slots, num_tokens, const_cast<void*>(k_cache), const_cast<void*>(v_cache),
+                        *cache, ctx->err, s);
+      if (st) return st;
+    }
+    return launch_generic_attention(a, ctx->err, s);
+  }
   // bf16, head_dim 128: tensor-core path
   const int32_t hkv = cache->num_kv_heads;
   const int32_t group = num_q_heads / hkv;
@@ -305,8 +324,20 @@ int attention_impl(const void* q, const void* k_cache, const void* v_cache, cons
   PlanArgs plan{seq_lens, query_start_loc, num_seqs, num_tokens, hkv, max_blocks_per_seq, max_seq_len,
                 kSplitKeys, kTileKeys / gp, ws.counters, ws.dec_prefix, ws.pre_prefix, ws.unit_bad,
                 ws.merge_list, ctx->err};
+  plan.bt = block_tables;
+  if (write) {
+    const int64_t warps_per_cta = 1024 / 32;
+    const int64_t want = (num_tokens + warps_per_cta - 1) / warps_per_cta;
+    plan.k_new = static_cast<const uint4*>(k_new);
+    plan.v_new = static_cast<const uint4*>(v_new);
+    plan.k_cache = static_cast<uint4*>(const_cast<void*>(k_cache));
+    plan.v_cache = static_cast<uint4*>(const_cast<void*>(v_cache));
+    plan.slots_out = slots_out;
+    plan.num_slots = cache->num_blocks * kBlock;
+    plan.vec_per_row = cache->head_dim * 2 / 16;
+    plan.write_ctas = static_cast<int32_t>(want < 2 * ctx->num_sms ? want : 2 * ctx->num_sms);
+  }
   if (casp) {
-    plan.bt = block_tables;
     plan.cas = cas;
     plan.cas_rows = kTileKeys / gp;
     plan.seq_prefix = ws.seq_prefix;
@@ -334,8 +365,9 @@ int paged_attention(const void* q, const void* k_cache, const void* v_cache, con
                     const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
                     const int32_t* query_start_loc, int32_t num_seqs, int32_t num_q_heads, int64_t num_tokens,
                     int32_t max_query_len, int32_t max_seq_len, float scale, void* out, void* stream) {
-  return attention_impl(q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq, seq_lens, query_start_loc,
-                        num_seqs, num_q_heads, num_tokens, max_query_len, max_seq_len, scale, nullptr, out, stream);
+  return attention_impl(q, nullptr, nullptr, k_cache, v_cache, cache, block_tables, max_blocks_per_seq, seq_lens,
+                        query_start_loc, num_seqs, num_q_heads, num_tokens, max_query_len, max_seq_len, scale,
+                        nullptr, nullptr, out, stream);
 }
 
 int paged_attention_cascade(const void* q, const void* k_cache, const void* v_cache, const pkv_cache_desc* cache,
@@ -343,8 +375,21 @@ int paged_attention_cascade(const void* q, const void* k_cache, const void* v_ca
                             const int32_t* query_start_loc, int32_t num_seqs, int32_t num_q_heads,
                             int64_t num_tokens, int32_t max_query_len, int32_t max_seq_len, float scale,
                             const pkv_prefix_groups* groups, void* out, void* stream) {
-  return attention_impl(q, k_cache, v_cache, cache, block_tables, max_blocks_per_seq, seq_lens, query_start_loc,
-                        num_seqs, num_q_heads, num_tokens, max_query_len, max_seq_len, scale, groups, out, stream);
+  return attention_impl(q, nullptr, nullptr, k_cache, v_cache, cache, block_tables, max_blocks_per_seq, seq_lens,
+                        query_start_loc, num_seqs, num_q_heads, num_tokens, max_query_len, max_seq_len, scale,
+                        groups, nullptr, out, stream);
+}
+
+int paged_attention_step(const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                         const pkv_cache_desc* cache, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                         const int32_t* seq_lens, const int32_t* query_start_loc, int32_t num_seqs,
+                         int32_t num_q_heads, int64_t num_tokens, int32_t max_query_len, int32_t max_seq_len,
+                         float scale, const pkv_prefix_groups* groups, int64_t* slot_mapping, void* out,
+                         void* stream) {
+  if (!k_new || !v_new) return PKV_ERR_INVALID_ARG;
+  return attention_impl(q, k_new, v_new, k_cache, v_cache, cache, block_tables, max_blocks_per_seq, seq_lens,
+                        query_start_loc, num_seqs, num_q_heads, num_tokens, max_query_len, max_seq_len, scale,
+                        groups, slot_mapping, out, stream);
 }
 
 int pkv_peek_error_bits(void* stream, uint32_t* bits) {

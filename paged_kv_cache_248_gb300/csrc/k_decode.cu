@@ -56,8 +56,9 @@ struct alignas(16) ItemInfo {
   int32_t idx;  // decode item index; -1 = queue exhausted
   int32_t seq, head, split;
   int32_t nsplit, key_start, key_end, valid;
-  int32_t trow, row_ok, member, pad1;  // the request's query row, whether it is addressable, and
-                                       // whether a shared prefix was attended by the cascade kernel
+  int32_t trow, row_ok, member, centry;  // the request's query row, whether it is addressable,
+                                         // whether a shared prefix was attended by the cascade
+                                         // kernel, and then the request's member-list entry
 };
 
 struct Ctl {
@@ -89,12 +90,36 @@ struct DecodeParams {
   float* part_o;   // [items][128][GP]
   float* part_ml;  // [items][GP][2]
   const int32_t* seq_prefix;  // [num_seqs] keys before this many are the cascade kernel's; null: none
+  const int32_t* seq_entry;   // [num_seqs] member-list entry of a shared-prefix member
+  const float* cas_o;         // prefix partials [entry][hkv][cas_np_max][GP][128]
+  const float* cas_ml;        // [entry][hkv][cas_np_max][GP][2]
+  int32_t cas_np_max;
   uint32_t* err;
   int64_t num_blocks;
   int64_t num_tokens;
   int32_t num_seqs, max_blocks, hkv, group, gp, hq, split_keys;
   float scale_log2;
 };
+
+// Folds one partial (running max m, sum l, accumulator o, per head) into a
+// log-sum-exp merge.
+template <int GP>
+__device__ __forceinline__ void merge_fold(float (&M)[GP], float (&num)[GP], float (&den)[GP], const float (&ml)[2 * GP],
+                                           const float (&ov)[GP]) {
+#pragma unroll
+  for (int g = 0; g < GP; ++g) {
+    const float m_new = fmaxf(M[g], ml[2 * g]);
+    const float a = exp2f(M[g] - m_new);
+    const float b = exp2f(ml[2 * g] - m_new);
+    den[g] = fmaf(den[g], a, ml[2 * g + 1] * b);
+    num[g] = fmaf(num[g], a, ov[g] * b);
+    M[g] = m_new;
+  }
+}
+
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
 
 __device__ __forceinline__ void raise_abort(Ctl& c, uint32_t* err) {
   *reinterpret_cast<volatile int*>(&c.abort_flag) = 1;
@@ -209,6 +234,7 @@ __device__ void scheduler_warp(const DecodeParams& P, Ctl& c) {
       if (ok) {
         r.valid = 1;
         r.member = pre > 0 ? 1 : 0;
+        r.centry = pre > 0 ? __ldg(P.seq_entry + i) : 0;
         if (nsplit == 1) {
           r.key_start = static_cast<int32_t>(pre);
           r.key_end = static_cast<int32_t>(L);
@@ -450,6 +476,17 @@ __device__ void softmax_warps(const DecodeParams& P, Ctl& c, uint8_t* stages, ui
       continue;
     }
 
+    // a shared-prefix member whose own keys are one split finishes here: its prefix
+    // partials (written by the cascade kernel) are pulled into L1 now, folded at the end
+    const bool fold_prefix = info.member && info.nsplit == 1;
+    const int64_t cbase = (static_cast<int64_t>(info.centry) * P.hkv + info.head) * P.cas_np_max;
+    const int npre = fold_prefix ? static_cast<int>(cascade_splits(info.key_start)) : 0;
+    for (int s = 0; s < npre; ++s) {
+#pragma unroll
+      for (int g = 0; g < GP; ++g) prefetch_l1(P.cas_o + ((cbase + s) * GP + g) * 128 + r);
+      if (r < GP / 2) prefetch_l1(P.cas_ml + (cbase + s) * GP * 2 + 4 * r);
+    }
+
     float m_run[GP], l_run[GP], acc[GP], alpha_prev[GP];
 #pragma unroll
     for (int g = 0; g < GP; ++g) {
@@ -463,8 +500,7 @@ __device__ void softmax_warps(const DecodeParams& P, Ctl& c, uint8_t* stages, ui
       if (!mbar_wait(&c.o_full[b], (cnt >> 1) & 1, abort_flag)) return false;
       tc_fence_after();
       uint32_t o[16];
-      tmem_ld16(tmem + lane_off + 32 + 16 * b, o);
-      tmem_ld_wait();
+      tmem_ld16_sync(tmem + lane_off + 32 + 16 * b, o);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&c.o_free[b]);
@@ -485,8 +521,7 @@ __device__ void softmax_warps(const DecodeParams& P, Ctl& c, uint8_t* stages, ui
       }
       tc_fence_after();
       uint32_t sraw[16];
-      tmem_ld16(tmem + lane_off + 16 * sb, sraw);
-      tmem_ld_wait();
+      tmem_ld16_sync(tmem + lane_off + 16 * sb, sraw);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&c.s_free[sb]);
@@ -591,6 +626,36 @@ __device__ void softmax_warps(const DecodeParams& P, Ctl& c, uint8_t* stages, ui
 #pragma unroll
       for (int g = 0; g < GP; ++g)
         if (g < G) orow[g * 128] = __float2bfloat16_rn(bad ? 0.f : acc[g] / lt[g]);
+    } else if (fold_prefix) {
+      // the prefix partials in split order, then this item: the split merge's order
+      float M[GP], num[GP], den[GP];
+#pragma unroll
+      for (int g = 0; g < GP; ++g) {
+        M[g] = -INFINITY;
+        num[g] = 0.f;
+        den[g] = 0.f;
+      }
+      for (int s = 0; s < npre; ++s) {
+        float ml[2 * GP], ov[GP];
+        const float* ml_p = P.cas_ml + (cbase + s) * GP * 2;
+#pragma unroll
+        for (int k = 0; k < 2 * GP; ++k) ml[k] = __ldg(ml_p + k);
+#pragma unroll
+        for (int g = 0; g < GP; ++g) ov[g] = __ldg(P.cas_o + ((cbase + s) * GP + g) * 128 + r);
+        merge_fold<GP>(M, num, den, ml, ov);
+      }
+      float ml[2 * GP];
+#pragma unroll
+      for (int g = 0; g < GP; ++g) {
+        ml[2 * g] = m_run[g];
+        ml[2 * g + 1] = lt[g];
+      }
+      merge_fold<GP>(M, num, den, ml, acc);
+      // a bad block id in the prefix was flagged by the cascade kernel
+      const bool any_bad = bad || __ldg(P.unit_bad + unit) != 0;
+#pragma unroll
+      for (int g = 0; g < GP; ++g)
+        if (g < G) orow[g * 128] = __float2bfloat16_rn(any_bad ? 0.f : num[g] / den[g]);
     } else {
       // partials: accumulators [item][d][GP] (one float4 run per thread), max and sum
       // [item][GP][2]; the merge kernel that runs after this one combines them
@@ -702,21 +767,6 @@ struct MergeParams {
   int32_t num_seqs, hkv, group, hq;
 };
 
-// Folds one partial (running max m, sum l, accumulator o, per head) into the merge.
-template <int GP>
-__device__ __forceinline__ void merge_fold(float (&M)[GP], float (&num)[GP], float (&den)[GP], const float (&ml)[2 * GP],
-                                           const float (&ov)[GP]) {
-#pragma unroll
-  for (int g = 0; g < GP; ++g) {
-    const float m_new = fmaxf(M[g], ml[2 * g]);
-    const float a = exp2f(M[g] - m_new);
-    const float b = exp2f(ml[2 * g] - m_new);
-    den[g] = fmaf(den[g], a, ml[2 * g + 1] * b);
-    num[g] = fmaf(num[g], a, ov[g] * b);
-    M[g] = m_new;
-  }
-}
-
 template <int GP>
 __global__ void __launch_bounds__(128) merge_kernel(const MergeParams P) {
   const int d = threadIdx.x;
@@ -727,7 +777,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeParams P) {
     const int base_i = __ldg(P.dec_prefix + i);
     const int ns = (__ldg(P.dec_prefix + i + 1) - base_i) / P.hkv;
     const int pre = P.seq_prefix ? __ldg(P.seq_prefix + i) : 0;
-    if (ns <= 1 && pre == 0) continue;
+    if (ns <= 1) continue;  // (a member of one split was finished by the decode kernel)
     const int64_t base = base_i + static_cast<int64_t>(h) * ns;
     float M[GP], num[GP], den[GP];
 #pragma unroll
@@ -784,7 +834,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeParams P) {
 
 template <int GP>
 int launch_gp(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& vm, const DecodeParams& p, int grid,
-              const Workspace& ws, cudaStream_t s) {
+              const Workspace& ws, bool may_split, cudaStream_t s) {
   const int32_t* counters = ws.counters;
   const int32_t* merge_list = ws.merge_list;
   cudaError_t e = cudaFuncSetAttribute(decode_kernel<GP>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -795,6 +845,7 @@ int launch_gp(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& v
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_status(e);
   }
+  if (!may_split) return PKV_OK;  // no context is long enough to be split: nothing to merge
   MergeParams m{p.out,          counters,  merge_list, p.dec_prefix,  p.qsl,     p.unit_bad,    p.part_o,
                 p.part_ml,      p.seq_prefix, ws.seq_entry, ws.cas_o, ws.cas_ml, ws.cas_np_max, p.num_seqs,
                 p.hkv,          p.group,   p.hq};
@@ -840,6 +891,10 @@ int launch_decode_tc(const AttnArgs& a, const Workspace& ws, int num_sms, uint32
   p.part_o = ws.part_o;
   p.part_ml = ws.part_ml;
   p.seq_prefix = ws.seq_prefix;
+  p.seq_entry = ws.seq_entry;
+  p.cas_o = ws.cas_o;
+  p.cas_ml = ws.cas_ml;
+  p.cas_np_max = ws.cas_np_max;
   p.err = err;
   p.num_blocks = a.cache.num_blocks;
   p.num_tokens = a.num_tokens;
@@ -851,9 +906,11 @@ int launch_decode_tc(const AttnArgs& a, const Workspace& ws, int num_sms, uint32
   p.hq = a.num_q_heads;
   p.split_keys = kSplitKeys;
   p.scale_log2 = a.scale * 1.4426950408889634f;
-  if (gp == 4) return launch_gp<4>(qm, km, vm, p, num_sms, ws, s);
-  if (gp == 8) return launch_gp<8>(qm, km, vm, p, num_sms, ws, s);
-  return launch_gp<16>(qm, km, vm, p, num_sms, ws, s);
+  // the planner never splits a request longer than the host bound, and none up to kNoSplitKeys
+  const bool may_split = a.max_seq_len > kNoSplitKeys;
+  if (gp == 4) return launch_gp<4>(qm, km, vm, p, num_sms, ws, may_split, s);
+  if (gp == 8) return launch_gp<8>(qm, km, vm, p, num_sms, ws, may_split, s);
+  return launch_gp<16>(qm, km, vm, p, num_sms, ws, may_split, s);
 }
 
 }  // namespace pkv

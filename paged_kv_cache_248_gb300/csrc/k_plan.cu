@@ -16,8 +16,8 @@
 // Shared-prefix groups (paged_attention_cascade) are checked here first.  A listed
 // request becomes a member of its group only if it is listed once, is a decode whose
 // context goes past the prefix, and its block table starts with the prefix's block
-// ids (one warp compares a member's row, 32 ids per load).  A member's decode items
-// then cover only the keys after the prefix, it always goes to the split merge, and
+// ids.  A member's decode items then cover only the keys after the prefix, it goes
+// to the split merge when those keys are cut into several splits, and
 // the cascade kernel gets ceil(members / rows) x kv heads x cascade_splits(P) items
 // per group.  Anything else listed is attended the ordinary way.
 #include "pkv_internal.cuh"
@@ -88,33 +88,55 @@ __device__ void plan_cascade(const PlanArgs& p) {
     }
   }
   __syncthreads();
-  const int warp = tid >> 5, lane = tid & 31, nwarps = nthr >> 5;
-  for (int k = warp; k < g.num_members; k += nwarps) {  // warp-uniform per entry
+  // the group of entry k: last gi with start[gi] <= k
+  auto group_of = [&](int k) {
+    int lo = 0, hi = g.num_groups - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (g.start[mid] <= k) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+  };
+  // per entry, the conditions on the request; member_ok[k] holds the prefix length in
+  // blocks while the tables are compared (0: rejected)
+  for (int k = tid; k < g.num_members; k += nthr) {
     const int i = g.members[k];
-    int ok = 0, P = 0;
+    int pb_ok = 0;
     if (csr_ok && i >= 0 && i < p.num_seqs && p.seq_entry[i] == k && p.seq_prefix[i] == 0) {
-      int lo = 0, hi = g.num_groups - 1;  // the group of entry k: last gi with start[gi] <= k
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (g.start[mid] <= k) lo = mid; else hi = mid - 1;
-      }
-      const int pb = g.blocks[lo];
+      const int pb = g.blocks[group_of(k)];
       const int64_t q0 = p.qsl[i], q1 = p.qsl[i + 1], L = p.seq_lens[i];
       if (pb >= 1 && pb <= g.max_blocks && q0 >= 0 && q1 == q0 + 1 && q1 <= p.num_tokens && L <= p.max_seq_len &&
-          (L + kBlock - 1) / kBlock <= p.max_blocks && L > static_cast<int64_t>(pb) * kBlock) {
-        const int32_t* own = p.bt + static_cast<int64_t>(i) * p.max_blocks;
-        const int32_t* pre = g.tables + static_cast<int64_t>(lo) * g.max_blocks;
-        int diff = 0;
-        for (int j = lane; j < pb; j += 32) diff |= __ldg(own + j) != __ldg(pre + j);
-        ok = !__any_sync(0xffffffffu, diff);
-        P = pb * kBlock;
-      }
+          (L + kBlock - 1) / kBlock <= p.max_blocks && L > static_cast<int64_t>(pb) * kBlock)
+        pb_ok = pb;
     }
-    if (lane == 0) {
-      p.member_ok[k] = ok;
-      if (ok) p.seq_prefix[i] = P;
-      else if (csr_ok && i >= 0 && i < p.num_seqs && p.seq_entry[i] == k && p.seq_prefix[i] == 0)
-        p.seq_entry[i] = -1;  // claimed but not a member
+    p.member_ok[k] = pb_ok;
+  }
+  __syncthreads();
+  // the member's table must start with the prefix's block ids: (entry, 16-id chunk)
+  // pairs spread over the block; a mismatch anywhere rejects the entry
+  constexpr int kChunk = 16;
+  const int chunks = (g.max_blocks + kChunk - 1) / kChunk;
+  const int64_t work = static_cast<int64_t>(g.num_members) * chunks;
+  for (int64_t wi = tid; wi < work; wi += nthr) {
+    const int k = static_cast<int>(wi / chunks), j0 = static_cast<int>(wi % chunks) * kChunk;
+    const int pb = *reinterpret_cast<volatile int32_t*>(p.member_ok + k);
+    if (j0 >= pb) continue;
+    const int32_t* own = p.bt + static_cast<int64_t>(g.members[k]) * p.max_blocks;
+    const int32_t* pre = g.tables + static_cast<int64_t>(group_of(k)) * g.max_blocks;
+    const int j1 = min(pb, j0 + kChunk);
+    int diff = 0;
+    for (int j = j0; j < j1; ++j) diff |= __ldg(own + j) != __ldg(pre + j);
+    if (diff) *reinterpret_cast<volatile int32_t*>(p.member_ok + k) = 0;
+  }
+  __syncthreads();
+  for (int k = tid; k < g.num_members; k += nthr) {
+    const int i = g.members[k];
+    const int pb = p.member_ok[k];
+    if (pb > 0) {
+      p.seq_prefix[i] = pb * kBlock;
+      p.member_ok[k] = 1;
+    } else if (csr_ok && i >= 0 && i < p.num_seqs && p.seq_entry[i] == k && p.seq_prefix[i] == 0) {
+      p.seq_entry[i] = -1;  // claimed but not a member
     }
   }
   __syncthreads();
@@ -145,7 +167,66 @@ __device__ void plan_cascade(const PlanArgs& p) {
   __syncthreads();
 }
 
+// The writer CTAs of a fused step: a warp per new token computes its slot (as
+// slot_mapping_kernel does) and copies the token's K and V rows for every kv head
+// into it (as write_kernel does), with the same error flags.  The attention kernels
+// launched after this one see the rows.
+__device__ void write_new_tokens(const PlanArgs& p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x - 1) * (blockDim.x >> 5);
+  const int64_t per_tok = static_cast<int64_t>(p.hkv) * p.vec_per_row;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x - 1) * (blockDim.x >> 5) + (threadIdx.x >> 5); t < p.num_tokens;
+       t += nwarps) {
+    int64_t slot = -1;
+    if (lane == 0) {
+      const int i = find_seq(p.qsl, p.num_seqs, t);
+      const int64_t q0 = __ldg(p.qsl + i), q1 = __ldg(p.qsl + i + 1);
+      const int64_t pos = static_cast<int64_t>(__ldg(p.seq_lens + i)) - (q1 - q0) + (t - q0);
+      if (t < q0 || t >= q1 || pos < 0 || pos / kBlock >= p.max_blocks) {
+        flag_error(p.err, kErrLength);
+      } else {
+        const int32_t b = __ldg(p.bt + static_cast<int64_t>(i) * p.max_blocks + pos / kBlock);
+        if (b < 0) flag_error(p.err, kErrBlockId);
+        else slot = static_cast<int64_t>(b) * kBlock + pos % kBlock;
+      }
+      if (p.slots_out) p.slots_out[t] = slot;
+      if (slot >= p.num_slots) {
+        flag_error(p.err, kErrSlot);
+        slot = -1;
+      }
+    }
+    slot = __shfl_sync(0xffffffffu, slot, 0);
+    if (slot < 0) continue;
+    const int64_t blk = slot / kBlock, off = slot % kBlock;
+    const uint4* ks = p.k_new + t * per_tok;
+    const uint4* vs = p.v_new + t * per_tok;
+    for (int64_t r0 = lane; r0 < per_tok; r0 += 64) {
+      const int64_t r1 = r0 + 32;
+      const uint4 ka = __ldcs(ks + r0), va = __ldcs(vs + r0);
+      uint4 kb = make_uint4(0, 0, 0, 0), vb = kb;
+      if (r1 < per_tok) {
+        kb = __ldcs(ks + r1);
+        vb = __ldcs(vs + r1);
+      }
+      const int64_t h0 = r0 / p.vec_per_row, c0 = r0 - h0 * p.vec_per_row;
+      const int64_t d0 = ((blk * p.hkv + h0) * kBlock + off) * p.vec_per_row + c0;
+      p.k_cache[d0] = ka;
+      p.v_cache[d0] = va;
+      if (r1 < per_tok) {
+        const int64_t h1 = r1 / p.vec_per_row, c1 = r1 - h1 * p.vec_per_row;
+        const int64_t d1 = ((blk * p.hkv + h1) * kBlock + off) * p.vec_per_row + c1;
+        p.k_cache[d1] = kb;
+        p.v_cache[d1] = vb;
+      }
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs p) {
+  if (blockIdx.x > 0) {  // writer CTAs never join the planner's block barriers
+    write_new_tokens(p);
+    return;
+  }
   const int64_t n_units = static_cast<int64_t>(p.num_seqs) * p.hkv;
   for (int64_t u = threadIdx.x; u < n_units; u += blockDim.x) {
     p.unit_bad[u] = 0;
@@ -170,7 +251,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs p) {
         const int P = cascade ? p.seq_prefix[i] : 0;  // keys the cascade kernel attends
         const int ns = ok ? static_cast<int>(decode_splits(L - P)) : 1;
         nd = p.hkv * ns;
-        nm = (ns > 1 || P > 0) ? 1 : 0;  // its partials need the split merge
+        nm = ns > 1 ? 1 : 0;  // its partials need the split merge (a member of one split
+                              // folds its prefix partials in the decode kernel)
       } else if (q_len > 1) {
         np = p.hkv * static_cast<int>((q_len + p.rows_per_tile - 1) / p.rows_per_tile);
       }
@@ -198,7 +280,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs p) {
 
 int launch_plan(const PlanArgs& p, cudaStream_t s) {
   TraceScope trace(kTracePlan, s);
-  plan_kernel<<<1, kPlanThreads, 0, s>>>(p);
+  const int writers = p.k_new ? p.write_ctas : 0;
+  plan_kernel<<<1 + writers, kPlanThreads, 0, s>>>(p);
   return cuda_status(cudaGetLastError());
 }
 

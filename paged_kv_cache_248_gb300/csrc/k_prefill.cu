@@ -444,24 +444,28 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uin
       tc_fence_after();
       float s[128];
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        uint32_t v[16];
-        tmem_ld16(tmem + lane_off + 128 * sb + 16 * ch, v);
-        tmem_ld_wait();
+      for (int h = 0; h < 2; ++h) {  // two 64-column loads, each waited for in its own statement
+        uint32_t v[64];
+        tmem_ld64_sync(tmem + lane_off + 128 * sb + 64 * h, v);
 #pragma unroll
-        for (int k = 0; k < 16; ++k) s[16 * ch + k] = __uint_as_float(v[k]);
+        for (int k = 0; k < 64; ++k) s[64 * h + k] = __uint_as_float(v[k]);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&c.s_free[sb]);
-      float tmax = -INFINITY;
-      // keys k0 .. k0 + nvis - 1 are visible to this row (cascade: the whole split)
+      // keys k0 .. k0 + nvis - 1 are visible to this row (cascade: the whole split);
+      // eight independent running maxima keep the dependency chains short
       const int nvis = kCas ? info.kend - k0 : pos - k0 + 1;
+      float mx[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
 #pragma unroll
       for (int k = 0; k < 128; ++k) {
         s[k] = k < nvis ? s[k] * P.scale_log2 : -INFINITY;
-        tmax = fmaxf(tmax, s[k]);
+        mx[k & 7] = fmaxf(mx[k & 7], s[k]);
       }
+      const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       if (j == 0) {
         m_ref = tmax;  // key 0 is visible to every row, so this is finite
       } else {
@@ -479,10 +483,9 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uin
           const float m_new = need ? tmax : m_ref;
           const float alpha = exp2f(m_ref - m_new);
 #pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
+          for (int ch = 0; ch < 8; ++ch) {  // rare: 16 columns at a time keeps registers low
             uint32_t v[16];
-            tmem_ld16(tmem + lane_off + kOCol + 16 * ch, v);
-            tmem_ld_wait();
+            tmem_ld16_sync(tmem + lane_off + kOCol + 16 * ch, v);
 #pragma unroll
             for (int k = 0; k < 16; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
             tmem_st16(tmem + lane_off + kOCol + 16 * ch, v);
@@ -510,20 +513,22 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uin
         break;
       }
       uint8_t* prow = pbuf + pb * kTileBytes + r * 128;
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};  // the tile's row sum in four independent parts
 #pragma unroll
       for (int kc = 0; kc < 16; ++kc) {
         uint32_t w[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const float a = exp2f(s[8 * kc + 2 * q] - m_ref);
-          const float b = exp2f(s[8 * kc + 2 * q + 1] - m_ref);
-          l_sum += a + b;
+          const float a = ex2_approx(s[8 * kc + 2 * q] - m_ref);
+          const float b = ex2_approx(s[8 * kc + 2 * q + 1] - m_ref);
+          ls[q] += a + b;
           __nv_bfloat162 h2 = __floats2bfloat162_rn(a, b);
           w[q] = *reinterpret_cast<uint32_t*>(&h2);
         }
         const int half = kc >> 3, c8 = kc & 7;
         *reinterpret_cast<uint4*>(prow + half * kHalfBytes + ((c8 ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
+      l_sum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
@@ -543,14 +548,13 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uin
       const int64_t cslot = (static_cast<int64_t>(entry) * P.hkv + info.head) * P.cas_np_max + info.split;
       float4* dst = reinterpret_cast<float4*>(P.cas_o + (cslot * P.gp + rg) * 128);
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        uint32_t v[16];
-        tmem_ld16(tmem + lane_off + kOCol + 16 * ch, v);
-        tmem_ld_wait();
+      for (int h = 0; h < 2; ++h) {
+        uint32_t v[64];
+        tmem_ld64_sync(tmem + lane_off + kOCol + 64 * h, v);
         if (cas_live) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            dst[4 * ch + q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+          for (int q = 0; q < 16; ++q)
+            dst[16 * h + q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
                                           __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
         }
       }
@@ -569,19 +573,21 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uin
     }
     const float inv = bad ? 0.f : 1.f / l_sum;
 #pragma unroll
-    for (int ch = 0; ch < 8; ++ch) {
-      uint32_t v[16];
-      tmem_ld16(tmem + lane_off + kOCol + 16 * ch, v);
-      tmem_ld_wait();
+    for (int h = 0; h < 2; ++h) {
+      uint32_t v[64];
+      tmem_ld64_sync(tmem + lane_off + kOCol + 64 * h, v);
       if (row_out) {
-        uint32_t w[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(v[2 * q]) * inv, __uint_as_float(v[2 * q + 1]) * inv);
-          w[q] = *reinterpret_cast<uint32_t*>(&h2);
+        for (int ch = 0; ch < 8; ++ch) {
+          uint32_t w[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(v[8 * ch + 2 * q]) * inv,
+                                                      __uint_as_float(v[8 * ch + 2 * q + 1]) * inv);
+            w[q] = *reinterpret_cast<uint32_t*>(&h2);
+          }
+          reinterpret_cast<uint4*>(orow)[8 * h + ch] = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        reinterpret_cast<uint4*>(orow)[2 * ch] = make_uint4(w[0], w[1], w[2], w[3]);
-        reinterpret_cast<uint4*>(orow)[2 * ch + 1] = make_uint4(w[4], w[5], w[6], w[7]);
       }
     }
     tc_fence_before();

@@ -61,8 +61,7 @@ __global__ void __launch_bounds__(128) umma_probe_kernel(UmmaProbe P, const uint
     const int row = (warp % 4) * 32 + threadIdx.x % 32;
     for (int c0 = 0; c0 < P.N; c0 += 16) {
       uint32_t r[16];
-      tmem_ld16(tmem + ((static_cast<uint32_t>(warp % 4) * 32u) << 16) + static_cast<uint32_t>(c0), r);
-      tmem_ld_wait();
+      tmem_ld16_sync(tmem + ((static_cast<uint32_t>(warp % 4) * 32u) << 16) + static_cast<uint32_t>(c0), r);
       if (row < P.M)
         for (int j = 0; j < 16; ++j) d[row * P.N + c0 + j] = __uint_as_float(r[j]);
     }

@@ -196,7 +196,17 @@ struct PlanArgs {
   int32_t* seq_entry = nullptr;
   int32_t* member_ok = nullptr;
   int32_t* cas_prefix = nullptr;
+  // new tokens written by the same launch (k_new null: none): slot mapping and K/V scatter
+  const uint4* k_new = nullptr;
+  const uint4* v_new = nullptr;
+  uint4* k_cache = nullptr;
+  uint4* v_cache = nullptr;
+  int64_t* slots_out = nullptr;  // optional
+  int64_t num_slots = 0;         // num_blocks * 16
+  int32_t vec_per_row = 0;       // 16-byte vectors per (token, kv head) row
+  int32_t write_ctas = 0;        // CTAs after the planning CTA that do the writes
 };
+// One launch: CTA 0 plans; CTAs 1..write_ctas (if any) map and scatter the new tokens.
 int launch_plan(const PlanArgs& p, cudaStream_t s);
 int launch_decode_tc(const AttnArgs& a, const Workspace& ws, int num_sms, uint32_t* err, cudaStream_t s);
 // Attends the member decodes of every prefix group to the group's shared prefix,

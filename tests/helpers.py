@@ -8,6 +8,8 @@ mapping and scatter; nothing it reads comes from the CUDA path.
 """
 from __future__ import annotations
 
+import dataclasses
+
 import numpy as np
 import torch
 
@@ -78,3 +80,29 @@ def compare(got: torch.Tensor, ref: np.ndarray, dtype: str, what: str = ""):
     assert err.max() <= max_tol, f"{what}: max-abs {err.max():.3e} > {max_tol}" + where()
     assert err.mean() <= mean_tol, f"{what}: mean-abs {err.mean():.3e} > {mean_tol}"
     return float(err.max()), float(err.mean())
+
+
+def sub_batch(w, t_gpu, seq_ids):
+    """Requests ``seq_ids`` of a large batch, with only their blocks, copied to the host
+    before the GPU step writes into the pool (block ids renumbered: the oracle's
+    result does not depend on physical ids)."""
+    seq_ids = np.asarray(seq_ids)
+    bt = w.block_tables[seq_ids]
+    used = np.unique(bt[bt >= 0])
+    remap = np.full(w.num_blocks, -1, np.int32)
+    remap[used] = np.arange(len(used), dtype=np.int32)
+    bt2 = np.where(bt >= 0, remap[np.maximum(bt, 0)], -1).astype(np.int32)
+    qsl = w.query_start_loc
+    rows = np.concatenate([np.arange(qsl[i], qsl[i + 1]) for i in seq_ids]).astype(np.int64)
+    q_lens = np.array([qsl[i + 1] - qsl[i] for i in seq_ids], np.int32)
+    idx = torch.from_numpy(used.astype(np.int64)).cuda()
+    ridx = torch.from_numpy(rows).cuda()
+    t_sub = {"k_cache": t_gpu["k_cache"].index_select(0, idx).cpu(),
+             "v_cache": t_gpu["v_cache"].index_select(0, idx).cpu(),
+             "q": t_gpu["q"].index_select(0, ridx).cpu(),
+             "k_new": t_gpu["k_new"].index_select(0, ridx).cpu(),
+             "v_new": t_gpu["v_new"].index_select(0, ridx).cpu()}
+    w2 = dataclasses.replace(w, num_blocks=len(used), seq_lens=w.seq_lens[seq_ids].copy(),
+                             query_start_loc=np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32),
+                             block_tables=bt2)
+    return w2, t_sub, rows

@@ -15,7 +15,7 @@ import torch
 
 import oracle
 import workloads as wl
-from helpers import bits, compare, gpu_step, oracle_step, to_gpu_meta
+from helpers import bits, compare, gpu_step, oracle_step, sub_batch, to_gpu_meta
 
 pytestmark = pytest.mark.gpu
 
@@ -108,36 +108,10 @@ def test_prefix_workload_full_with_cow(pkv):
     run_pair(pkv, wl.make("prefix"), cow=True)
 
 
-def _sub_batch(w, t_gpu, seq_ids):
-    """Requests ``seq_ids`` of a large batch, with only their blocks, copied to the host
-    before the GPU step writes into the pool (block ids renumbered: the oracle's
-    result does not depend on physical ids)."""
-    seq_ids = np.asarray(seq_ids)
-    bt = w.block_tables[seq_ids]
-    used = np.unique(bt[bt >= 0])
-    remap = np.full(w.num_blocks, -1, np.int32)
-    remap[used] = np.arange(len(used), dtype=np.int32)
-    bt2 = np.where(bt >= 0, remap[np.maximum(bt, 0)], -1).astype(np.int32)
-    qsl = w.query_start_loc
-    rows = np.concatenate([np.arange(qsl[i], qsl[i + 1]) for i in seq_ids]).astype(np.int64)
-    q_lens = np.array([qsl[i + 1] - qsl[i] for i in seq_ids], np.int32)
-    idx = torch.from_numpy(used.astype(np.int64)).cuda()
-    ridx = torch.from_numpy(rows).cuda()
-    t_sub = {"k_cache": t_gpu["k_cache"].index_select(0, idx).cpu(),
-             "v_cache": t_gpu["v_cache"].index_select(0, idx).cpu(),
-             "q": t_gpu["q"].index_select(0, ridx).cpu(),
-             "k_new": t_gpu["k_new"].index_select(0, ridx).cpu(),
-             "v_new": t_gpu["v_new"].index_select(0, ridx).cpu()}
-    w2 = dataclasses.replace(w, num_blocks=len(used), seq_lens=w.seq_lens[seq_ids].copy(),
-                             query_start_loc=np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32),
-                             block_tables=bt2)
-    return w2, t_sub, rows
-
-
 def _sampled(pkv, name, seq_ids, row_pick=None):
     w = wl.make(name)
     t = w.make_tensors("cuda")
-    w2, t_sub, rows = _sub_batch(w, t, seq_ids)
+    w2, t_sub, rows = sub_batch(w, t, seq_ids)
     out, slots, st = gpu_step(pkv, w, t)
     assert st == 0, pkv.status_string(st)
     sub_rows = np.arange(len(rows)) if row_pick is None else row_pick(w2)

@@ -1,0 +1,142 @@
+"""paged_attention_step: slot mapping, K/V scatter and attention in one call must
+give exactly what pkv_slot_mapping + pkv_write + paged_attention(_cascade) give --
+the same caches, slots and outputs, bit for bit -- and match the oracle.
+
+The step appends every running request's new tokens to its blocks and attends
+over them ("vLLM's PagedAttention" teardown, section "Continuous batching").
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+from helpers import compare, oracle_step, sub_batch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    import paged_kv_cache_248_gb300 as m
+    m.lib()
+    assert m.pkv_get_last_error() == 0
+    return m
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def both_ways(pkv, w, t, groups=None):
+    """(separate: out, slots, k, v, status), (fused: ...) on two copies of the caches."""
+    bt, sl, qsl = dev(w.block_tables), dev(w.seq_lens), dev(w.query_start_loc)
+    mq, ms = max(1, w.max_query_len), max(1, w.max_seq_len)
+    res = []
+    for fused in (False, True):
+        kc, vc = t["k_cache"].clone(), t["v_cache"].clone()
+        slots = torch.full((w.num_tokens,), -7, dtype=torch.int64, device="cuda")
+        if fused:
+            out = pkv.paged_attention_step(t["q"], t["k_new"], t["v_new"], kc, vc, bt, sl, qsl, w.scale, mq, ms,
+                                           prefix_groups=groups, slot_mapping=slots)
+        else:
+            pkv.pkv_slot_mapping(bt, sl, qsl, w.num_tokens, out=slots)
+            pkv.pkv_write(t["k_new"], t["v_new"], slots, kc, vc)
+            if groups is None:
+                out = pkv.paged_attention(t["q"], kc, vc, bt, sl, qsl, w.scale, mq, ms)
+            else:
+                out = pkv.paged_attention_cascade(t["q"], kc, vc, bt, sl, qsl, w.scale, mq, ms, *groups)
+        res.append((out, slots, kc, vc, pkv.pkv_get_last_error()))
+    return res
+
+
+def assert_same(a, b):
+    for x, y, name in zip(a, b, ("out", "slots", "k_cache", "v_cache", "status")):
+        if isinstance(x, torch.Tensor):
+            assert torch.equal(x, y), name
+        else:
+            assert x == y, name
+
+
+@pytest.mark.parametrize("seed,group,hkv,dtype", [(21, 4, 2, "bf16"), (22, 8, 2, "bf16"), (23, 16, 1, "bf16"),
+                                                  (24, 6, 2, "bf16"), (25, 2, 2, "f32")])
+def test_step_equals_the_separate_calls_and_the_oracle(pkv, seed, group, hkv, dtype):
+    d = 128 if dtype == "bf16" else 64
+    w = wl.random_case(seed, num_seqs=14, max_ctx=1400, max_q=260, group=group, num_kv_heads=hkv, head_dim=d,
+                       dtype=dtype)
+    t_cpu = w.make_tensors("cpu")
+    t = {k: v.cuda() for k, v in t_cpu.items()}
+    sep, fus = both_ways(pkv, w, t)
+    assert sep[4] == 0
+    assert_same(sep, fus)
+    ref, ref_slots, ref_k, ref_v = oracle_step(w, t_cpu)
+    assert np.array_equal(fus[1].cpu().numpy(), ref_slots)
+    compare(fus[0], ref, dtype, w.name)
+
+
+def test_step_with_prefix_groups(pkv):
+    w, hints = wl.shared_prefix_case(26, prefix_blocks=(24, 40), members=(20, 9), bystanders=6)
+    t_cpu = w.make_tensors("cpu")
+    t = {k: v.cuda() for k, v in t_cpu.items()}
+    groups = tuple(dev(hints[k]) for k in ("prefix_block_tables", "prefix_num_blocks", "member_start",
+                                            "member_seqs"))
+    sep, fus = both_ways(pkv, w, t, groups)
+    assert sep[4] == 0
+    assert_same(sep, fus)
+    ref, _, _, _ = oracle_step(w, t_cpu)
+    compare(fus[0], ref, "bf16", w.name)
+
+
+def test_step_errors_match_the_separate_calls(pkv):
+    # a new token whose block id is past the pool: the write is skipped and flagged,
+    # attention zeroes the request's rows -- the same on both paths
+    w = wl.random_case(27, num_seqs=6, max_ctx=300, max_q=40, group=4, num_kv_heads=2, head_dim=128, dtype="bf16")
+    i = int(np.argmax(w.q_lens))
+    last = (int(w.seq_lens[i]) - 1) // 16
+    w.block_tables[i, last] = w.num_blocks + 3
+    t = {k: v.cuda() for k, v in w.make_tensors("cpu").items()}
+    sep, fus = both_ways(pkv, w, t)
+    assert sep[4] == pkv.PKV_ERR_INDEX
+    assert_same(sep, fus)
+
+
+def test_mixed_workload_full_size(pkv):
+    """The 8192-token mixed step (21 GB pool, two copies): fused and separate agree bit
+    for bit; two chunks and 64 decodes, with only their blocks, match the oracle."""
+    w = wl.make("mixed")
+    t = w.make_tensors("cuda")
+    seq_ids = np.concatenate([[1, 6], 8 + np.random.default_rng(5).choice(4096, size=64, replace=False)])
+    w2, t_sub, rows = sub_batch(w, t, seq_ids)  # host copies taken before the step writes
+    sep, fus = both_ways(pkv, w, t)
+    assert sep[4] == 0
+    assert_same(sep, fus)
+    del sep, t
+    ref, _, _, _ = oracle_step(w2, t_sub)
+    compare(fus[0][torch.from_numpy(rows).cuda()], ref, "bf16", "mixed sub-batch")
+
+
+def test_step_replays_from_a_cuda_graph(pkv):
+    w = wl.random_case(28, num_seqs=20, max_ctx=2500, max_q=300, group=4, num_kv_heads=8, head_dim=128,
+                       dtype="bf16")
+    t = {k: v.cuda() for k, v in w.make_tensors("cpu").items()}
+    bt, sl, qsl = dev(w.block_tables), dev(w.seq_lens), dev(w.query_start_loc)
+    kc0, vc0 = t["k_cache"].clone(), t["v_cache"].clone()
+    out_e, out_g = torch.empty_like(t["q"]), torch.full_like(t["q"], float("nan"))
+
+    def call(out):
+        pkv.paged_attention_step(t["q"], t["k_new"], t["v_new"], t["k_cache"], t["v_cache"], bt, sl, qsl, w.scale,
+                                 w.max_query_len, w.max_seq_len, out=out)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        call(out_e)
+    s.synchronize()
+    k_after, v_after = t["k_cache"].clone(), t["v_cache"].clone()
+    t["k_cache"].copy_(kc0)
+    t["v_cache"].copy_(vc0)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call(out_g)
+    g.replay()
+    torch.cuda.synchronize()
+    assert pkv.pkv_get_last_error() == 0
+    assert torch.equal(out_g, out_e)
+    assert torch.equal(t["k_cache"], k_after) and torch.equal(t["v_cache"], v_after)
