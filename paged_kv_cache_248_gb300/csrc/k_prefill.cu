@@ -15,8 +15,10 @@
 //
 // Per CTA (192 threads):
 //   warp 0     producer: TMA-loads the Q tile (a 3-D box over [token][head][dim])
-//              and, per 128-key tile, 4 boxes per 16-token block from the block's
-//              physical location (the block-table gather), 128-byte swizzle.
+//              and, per 128-key tile, 2 K and 2 V boxes per 16-token block from the
+//              block's physical location (the block-table gather), 128-byte swizzle.
+//              K and V have separate stage barriers and K runs one tile ahead of V:
+//              a K tile is released by its S MMA, a V tile by its P V.
 //   warp 1     MMA issuer: S = Q K^T (M = 128 rows, N = 128 keys) into one of two
 //              TMEM buffers, then O += P V into a TMEM accumulator, V read MN-major.
 //   warps 2-5  softmax: thread r owns row r.  It loads its S row from TMEM, applies
@@ -62,7 +64,10 @@ struct alignas(16) PItem {
 };
 
 struct Ctl {
-  uint64_t full[kStages], empty[kStages];
+  // K and V of a stage have their own barriers: a K tile is released when its S MMA
+  // completes and a V tile when its P V completes, so the next K load starts about one
+  // softmax iteration before the stage's P V is done
+  uint64_t kfull[kStages], kempty[kStages], vfull[kStages], vempty[kStages];
   uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
   uint64_t o_full, o_free;
   uint64_t q_full, q_free;
@@ -187,7 +192,7 @@ __device__ void producer_warp(const PrefillParams& P, const CUtensorMap* qmap, c
   const int lane = threadIdx.x & 31;
   const int total = kCas ? P.cas_prefix[P.cas_groups] : P.pre_prefix[P.num_seqs];
   volatile int* abort_flag = &c.abort_flag;
-  uint32_t it = 0, tc = 0, qc = 0;
+  uint32_t it = 0, tk = 0, tv = 0, qc = 0;  // items; K and V tiles issued; query tiles
   bool ok = true;
   while (ok) {
     const int slot = it % kRing;
@@ -221,9 +226,25 @@ __device__ void producer_warp(const PrefillParams& P, const CUtensorMap* qmap, c
     }
     const int32_t* btrow = kCas ? P.cas_tables + static_cast<int64_t>(info.seq) * P.cas_max_blocks
                                 : P.bt + static_cast<int64_t>(info.seq) * P.max_blocks;
+    // V of tile j - 1 into its stage once that stage's previous P V is done
+    auto load_v = [&](int id, int nblk) -> bool {
+      const int st = tv % kStages;
+      if (!mbar_wait(&c.vempty[st], ((tv / kStages) & 1) ^ 1, abort_flag)) return false;
+      if (lane == 0) mbar_arrive_expect_tx(&c.vfull[st], static_cast<uint32_t>(nblk) * 4096u);
+      __syncwarp();
+      if (lane < nblk) {
+        uint8_t* s = stages + st * kStageBytes + kTileBytes + lane * 2048;
+        const int32_t row = (id * P.hkv + info.head) * kBlock;
+        tma_load_2d(s, vmap, &c.vfull[st], 0, row);
+        tma_load_2d(s + kHalfBytes, vmap, &c.vfull[st], 64, row);
+      }
+      ++tv;
+      return true;
+    };
+    int prev_id = 0, prev_nblk = 0;
     for (int j = 0; j < info.nt; ++j) {
-      const int st = tc % kStages;
-      if (!mbar_wait(&c.empty[st], ((tc / kStages) & 1) ^ 1, abort_flag)) {
+      const int st = tk % kStages;
+      if (!mbar_wait(&c.kempty[st], ((tk / kStages) & 1) ^ 1, abort_flag)) {
         ok = false;
         break;
       }
@@ -243,23 +264,31 @@ __device__ void producer_warp(const PrefillParams& P, const CUtensorMap* qmap, c
         if (lane == 0) c.bad[slot] = 1;
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive_expect_tx(&c.full[st], static_cast<uint32_t>(nblk) * 8192u);
+      if (lane == 0) mbar_arrive_expect_tx(&c.kfull[st], static_cast<uint32_t>(nblk) * 4096u);
       __syncwarp();
       if (lane < nblk) {
         uint8_t* s = stages + st * kStageBytes + lane * 2048;
         const int32_t row = (id * P.hkv + info.head) * kBlock;
-        tma_load_2d(s, kmap, &c.full[st], 0, row);
-        tma_load_2d(s + kHalfBytes, kmap, &c.full[st], 64, row);
-        tma_load_2d(s + kTileBytes, vmap, &c.full[st], 0, row);
-        tma_load_2d(s + kTileBytes + kHalfBytes, vmap, &c.full[st], 64, row);
+        tma_load_2d(s, kmap, &c.kfull[st], 0, row);
+        tma_load_2d(s + kHalfBytes, kmap, &c.kfull[st], 64, row);
       }
-      ++tc;
+      ++tk;
+      if (j > 0 && !load_v(prev_id, prev_nblk)) {  // K runs one tile ahead of V
+        ok = false;
+        break;
+      }
+      prev_id = id;
+      prev_nblk = nblk;
     }
+    if (ok && info.nt > 0 && !load_v(prev_id, prev_nblk)) ok = false;
   }
   if (!ok && !*abort_flag && lane == 0) raise_abort(c, P.err);
   if (*abort_flag) {
-    const uint32_t first = tc > static_cast<uint32_t>(kStages) ? tc - kStages : 0;
-    for (uint32_t cnt = first; cnt < tc; ++cnt) mbar_wait(&c.full[cnt % kStages], (cnt / kStages) & 1, nullptr);
+    // let copies already issued land before the CTA's shared memory goes away
+    for (uint32_t cnt = tk > static_cast<uint32_t>(kStages) ? tk - kStages : 0; cnt < tk; ++cnt)
+      mbar_wait(&c.kfull[cnt % kStages], (cnt / kStages) & 1, nullptr);
+    for (uint32_t cnt = tv > static_cast<uint32_t>(kStages) ? tv - kStages : 0; cnt < tv; ++cnt)
+      mbar_wait(&c.vfull[cnt % kStages], (cnt / kStages) & 1, nullptr);
     if (qc > 0) mbar_wait(&c.q_full, (qc - 1) & 1, nullptr);
   }
 }
@@ -278,6 +307,7 @@ __device__ void mma_warp(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uint8_t*
   auto pv = [&](uint32_t cnt, bool first) -> bool {
     const int st = cnt % kStages, b = cnt & 1;
     if (!mbar_wait(&c.p_full[b], (cnt >> 1) & 1, abort_flag)) return false;
+    if (!mbar_wait(&c.vfull[st], (cnt / kStages) & 1, abort_flag)) return false;
     // the previous item's O must have been read out before its accumulator restarts
     if (first && !mbar_wait(&c.o_free, (ic & 1) ^ 1, abort_flag)) return false;
     tc_fence_after();
@@ -291,7 +321,7 @@ __device__ void mma_warp(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uint8_t*
                     umma_desc_advance(bd, kk * 2048), idesc_o, (!first || kk > 0) ? 1u : 0u);
       umma_commit(&c.o_full);
       umma_commit(&c.p_free[b]);
-      umma_commit(&c.empty[st]);
+      umma_commit(&c.vempty[st]);
     }
     __syncwarp();
     return true;
@@ -313,7 +343,7 @@ __device__ void mma_warp(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uint8_t*
       }
       for (int j = 0; j < info.nt && ok; ++j) {
         const int st = tc % kStages, sb = tc & 1;
-        if (!mbar_wait(&c.full[st], (tc / kStages) & 1, abort_flag) ||
+        if (!mbar_wait(&c.kfull[st], (tc / kStages) & 1, abort_flag) ||
             !mbar_wait(&c.s_free[sb], ((tc >> 1) & 1) ^ 1, abort_flag)) {
           ok = false;
           break;
@@ -328,6 +358,7 @@ __device__ void mma_warp(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uint8_t*
             umma_f16_ss(tmem + 128 * sb, umma_desc_advance(a, off), umma_desc_advance(b, off), idesc_s, kk > 0);
           }
           umma_commit(&c.s_full[sb]);
+          umma_commit(&c.kempty[st]);
           if (j == info.nt - 1) umma_commit(&c.q_free);
           issued = true;
         }
@@ -495,8 +526,8 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uin
           m_ref = m_new;
         }
       }
-      // K/V of this stage have landed (also orders the producer's bad-block flag)
-      if (!mbar_wait(&c.full[st], (tc / kStages) & 1, abort_flag)) {
+      // V of this stage has landed (also orders the producer's bad-block flag)
+      if (!mbar_wait(&c.vfull[st], (tc / kStages) & 1, abort_flag)) {
         ok = false;
         break;
       }
@@ -615,8 +646,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&c.full[s], 1);
-      mbar_init(&c.empty[s], 1);
+      mbar_init(&c.kfull[s], 1);
+      mbar_init(&c.kempty[s], 1);
+      mbar_init(&c.vfull[s], 1);
+      mbar_init(&c.vempty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&c.s_full[b], 1);

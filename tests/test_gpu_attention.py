@@ -100,6 +100,33 @@ def test_request_without_query_tokens(pkv):
     run_pair(pkv, w)
 
 
+@pytest.mark.parametrize("group,hkv", [(4, 8), (8, 4), (16, 2)])
+def test_many_short_decodes_with_invalid_items(pkv, group, hkv):
+    """3000 decodes of 1..400 keys: every CTA takes ~20 items, so the item ring wraps
+    many times and consecutive items alternate between softmax groups; every 97th
+    request has seq_len 0 (an invalid item: flagged, its rows zeroed) so that
+    invalid items fall on both groups.  Valid rows match the oracle."""
+    rng = np.random.default_rng(31)
+    n = 3000
+    L = rng.integers(1, 400, size=n, endpoint=True).astype(np.int32)
+    w = wl.sized_case(32, L, np.ones(n, np.int32), group * hkv, hkv, 128, "bf16")
+    bad = np.arange(5, n, 97)
+    L_run = L.copy()
+    L_run[bad] = 0
+    t_cpu = w.make_tensors("cpu")
+    t = {k: v.cuda() for k, v in t_cpu.items()}
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    out = pkv.paged_attention(t["q"], t["k_cache"], t["v_cache"], dev(w.block_tables), dev(L_run),
+                              dev(w.query_start_loc), w.scale, 1, int(L.max()))
+    assert pkv.pkv_get_last_error() == pkv.PKV_ERR_INDEX
+    good = np.setdiff1d(np.arange(n), bad)
+    ref = oracle.attention(bits(t_cpu["q"]), bits(t_cpu["k_cache"]), bits(t_cpu["v_cache"]), w.block_tables, L,
+                           w.query_start_loc, w.scale, rows=good)
+    compare(out[torch.from_numpy(good).cuda()], ref, "bf16", "valid rows")
+    zero = out[torch.from_numpy(bad).cuda()].float()
+    assert torch.equal(zero, torch.zeros_like(zero))
+
+
 def test_decode_workload_full(pkv):
     run_pair(pkv, wl.make("decode"))
 
