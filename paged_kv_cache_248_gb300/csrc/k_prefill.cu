@@ -484,19 +484,35 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uin
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&c.s_free[sb]);
-      // keys k0 .. k0 + nvis - 1 are visible to this row (cascade: the whole split);
-      // eight independent running maxima keep the dependency chains short
+      // keys k0 .. k0 + nvis - 1 are visible to this row (cascade: the whole split).
+      // The scores stay unscaled: the tile maximum of scale * s is scale times the
+      // maximum of s (the minimum, for a negative scale), and each exponent takes
+      // scale * s - m in one fused multiply-add.  Masked keys get the raw value that
+      // scales to -inf.  Tiles every row of the warp sees whole skip the masking.
+      const float scale = P.scale_log2;
+      const bool pos_scale = scale >= 0.f;
       const int nvis = kCas ? info.kend - k0 : pos - k0 + 1;
-      float mx[8];
+      if (!__all_sync(0xffffffffu, nvis >= kTileKeys)) {
+        const float hidden = pos_scale ? -INFINITY : INFINITY;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
-#pragma unroll
-      for (int k = 0; k < 128; ++k) {
-        s[k] = k < nvis ? s[k] * P.scale_log2 : -INFINITY;
-        mx[k & 7] = fmaxf(mx[k & 7], s[k]);
+        for (int k = 0; k < 128; ++k) s[k] = k < nvis ? s[k] : hidden;
       }
-      const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      float mx[8];  // eight independent running extrema keep the dependency chains short
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx[k] = s[k];
+      if (pos_scale) {
+#pragma unroll
+        for (int k = 8; k < 128; ++k) mx[k & 7] = fmaxf(mx[k & 7], s[k]);
+      } else {
+#pragma unroll
+        for (int k = 8; k < 128; ++k) mx[k & 7] = fminf(mx[k & 7], s[k]);
+      }
+      const float raw = pos_scale ? fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                          fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])))
+                                  : fminf(fminf(fminf(mx[0], mx[1]), fminf(mx[2], mx[3])),
+                                          fminf(fminf(mx[4], mx[5]), fminf(mx[6], mx[7])));
+      // (a fully masked row gives -inf either way: -inf * scale or +inf * a negative scale)
+      const float tmax = raw * scale;
       if (j == 0) {
         m_ref = tmax;  // key 0 is visible to every row, so this is finite
       } else {
@@ -550,8 +566,8 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uin
         uint32_t w[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const float a = ex2_approx(s[8 * kc + 2 * q] - m_ref);
-          const float b = ex2_approx(s[8 * kc + 2 * q + 1] - m_ref);
+          const float a = ex2_approx(fmaf(s[8 * kc + 2 * q], scale, -m_ref));
+          const float b = ex2_approx(fmaf(s[8 * kc + 2 * q + 1], scale, -m_ref));
           ls[q] += a + b;
           __nv_bfloat162 h2 = __floats2bfloat162_rn(a, b);
           w[q] = *reinterpret_cast<uint32_t*>(&h2);

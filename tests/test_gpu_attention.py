@@ -74,6 +74,15 @@ def test_prefill_edge_lengths_bf16(pkv, lens, qs):
     run_pair(pkv, w)
 
 
+@pytest.mark.parametrize("scale", [-0.0884, -0.5])
+def test_negative_scale_bf16(pkv, scale):
+    # a negative scale flips which key is each row's largest logit; the kernels take the
+    # tile minimum of the raw scores then (the API accepts any finite scale)
+    w = dataclasses.replace(wl.random_case(41, num_seqs=10, max_ctx=900, max_q=300, group=4, num_kv_heads=2,
+                                           head_dim=128, dtype="bf16"), scale=scale)
+    run_pair(pkv, w)
+
+
 @pytest.mark.parametrize("scale", [0.3, 1.0])
 def test_prefill_rescale_path_bf16(pkv, scale):
     # a large logit scale makes row maxima jump between key tiles, so the prefill
