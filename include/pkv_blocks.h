@@ -95,6 +95,20 @@ PKV_BM_API int32_t pkv_bm_cow(pkv_block_manager* bm, int64_t req, int32_t logica
 PKV_BM_API int32_t pkv_bm_usage(const pkv_block_manager* bm, int64_t* blocks_in_use, int64_t* tokens_held,
                                 int64_t* unused_slots);
 
+/* Shared-prefix groups of a batch, for paged_attention_cascade: requests reqs[0..n) (the batch
+ * order) whose block tables start with the same physical block form a group, and the group's prefix
+ * is the longest run of leading blocks that all its members share (at most max_prefix_blocks).
+ * Groups of a single request, or whose members share no block, are left out.  Writes group g's
+ * prefix block ids to prefix_tables[g * max_prefix_blocks ...], its length in blocks to
+ * prefix_num_blocks[g], and its members' batch indices to member_seqs[member_start[g] ..
+ * member_start[g + 1]) (member_start holds max_groups + 1 entries, member_seqs n).  The kernel
+ * admits only decodes whose context goes past the prefix; the rest of a group is attended the
+ * ordinary way.  Returns the number of groups (at most max_groups; further groups are dropped),
+ * -2 if a request is unknown, -3 on bad arguments. */
+PKV_BM_API int32_t pkv_bm_prefix_groups(const pkv_block_manager* bm, const int64_t* reqs, int32_t n,
+                                        int32_t max_prefix_blocks, int32_t max_groups, int32_t* prefix_tables,
+                                        int32_t* prefix_num_blocks, int32_t* member_start, int32_t* member_seqs);
+
 /* The chained hash of one full block: 64-bit hash of (parent_hash, 16 token ids,
  * extra_key).  Exposed for tests.  The first block of a request chains from 0. */
 PKV_BM_API uint64_t pkv_bm_block_hash(uint64_t parent_hash, const int32_t* tokens16, uint64_t extra_key);

@@ -318,6 +318,7 @@ class BlockManager:
             L.pkv_bm_fork.argtypes = [P, i64, i64]
             L.pkv_bm_cow.argtypes = [P, i64, i32, I32P, I32P]
             L.pkv_bm_usage.argtypes = [P, I64P, I64P, I64P]
+            L.pkv_bm_prefix_groups.argtypes = [P, I64P, i32, i32, i32, I32P, I32P, I32P, I32P]
             L.pkv_bm_block_hash.argtypes, L.pkv_bm_block_hash.restype = [ctypes.c_uint64, I32P, ctypes.c_uint64], \
                 ctypes.c_uint64
             for f in ("pkv_bm_get_computed_blocks", "pkv_bm_allocate_slots", "pkv_bm_cache_full_blocks",
@@ -385,6 +386,25 @@ class BlockManager:
         b, t, u = ctypes.c_int64(0), ctypes.c_int64(0), ctypes.c_int64(0)
         self._L.pkv_bm_usage(self._h, ctypes.byref(b), ctypes.byref(t), ctypes.byref(u))
         return {"blocks_in_use": b.value, "tokens_held": t.value, "unused_slots": u.value}
+
+    def prefix_groups(self, reqs, max_prefix_blocks: int, max_groups: int | None = None):
+        """Shared-prefix groups of the batch ``reqs`` (request ids in batch order), as
+        (prefix_block_tables [G, max_prefix_blocks], prefix_num_blocks [G], member_start
+        [G + 1], member_seqs) int32 numpy arrays for paged_attention_cascade / _step."""
+        import numpy as np
+        r = np.ascontiguousarray(np.asarray(reqs, dtype=np.int64).reshape(-1))
+        n = int(r.size)
+        mg = max(1, n // 2) if max_groups is None else int(max_groups)
+        tables = np.empty((mg, int(max_prefix_blocks)), np.int32)
+        nblk = np.empty(mg, np.int32)
+        start = np.zeros(mg + 1, np.int32)
+        members = np.empty(max(n, 1), np.int32)
+        P32 = ctypes.POINTER(ctypes.c_int32)
+        g = self._ok(self._L.pkv_bm_prefix_groups(
+            self._h, r.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), n, int(max_prefix_blocks), mg,
+            tables.ctypes.data_as(P32), nblk.ctypes.data_as(P32), start.ctypes.data_as(P32),
+            members.ctypes.data_as(P32)), "prefix_groups")
+        return tables[:g].copy(), nblk[:g].copy(), start[:g + 1].copy(), members[:start[g]].copy()
 
     def block_hash(self, parent: int, tokens16, extra: int = 0) -> int:
         a, p = self._i32(tokens16)

@@ -7,6 +7,7 @@
 // stays in the map while it waits in the free queue; it is evicted (its hash dropped)
 // only when allocation takes it from the head.  Hits compare token ids, so a hash
 // collision can never hand out the wrong block.
+#include <algorithm>
 #include <cstring>
 #include <unordered_map>
 #include <vector>
@@ -215,6 +216,48 @@ int32_t pkv_bm_cow(pkv_block_manager* bm, int64_t req, int32_t logical_block, in
   *src = old;
   *dst = fresh;
   return 1;
+}
+
+int32_t pkv_bm_prefix_groups(const pkv_block_manager* bm, const int64_t* reqs, int32_t n, int32_t max_prefix_blocks,
+                             int32_t max_groups, int32_t* prefix_tables, int32_t* prefix_num_blocks,
+                             int32_t* member_start, int32_t* member_seqs) {
+  if (!bm || n < 0 || (n > 0 && !reqs) || max_prefix_blocks < 1 || max_groups < 0 || !member_start) return -3;
+  if (max_groups > 0 && (!prefix_tables || !prefix_num_blocks || (n > 0 && !member_seqs))) return -3;
+  std::vector<const std::vector<int32_t>*> tab(static_cast<size_t>(n));
+  for (int32_t k = 0; k < n; ++k) {
+    auto it = bm->reqs.find(reqs[k]);
+    if (it == bm->reqs.end()) return -2;
+    tab[k] = &it->second.blocks;
+  }
+  // requests by first block, in batch order of each group's first member
+  std::unordered_map<int32_t, int32_t> group_of;
+  std::vector<std::vector<int32_t>> groups;
+  for (int32_t k = 0; k < n; ++k) {
+    if (tab[k]->empty()) continue;
+    auto ins = group_of.emplace((*tab[k])[0], static_cast<int32_t>(groups.size()));
+    if (ins.second) groups.emplace_back();
+    groups[ins.first->second].push_back(k);
+  }
+  int32_t ng = 0, nm = 0;
+  member_start[0] = 0;
+  for (const auto& members : groups) {
+    if (members.size() < 2 || ng == max_groups) continue;
+    const std::vector<int32_t>& lead = *tab[members[0]];
+    size_t lcp = std::min(lead.size(), static_cast<size_t>(max_prefix_blocks));
+    for (size_t m = 1; m < members.size(); ++m) {
+      const std::vector<int32_t>& t = *tab[members[m]];
+      size_t j = 0;
+      while (j < lcp && j < t.size() && t[j] == lead[j]) ++j;
+      lcp = j;
+    }
+    if (lcp == 0) continue;
+    for (size_t j = 0; j < static_cast<size_t>(max_prefix_blocks); ++j)
+      prefix_tables[static_cast<size_t>(ng) * max_prefix_blocks + j] = j < lcp ? lead[j] : -1;
+    prefix_num_blocks[ng] = static_cast<int32_t>(lcp);
+    for (int32_t k : members) member_seqs[nm++] = k;
+    member_start[++ng] = nm;
+  }
+  return ng;
 }
 
 int32_t pkv_bm_usage(const pkv_block_manager* bm, int64_t* blocks_in_use, int64_t* tokens_held,

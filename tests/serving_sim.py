@@ -50,6 +50,7 @@ class Step:
     k_new: torch.Tensor                                   # bf16 [T, hkv, d]
     v_new: torch.Tensor
     live: dict = field(default_factory=dict)              # rid -> (block table, tokens in the pool)
+    rids: list = field(default_factory=list)              # request ids in batch order
 
     @property
     def num_tokens(self):
@@ -125,7 +126,8 @@ def run(bm, hkv, d, steps=14, budget=160, seed=7, events=None):
         for (r, n), L in zip(batch, seq_lens):
             live[r.rid] = (bm.block_table(r.rid), r.tokens[:int(L)])
         yield Step(step, np.asarray([c[0] for c in cows], np.int32), np.asarray([c[1] for c in cows], np.int32),
-                   bt, seq_lens, np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32), k_new, v_new, live)
+                   bt, seq_lens, np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32), k_new, v_new, live,
+                   [r.rid for r, _ in batch])
         # chunks complete; a request whose tokens are all in the pool emits the next one
         for r, n in batch:
             r.done += n

@@ -173,3 +173,56 @@ def test_errors(pkv):
         bm.get_computed_blocks(1, [])                       # already exists
     with pytest.raises(ValueError):
         pkv.BlockManager(0)
+
+
+def test_prefix_groups_from_shared_blocks(pkv):
+    bm = pkv.BlockManager(64)
+    system = toks(20, 3 * BLOCK)
+    a = np.concatenate([system, toks(21, 10)])
+    bm.get_computed_blocks(1, a)
+    bm.allocate_slots(1, a.size)
+    bm.cache_full_blocks(1, a)
+    b = np.concatenate([system, toks(22, 30)])
+    assert bm.get_computed_blocks(2, b) == 3
+    bm.allocate_slots(2, b.size)
+    bm.get_computed_blocks(3, toks(23, 40))       # an unrelated request
+    bm.allocate_slots(3, 40)
+    tables, nblk, start, members = bm.prefix_groups([3, 1, 2], max_prefix_blocks=8)
+    assert nblk.tolist() == [3] and start.tolist() == [0, 2]
+    assert members.tolist() == [1, 2]                 # batch indices of requests 1 and 2
+    assert tables[0, :3].tolist() == bm.block_table(1)[:3]
+    assert (tables[0, 3:] == -1).all()
+
+
+def test_prefix_groups_take_the_shortest_common_run(pkv):
+    bm = pkv.BlockManager(64)
+    p = toks(24, 5 * BLOCK)
+    bm.get_computed_blocks(1, p)
+    bm.allocate_slots(1, p.size)
+    bm.fork(1, 2)                                     # shares all 5 blocks
+    bm.fork(1, 3)
+    src, dst = bm.cow(3, 2)                           # request 3 diverges at block 2
+    tables, nblk, start, members = bm.prefix_groups([1, 2, 3], max_prefix_blocks=8)
+    assert nblk.tolist() == [2] and members.tolist() == [0, 1, 2]
+    tables, nblk, _, _ = bm.prefix_groups([1, 2], max_prefix_blocks=8)
+    assert nblk.tolist() == [5]
+    tables, nblk, _, _ = bm.prefix_groups([1, 2], max_prefix_blocks=3)   # capped
+    assert nblk.tolist() == [3] and tables[0].tolist() == bm.block_table(1)[:3]
+
+
+def test_prefix_groups_limits_and_errors(pkv):
+    bm = pkv.BlockManager(64)
+    for g in range(3):                                # three pairs, each sharing a block
+        p = toks(30 + g, BLOCK)
+        bm.get_computed_blocks(10 * g, p)
+        bm.allocate_slots(10 * g, p.size + 1)
+        bm.fork(10 * g, 10 * g + 1)
+    reqs = [0, 1, 10, 11, 20, 21]
+    tables, nblk, start, members = bm.prefix_groups(reqs, max_prefix_blocks=4)
+    assert len(nblk) == 3 and start.tolist() == [0, 2, 4, 6]
+    tables, nblk, start, members = bm.prefix_groups(reqs, max_prefix_blocks=4, max_groups=2)
+    assert len(nblk) == 2 and members.tolist() == [0, 1, 2, 3]
+    single = bm.prefix_groups([0], max_prefix_blocks=4)
+    assert len(single[1]) == 0 and single[2].tolist() == [0]
+    with pytest.raises(ValueError):
+        bm.prefix_groups([0, 99], max_prefix_blocks=4)
