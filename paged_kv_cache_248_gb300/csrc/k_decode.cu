@@ -51,6 +51,7 @@ constexpr int kRing = 3;                      // ring of items prepared by the s
 constexpr int kMaxIds = kNoSplitKeys / kBlock;  // block ids of one item (the longest item is unsplit)
 constexpr uint32_t kTmemCols = 64;            // S^T x2 (cols 0, 16), O^T x2 (cols 32, 48)
 constexpr int kBlocksPerTile = kTileKeys / kBlock;
+constexpr int kCasStage = 16;                 // prefix-partial floats a softmax thread stages per item
 
 struct alignas(16) ItemInfo {
   int32_t idx;  // decode item index; -1 = queue exhausted
@@ -72,6 +73,10 @@ struct Ctl {
   int bad[kRing];
   int32_t ids[kRing][kMaxIds];  // physical block ids of each ring item, validated
   float red[2][4][16];
+  // a shared-prefix member's prefix partials, copied in at the start of its item and
+  // folded at the end: accumulators [split * GP + head][128], max and sum by item parity
+  float cas_o[kCasStage][128];
+  float cas_ml[2][2 * kCasStage];
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -115,10 +120,6 @@ __device__ __forceinline__ void merge_fold(float (&M)[GP], float (&num)[GP], flo
     num[g] = fmaf(num[g], a, ov[g] * b);
     M[g] = m_new;
   }
-}
-
-__device__ __forceinline__ void prefetch_l1(const void* p) {
-  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
 }
 
 __device__ __forceinline__ void raise_abort(Ctl& c, uint32_t* err) {
@@ -453,7 +454,7 @@ __device__ void softmax_warps(const DecodeParams& P, Ctl& c, uint8_t* stages, ui
   const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
   const int G = P.group;
   volatile int* abort_flag = &c.abort_flag;
-  uint32_t it = 0, tc = 0, gph = 0;
+  uint32_t it = 0, tc = 0, gph = 0, nstaged = 0;
   bool ok = true;
   while (ok) {
     const int slot = it % kRing;
@@ -476,15 +477,24 @@ __device__ void softmax_warps(const DecodeParams& P, Ctl& c, uint8_t* stages, ui
       continue;
     }
 
-    // a shared-prefix member whose own keys are one split finishes here: its prefix
-    // partials (written by the cascade kernel) are pulled into L1 now, folded at the end
+    // a shared-prefix member whose own keys are one split finishes here: the first nst
+    // of its prefix partials (written by the cascade kernel) are copied into shared
+    // memory now, so that the fold at the end does not wait on global loads.  Each
+    // thread copies (and later reads) its own accumulator elements; the max/sum pairs
+    // are read by all four warps after the group barrier that follows the copies' wait.
     const bool fold_prefix = info.member && info.nsplit == 1;
     const int64_t cbase = (static_cast<int64_t>(info.centry) * P.hkv + info.head) * P.cas_np_max;
     const int npre = fold_prefix ? static_cast<int>(cascade_splits(info.key_start)) : 0;
-    for (int s = 0; s < npre; ++s) {
-#pragma unroll
-      for (int g = 0; g < GP; ++g) prefetch_l1(P.cas_o + ((cbase + s) * GP + g) * 128 + r);
-      if (r < GP / 2) prefetch_l1(P.cas_ml + (cbase + s) * GP * 2 + 4 * r);
+    const int nst = npre < kCasStage / GP ? npre : kCasStage / GP;
+    // the pairs alternate between two buffers over the items that stage them: another
+    // warp may still be reading the previous such item's pairs, but not the one before
+    // (that would take it past the previous item's group barriers)
+    const int mlb = nstaged & 1;
+    if (nst > 0) {
+      ++nstaged;
+      for (int k = 0; k < nst * GP; ++k) cp_async4(&c.cas_o[k][r], P.cas_o + (cbase * GP + k) * 128 + r);
+      if (r < 2 * GP * nst) cp_async4(&c.cas_ml[mlb][r], P.cas_ml + cbase * GP * 2 + r);
+      cp_async_commit();
     }
 
     float m_run[GP], l_run[GP], acc[GP], alpha_prev[GP];
@@ -605,6 +615,7 @@ __device__ void softmax_warps(const DecodeParams& P, Ctl& c, uint8_t* stages, ui
 
     // total softmax denominators: sum the per-thread partial sums over the 128 keys lanes
     float lt[GP];
+    if (nst > 0) cp_async_wait_all();  // the staged prefix partials, before the barrier
     {
 #pragma unroll
       for (int g = 0; g < GP; ++g) lt[g] = l_run[g];
@@ -635,14 +646,31 @@ __device__ void softmax_warps(const DecodeParams& P, Ctl& c, uint8_t* stages, ui
         num[g] = 0.f;
         den[g] = 0.f;
       }
-      for (int s = 0; s < npre; ++s) {
+      for (int s = 0; s < nst; ++s) {
         float ml[2 * GP], ov[GP];
-        const float* ml_p = P.cas_ml + (cbase + s) * GP * 2;
 #pragma unroll
-        for (int k = 0; k < 2 * GP; ++k) ml[k] = __ldg(ml_p + k);
+        for (int k = 0; k < 2 * GP; ++k) ml[k] = c.cas_ml[mlb][s * 2 * GP + k];
 #pragma unroll
-        for (int g = 0; g < GP; ++g) ov[g] = __ldg(P.cas_o + ((cbase + s) * GP + g) * 128 + r);
+        for (int g = 0; g < GP; ++g) ov[g] = c.cas_o[s * GP + g][r];
         merge_fold<GP>(M, num, den, ml, ov);
+      }
+      // the rest straight from global memory, kU splits' loads issued before their folds
+      constexpr int kU = GP <= 4 ? 4 : GP == 8 ? 2 : 1;
+      for (int s0 = nst; s0 < npre; s0 += kU) {
+        float ml[kU][2 * GP], ov[kU][GP];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          if (s0 + u < npre) {
+            const int64_t e = cbase + s0 + u;
+#pragma unroll
+            for (int k = 0; k < 2 * GP; ++k) ml[u][k] = __ldg(P.cas_ml + e * GP * 2 + k);
+#pragma unroll
+            for (int g = 0; g < GP; ++g) ov[u][g] = __ldg(P.cas_o + (e * GP + g) * 128 + r);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+          if (s0 + u < npre) merge_fold<GP>(M, num, den, ml[u], ov[u]);
       }
       float ml[2 * GP];
 #pragma unroll

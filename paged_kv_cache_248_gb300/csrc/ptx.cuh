@@ -153,6 +153,13 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
                    smem_u32(bar))
                : "memory");
 }
+// 4-byte global -> shared copy by the issuing thread (cp.async through L1); the copy is
+// complete, and visible to this thread, after its cp_async_wait_all.
+__device__ __forceinline__ void cp_async4(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem_dst)), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 // Each thread of the warp reads 16 consecutive 32-bit columns of its own TMEM lane; the
 // wait for the load is in the same statement, so the outputs cannot be used before the
 // load has completed.

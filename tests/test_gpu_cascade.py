@@ -84,6 +84,22 @@ def test_suffix_of_one_key_and_exact_split_boundaries(pkv):
     compare(cas, ref, "bf16", w.name)
 
 
+@pytest.mark.parametrize("group", [4, 8, 16])
+def test_long_prefixes_fold_every_prefix_split(pkv, group):
+    # prefixes of 5 and 10 prefix splits (2400 and 4800 keys): a member's decode item
+    # folds more prefix partials than it stages in shared memory at its start (four
+    # for a padded group of 4, two for 8, one for 16), the rest straight from global
+    w, hints = wl.shared_prefix_case(17, prefix_blocks=(150, 300), members=(9, 6), group=group, num_kv_heads=1,
+                                     bystanders=3, bad_hints=False)
+    t_cpu = w.make_tensors("cpu")
+    t = {k: v.cuda() for k, v in t_cpu.items()}
+    _, cas, st = run_both(pkv, w, hints, t)
+    assert st == 0
+    ref = oracle.attention(bits(t_cpu["q"]), bits(t_cpu["k_cache"]), bits(t_cpu["v_cache"]), w.block_tables,
+                           w.seq_lens, w.query_start_loc, w.scale)
+    compare(cas, ref, "bf16", w.name)
+
+
 def test_malformed_hints_fall_back(pkv):
     w, hints = wl.shared_prefix_case(13, bad_hints=True)
     t_cpu = w.make_tensors("cpu")
