@@ -288,6 +288,10 @@ PKV_API const char* pkv_trace_kind_name(int kind);
  * params (host int32[29]): M, N, a_mn_major, b_mn_major, a_layout, a_lbo, a_sbo,
  * b_layout, b_lbo, b_sbo, a_bytes, b_bytes, k_steps, a_off[8], b_off[8] -- layouts
  * use the descriptor codes (0 none, 2 128B, 4 64B, 6 32B), offsets are bytes.
+ * a_layout = -1 reads A from TMEM instead (M must be 128, A K-major): a_img is then
+ * [128 rows][a_bytes / 512] 32-bit columns, two bf16 each, stored to the rows' lanes
+ * after the N accumulator columns, and a_off[k] is k step k's first column (a multiple
+ * of 8) within them.
  * pkv_tma_selftest loads rows [row0, row0+16) of a bf16 [rows][128] matrix with two
  * 16 x 64 boxes in the 128-byte swizzle and copies the 4 KiB of shared memory they
  * land in to dump.

@@ -1,9 +1,10 @@
 // k_probe.cu -- self-tests of the tcgen05 operand layouts and of TMA swizzled loads.
 //
 // The attention kernels feed tcgen05.mma from shared memory through 64-bit matrix
-// descriptors and stage K/V with 128-byte-swizzled TMA boxes.  These two small
-// kernels exercise exactly those mechanisms on caller-given operand images so the
-// layouts can be checked against a host matmul, independent of any attention code.
+// descriptors (or, for the A operand, from TMEM) and stage K/V with 128-byte-swizzled
+// TMA boxes.  These two small kernels exercise exactly those mechanisms on
+// caller-given operand images so the layouts can be checked against a host matmul,
+// independent of any attention code.
 #include <cstring>
 
 #include "ptx.cuh"
@@ -34,8 +35,12 @@ __global__ void __launch_bounds__(128) umma_probe_kernel(UmmaProbe P, const uint
   for (int i = threadIdx.x; i < P.b_bytes / 16; i += blockDim.x) reinterpret_cast<uint4*>(b_s)[i] = b_img[i];
   fence_proxy_async_smem();
   const int warp = threadIdx.x / 32;
+  // a_layout < 0: A comes from TMEM, a_img being [128 rows][acols] 32-bit columns
+  // (two bf16 each) that land in columns [N, N + acols) of the rows' lanes
+  const bool a_tm = P.a_layout < 0;
+  const int acols = a_tm ? P.a_bytes / (128 * 4) : 0;
   uint32_t ncols = 32;
-  while (ncols < static_cast<uint32_t>(P.N)) ncols <<= 1;
+  while (ncols < static_cast<uint32_t>(P.N + acols)) ncols <<= 1;
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(&bar, 1);
@@ -46,12 +51,32 @@ __global__ void __launch_bounds__(128) umma_probe_kernel(UmmaProbe P, const uint
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base;
+  if (a_tm) {
+    const uint32_t lane_base = (static_cast<uint32_t>(warp % 4) * 32u) << 16;
+    const int row = (warp % 4) * 32 + threadIdx.x % 32;
+    const uint32_t* a_rows = reinterpret_cast<const uint32_t*>(a_img);
+    for (int c0 = 0; c0 < acols; c0 += 16) {
+      uint32_t r[16];
+      for (int j = 0; j < 16; ++j) r[j] = a_rows[row * acols + c0 + j];
+      tmem_st16(tmem + lane_base + static_cast<uint32_t>(P.N + c0), r);
+    }
+    tmem_st_wait();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
   if (threadIdx.x == 0) {
     const uint32_t idesc = umma_idesc_bf16(P.M, P.N, P.a_mn != 0, P.b_mn != 0);
-    const uint64_t a0 = umma_smem_desc(smem_u32(a_s), P.a_lbo, P.a_sbo, P.a_layout);
     const uint64_t b0 = umma_smem_desc(smem_u32(b_s), P.b_lbo, P.b_sbo, P.b_layout);
-    for (int k = 0; k < P.k_steps; ++k)
-      umma_f16_ss(tmem, umma_desc_advance(a0, P.a_off[k]), umma_desc_advance(b0, P.b_off[k]), idesc, k > 0);
+    if (a_tm) {
+      for (int k = 0; k < P.k_steps; ++k)
+        umma_f16_ts(tmem, tmem + static_cast<uint32_t>(P.N + P.a_off[k]), umma_desc_advance(b0, P.b_off[k]), idesc,
+                    k > 0);
+    } else {
+      const uint64_t a0 = umma_smem_desc(smem_u32(a_s), P.a_lbo, P.a_sbo, P.a_layout);
+      for (int k = 0; k < P.k_steps; ++k)
+        umma_f16_ss(tmem, umma_desc_advance(a0, P.a_off[k]), umma_desc_advance(b0, P.b_off[k]), idesc, k > 0);
+    }
     umma_commit(&bar);
   }
   const bool ok = mbar_wait(&bar, 0, &abort_flag);
@@ -108,9 +133,15 @@ int run_umma_selftest(const int32_t* params, const void* a_img, const void* b_im
   if (!(P.M == 128) || P.N < 16 || P.N > 256 || P.N % 16 != 0) return PKV_ERR_INVALID_ARG;
   if (P.a_bytes <= 0 || P.a_bytes > 65536 || P.b_bytes <= 0 || P.b_bytes > 65536) return PKV_ERR_INVALID_ARG;
   if (P.a_bytes % 16 || P.b_bytes % 16 || P.k_steps < 1 || P.k_steps > 8) return PKV_ERR_INVALID_ARG;
+  if (P.a_layout < 0) {  // A from TMEM: 128 rows of acols columns, each k step 8 columns in
+    const int acols = P.a_bytes / (128 * 4);
+    if (P.a_bytes != acols * 128 * 4 || acols % 16 || P.N + acols > 512 || P.a_mn) return PKV_ERR_INVALID_ARG;
+    for (int k = 0; k < P.k_steps; ++k)
+      if (P.a_off[k] < 0 || P.a_off[k] % 8 || P.a_off[k] + 8 > acols) return PKV_ERR_INVALID_ARG;
+  }
   for (int k = 0; k < P.k_steps; ++k)
-    if (P.a_off[k] < 0 || P.a_off[k] >= P.a_bytes || P.b_off[k] < 0 || P.b_off[k] >= P.b_bytes ||
-        P.a_off[k] % 16 || P.b_off[k] % 16)
+    if ((P.a_layout >= 0 && (P.a_off[k] < 0 || P.a_off[k] >= P.a_bytes || P.a_off[k] % 16)) || P.b_off[k] < 0 ||
+        P.b_off[k] >= P.b_bytes || P.b_off[k] % 16)
       return PKV_ERR_INVALID_ARG;
   cudaError_t e = cudaFuncSetAttribute(umma_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kProbeSmem);
   if (e != cudaSuccess) return cuda_status(e);

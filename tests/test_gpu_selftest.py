@@ -118,6 +118,18 @@ def test_kmajor_a_mnmajor_b_n128(pkv):
         pytest.fail(f"MN-major B mismatch; swapped LBO/SBO matches: {bool(np.array_equal(dd, expect))}")
 
 
+def test_tmem_a_mnmajor_b_n128(pkv):
+    # prefill O = P V with P read from TMEM: lane r holds row r of P, keys 2c and 2c+1
+    # packed low/high in 32-bit column c, i.e. the row-major bf16 bits of P; k step kk
+    # reads columns 8 kk .. 8 kk + 7.  B = V as above.
+    P = small_ints((128, 128), 9)
+    V = small_ints((128, 128), 10)
+    a_img, b_img = bf16_bits(P).reshape(-1).copy(), ksw_image(bf16_bits(V))
+    d = run(pkv, 128, 128, 0, 1, -1, 0, 0, 2, 16384, 1024, a_img, b_img, [8 * kk for kk in range(8)],
+            [kk * 2048 for kk in range(8)])
+    np.testing.assert_array_equal(d, P @ V)
+
+
 @pytest.mark.parametrize("row0", [0, 16, 37])
 def test_tma_swizzle_128b(pkv, row0):
     rows = 64
