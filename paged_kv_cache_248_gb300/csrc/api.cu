@@ -322,7 +322,7 @@ int attention_impl(const void* q, const void* k_new, const void* v_new, const vo
   Workspace ws;
   layout_workspace(ctx->ws, num_seqs, hkv, gp, cache->head_dim, max_dec_items, &ws, casp);
   PlanArgs plan{seq_lens, query_start_loc, num_seqs, num_tokens, hkv, max_blocks_per_seq, max_seq_len,
-                kSplitKeys, kTileKeys / gp, ws.counters, ws.dec_prefix, ws.pre_prefix, ws.unit_bad,
+                kSplitKeys, kPrefillTilesPerItem * (kTileKeys / gp), ws.counters, ws.dec_prefix, ws.pre_prefix, ws.unit_bad,
                 ws.merge_list, ctx->err};
   plan.bt = block_tables;
   if (write) {
@@ -339,7 +339,7 @@ int attention_impl(const void* q, const void* k_new, const void* v_new, const vo
   }
   if (casp) {
     plan.cas = cas;
-    plan.cas_rows = kTileKeys / gp;
+    plan.cas_rows = kPrefillTilesPerItem * (kTileKeys / gp);
     plan.seq_prefix = ws.seq_prefix;
     plan.seq_entry = ws.seq_entry;
     plan.member_ok = ws.member_ok;

@@ -106,7 +106,7 @@ extern "C" PKV_API int paged_attention_noalloc(const void* q, const void* k_cach
   AttnArgs a{q,        k_cache,    v_cache,       *cache,      block_tables, max_blocks_per_seq, seq_lens,
              query_start_loc, num_seqs, num_q_heads, num_tokens, max_query_len, max_seq_len, scale, out};
   PlanArgs plan{seq_lens, query_start_loc, num_seqs, num_tokens, hkv, max_blocks_per_seq, max_seq_len,
-                kSplitKeys, kTileKeys / gp, ws.counters, ws.dec_prefix, ws.pre_prefix, ws.unit_bad,
+                kSplitKeys, kPrefillTilesPerItem * (kTileKeys / gp), ws.counters, ws.dec_prefix, ws.pre_prefix, ws.unit_bad,
                 ws.merge_list, err};
   st = launch_plan(plan, s);
   if (st) return st;

@@ -6,7 +6,8 @@
 //   decode items  -- requests with exactly one query token: num_kv_heads x
 //                    decode_splits(seq_len) (kv head, key split) items;
 //   prefill items -- requests with more query tokens: num_kv_heads x
-//                    ceil(q_len / rows_per_tile) (kv head, query tile) items.
+//                    ceil(q_len / rows_per_tile) (kv head, query rows) items, an item
+//                    being the prefill kernel's pair of query tiles.
 // Split boundaries depend only on a request's own length and a library constant,
 // so a request's result does not depend on what else is in the batch.  It also
 // zeroes the work-queue counters and the per-(request, kv head) bad-block flags
@@ -19,6 +20,7 @@
 // ids.  A member's decode items then cover only the keys after the prefix, it goes
 // to the split merge when those keys are cut into several splits, and
 // the cascade kernel gets ceil(members / rows) x kv heads x cascade_splits(P) items
+// (rows: the member requests of one item)
 // per group.  Anything else listed is attended the ordinary way.
 #include "pkv_internal.cuh"
 

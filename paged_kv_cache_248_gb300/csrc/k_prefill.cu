@@ -9,68 +9,75 @@
 //
 // Work decomposition.  The G query heads that share a kv head are folded into the
 // 128 rows of one MMA tile: R = 128 / GP queries x GP heads (GP = G rounded up to
-// 4, 8 or 16), row r <-> (query j0 + r / GP, head r % GP).  One K/V tile then feeds
-// the whole group.  Items (request, kv head, query tile), heaviest query tiles of a
+// 4, 8 or 16), row r <-> (query j0 + r / GP, head r % GP).  An item is a pair of
+// query tiles of one (request, kv head) -- tiles 2p + 1 and 2p, the later one as
+// tile 0 of the item -- and every K/V tile it loads feeds both: the later tile sees
+// the earlier one's keys and at most one tile more.  Items, the heaviest pairs of a
 // request first, come from an atomic queue to persistent CTAs, one per SM.
 //
-// Per CTA (192 threads):
-//   warp 0     producer: TMA-loads the Q tile (a 3-D box over [token][head][dim])
+// Per CTA (320 threads):
+//   warp 0     producer: TMA-loads the two Q tiles (3-D boxes over [token][head][dim])
 //              and, per 128-key tile, 2 K and 2 V boxes per 16-token block from the
 //              block's physical location (the block-table gather), 128-byte swizzle.
-//              K and V have separate stage barriers and K runs one tile ahead of V:
-//              a K tile is released by its S MMA, a V tile by its P V.
-//   warp 1     MMA issuer: S = Q K^T (M = 128 rows, N = 128 keys) into one of two
-//              TMEM buffers, then O += P V into a TMEM accumulator, V read MN-major.
-//   warps 2-5  softmax: thread r owns row r.  It loads its S row from TMEM, applies
-//              the causal mask, and keeps a per-row reference maximum; only when a
-//              row's maximum grows by more than 2^8 does the warp rescale its O rows
-//              in TMEM.  It observes every P V completion in order (mbarrier parity
-//              waits must not skip a phase) before handing over the next P.  P is written as bf16 into
-//              a swizzled K-major operand.  The final O / l is stored per row.
+//              K and V have separate stage barriers and K runs one tile ahead of V.
+//   warp 1     MMA issuer.  Per key tile j and query tile w it issues O_w += P_w(j-1)
+//              V(j-1), then S_w(j) = Q_w K(j)^T.  S_w lives in TMEM; the softmax writes
+//              P_w as bf16 over the first 64 of S_w's columns and the P V MMA reads its
+//              A operand from there.  MMAs issued by one thread complete in order, so
+//              S_w(j+1) cannot overwrite P_w(j) before P_w(j) V(j) has read it, and S_w(j)
+//              complete means P_w(j-1) V(j-1) is complete too.  While one tile's softmax
+//              runs, the tensor core works on the other tile.
+//   warps 2-5  softmax of query tile 0, warps 6-9 of tile 1: thread r owns row r.  Per
+//              key tile it reads its S row from TMEM twice -- for the row maximum, then
+//              for the exponents -- so that no whole row is held in registers, applies the
+//              causal mask, and keeps a per-row reference maximum; only when a row's
+//              maximum grows by more than 2^8 does the warp rescale its O rows in TMEM.
+//              The final O / l is stored per row.
 // All waits are bounded (see ptx.cuh); a timeout raises the CTA abort flag.
 //
 // Shared-prefix (cascade) mode, kCas = true.  The same pipeline attends the member
-// decodes of a prefix group to the group's shared prefix: an item is (group, tile of
-// R member requests, kv head, key split of kCascadeSplitKeys prefix keys), its 128
-// rows are (member, head) pairs whose query rows the softmax warps gather with plain
-// loads into the swizzled Q tile (members are scattered over the batch), every key of
-// the split is visible to every row (all members sit past the prefix), and each row
-// leaves its unnormalised accumulator, reference maximum and sum as a partial for the
-// split merge instead of a final output.  The prefix's K/V are read once per
-// (group, kv head, split) for all its members.
+// decodes of a prefix group to the group's shared prefix: an item is (group, two
+// tiles of R member requests each, kv head, key split of kCascadeSplitKeys prefix
+// keys), a tile's 128 rows are (member, head) pairs whose query rows the softmax warps
+// gather with plain loads into the swizzled Q tile (members are scattered over the
+// batch), every key of the split is visible to every row (all members sit past the
+// prefix), and each row leaves its unnormalised accumulator, reference maximum and
+// sum as a partial for the split merge instead of a final output.  The prefix's K/V
+// are read once per (group, kv head, split, 2R members).
 #include "ptx.cuh"
 #include "pkv_internal.cuh"
 
 namespace pkv {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr int kStages = 2;
 constexpr int kHalfBytes = 16384;          // 128 rows x 128 B
 constexpr int kTileBytes = 2 * kHalfBytes;  // 128 x 128 bf16, K-major, two 64-column halves
 constexpr int kStageBytes = 2 * kTileBytes; // K tile + V tile
 constexpr int kRing = 4;
-constexpr uint32_t kTmemCols = 512;         // S x2 (cols 0, 128), O (col 256)
+constexpr uint32_t kTmemCols = 512;         // S_0, S_1 (cols 0, 128; P_w over S_w's first 64), O_0, O_1 (256, 384)
 constexpr uint32_t kOCol = 256;
 constexpr int kBlocksPerTile = kTileKeys / kBlock;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale O when a row max grows by > 2^8
+static_assert(kPrefillTilesPerItem == 2, "an item is a pair of query tiles");
 
 struct alignas(16) PItem {
-  int32_t idx;  // -1: queue exhausted
-  int32_t seq, head, qt;  // seq: the request (cascade: the prefix group)
-  int32_t q_len, ctx, j0, nq;  // j0: first query of the tile (cascade: first member entry)
-  int32_t nt, valid, t0, kend;  // keys [ks, kend) in nt tiles
-  int32_t ks, split, pad0, pad1;
+  int32_t idx;                    // -1: queue exhausted
+  int32_t seq, head, split;       // seq: the request (cascade: the prefix group)
+  int32_t q_len, ctx, t0, valid;  // t0: the request's first token row
+  int32_t ks, pad0, pad1, pad2;   // the item's keys start at ks (cascade: the split's first key)
+  int32_t nt[2], kend[2];         // query tile w: keys [ks, kend[w]) in nt[w] tiles (0: no tile w)
+  int32_t j0[2], nq[2];           // its first query (cascade: first member entry) and how many
+  int32_t qt[2], pad3, pad4;      // its query-tile index (-1: none)
 };
 
 struct Ctl {
-  // K and V of a stage have their own barriers: a K tile is released when its S MMA
-  // completes and a V tile when its P V completes, so the next K load starts about one
-  // softmax iteration before the stage's P V is done
+  // K and V of a stage have their own barriers: a K tile is released when the S MMAs
+  // of both query tiles have read it, a V tile when both P V MMAs have
   uint64_t kfull[kStages], kempty[kStages], vfull[kStages], vempty[kStages];
-  uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
-  uint64_t o_full, o_free;
-  uint64_t q_full, q_free;
+  uint64_t s_full[2], p_full[2], o_full[2], o_free[2];  // per query tile
+  uint64_t q_full[2], q_free[2];
   uint64_t item_full[kRing], item_empty[kRing];
   uint64_t drain;
   PItem ring[kRing];
@@ -79,8 +86,7 @@ struct Ctl {
   int abort_flag;
 };
 
-constexpr int kSmemBytes = kTileBytes /*Q*/ + kStages * kStageBytes + 2 * kTileBytes /*P x2*/ +
-                           static_cast<int>(sizeof(Ctl)) + 1024;
+constexpr int kSmemBytes = 2 * kTileBytes /*Q x2*/ + kStages * kStageBytes + static_cast<int>(sizeof(Ctl)) + 1024;
 static_assert(kSmemBytes <= 232448, "prefill shared memory");
 
 struct PrefillParams {
@@ -109,6 +115,69 @@ struct PrefillParams {
   int32_t cas_max_blocks, cas_groups, cas_np_max;
 };
 
+// The extremum of one S row of 128 raw scores from TMEM (taddr: the row's first
+// column): the maximum, or for kPos false the minimum (a negative scale turns it into
+// the maximum of scale * s).  With kMask, keys from nvis on do not count.  Each
+// 32-column piece is loaded while the previous one is reduced.
+template <bool kPos, bool kMask>
+__device__ __forceinline__ float row_extremum(uint32_t taddr, int nvis) {
+  const float hidden = kPos ? -INFINITY : INFINITY;
+  float mx[8];  // eight independent running extrema keep the dependency chains short
+#pragma unroll
+  for (int k = 0; k < 8; ++k) mx[k] = hidden;
+  uint32_t a[32], b[32];
+  tmem_ld32_issue(taddr, a);
+  tmem_ld32_wait(a);
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    uint32_t(&cur)[32] = (h & 1) ? b : a;
+    uint32_t(&nxt)[32] = (h & 1) ? a : b;
+    if (h < 3) tmem_ld32_issue(taddr + 32 * (h + 1), nxt);
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      const float x = (!kMask || 32 * h + k < nvis) ? __uint_as_float(cur[k]) : hidden;
+      mx[k & 7] = kPos ? fmaxf(mx[k & 7], x) : fminf(mx[k & 7], x);
+    }
+    if (h < 3) tmem_ld32_wait(nxt);
+  }
+  return kPos ? fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])))
+              : fminf(fminf(fminf(mx[0], mx[1]), fminf(mx[2], mx[3])), fminf(fminf(mx[4], mx[5]), fminf(mx[6], mx[7])));
+}
+
+// The exponents 2^(scale * s - m_ref) of one S row (masked keys: 0, with kMask),
+// written back as bf16 P over the row's first 64 columns; returns the row sum.  Each
+// 32-column piece is loaded while the previous one is converted, and the 16 P columns
+// a piece gives land on columns this thread has already read.
+template <bool kMask>
+__device__ __forceinline__ float row_exp_to_p(uint32_t taddr, int nvis, float scale, float m_ref) {
+  const float hidden = scale >= 0.f ? -INFINITY : INFINITY;  // raw score that scales to -inf
+  float ls[4] = {0.f, 0.f, 0.f, 0.f};  // the row sum in four independent parts
+  uint32_t a[32], b[32];
+  tmem_ld32_issue(taddr, a);
+  tmem_ld32_wait(a);
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    uint32_t(&cur)[32] = (h & 1) ? b : a;
+    uint32_t(&nxt)[32] = (h & 1) ? a : b;
+    if (h < 3) tmem_ld32_issue(taddr + 32 * (h + 1), nxt);
+    uint32_t pw[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const int k = 32 * h + 2 * q;
+      const float xa = (!kMask || k < nvis) ? __uint_as_float(cur[2 * q]) : hidden;
+      const float xb = (!kMask || k + 1 < nvis) ? __uint_as_float(cur[2 * q + 1]) : hidden;
+      const float pa = ex2_approx(fmaf(xa, scale, -m_ref));
+      const float pb = ex2_approx(fmaf(xb, scale, -m_ref));
+      ls[q & 3] += pa + pb;
+      __nv_bfloat162 h2 = __floats2bfloat162_rn(pa, pb);
+      pw[q] = *reinterpret_cast<uint32_t*>(&h2);
+    }
+    tmem_st16(taddr + 16 * h, pw);
+    if (h < 3) tmem_ld32_wait(nxt);
+  }
+  return (ls[0] + ls[1]) + (ls[2] + ls[3]);
+}
+
 __device__ __forceinline__ void raise_abort(Ctl& c, uint32_t* err) {
   *reinterpret_cast<volatile int*>(&c.abort_flag) = 1;
   flag_error(err, kErrTimeout);
@@ -116,6 +185,7 @@ __device__ __forceinline__ void raise_abort(Ctl& c, uint32_t* err) {
 
 __device__ PItem make_item(const PrefillParams& P, int idx, int total) {
   PItem r{};
+  r.qt[0] = r.qt[1] = -1;
   if (idx >= total) {
     r.idx = -1;
     return r;
@@ -128,35 +198,44 @@ __device__ PItem make_item(const PrefillParams& P, int idx, int total) {
   const int i = lo;
   const int base = P.pre_prefix[i];
   const int cnt = P.pre_prefix[i + 1] - base;
-  const int nqt = cnt / P.hkv;
+  const int npair = cnt / P.hkv;
   r.idx = idx;
   r.seq = i;
-  if (nqt <= 0) return r;  // inconsistent plan: invalid item
+  if (npair <= 0) return r;  // inconsistent plan: invalid item
   const int local = idx - base;
-  r.qt = nqt - 1 - local / P.hkv;  // heaviest (latest) query tiles first
+  const int pair = npair - 1 - local / P.hkv;  // heaviest (latest) query tiles first
   r.head = local % P.hkv;
   const int64_t q0 = P.qsl[i], q1 = P.qsl[i + 1];
   const int64_t L = P.seq_lens[i];
   const int64_t q_len = q1 - q0;
   r.q_len = static_cast<int32_t>(q_len);
   r.t0 = static_cast<int32_t>(q0);
-  r.j0 = r.qt * P.rows_q;
-  const int64_t left = q_len - r.j0;
-  r.nq = static_cast<int32_t>(left < P.rows_q ? left : P.rows_q);
+  // tile 0 of the item is the later query tile of the pair, tile 1 the earlier one
+  const int64_t nqt = q_len > 0 ? (q_len + P.rows_q - 1) / P.rows_q : 0;
+  const int hi_t = 2 * pair + 1, lo_t = 2 * pair;
+  r.qt[0] = hi_t < nqt ? hi_t : lo_t;
+  r.qt[1] = hi_t < nqt ? lo_t : -1;
   const bool ok = q_len > 1 && L >= q_len && (L + kBlock - 1) / kBlock <= P.max_blocks && q0 >= 0 &&
-                  q1 <= P.num_tokens && (q_len + P.rows_q - 1) / P.rows_q == nqt && r.nq > 0;
+                  q1 <= P.num_tokens && (q_len + 2 * P.rows_q - 1) / (2 * P.rows_q) == npair && lo_t < nqt;
   r.valid = ok ? 1 : 0;
   if (ok) {
     r.ctx = static_cast<int32_t>(L - q_len);
-    r.kend = r.ctx + r.j0 + r.nq;  // keys [0, kend) are visible to some row of the tile
-    r.nt = (r.kend + kTileKeys - 1) / kTileKeys;
+    for (int w = 0; w < 2; ++w) {
+      if (r.qt[w] < 0) continue;
+      r.j0[w] = r.qt[w] * P.rows_q;
+      const int64_t left = q_len - r.j0[w];
+      r.nq[w] = static_cast<int32_t>(left < P.rows_q ? left : P.rows_q);
+      r.kend[w] = r.ctx + r.j0[w] + r.nq[w];  // keys [0, kend) are visible to some row of the tile
+      r.nt[w] = (r.kend[w] + kTileKeys - 1) / kTileKeys;
+    }
   }
   return r;
 }
 
-// A cascade item: group g by its item prefix, then (member tile, kv head, key split).
+// A cascade item: group g by its item prefix, then (member tile pair, kv head, key split).
 __device__ PItem make_cas_item(const PrefillParams& P, int idx, int total) {
   PItem r{};
+  r.qt[0] = r.qt[1] = -1;
   if (idx >= total) {
     r.idx = -1;
     return r;
@@ -175,13 +254,23 @@ __device__ PItem make_cas_item(const PrefillParams& P, int idx, int total) {
   const int local = idx - P.cas_prefix[lo];
   r.split = local % np;
   r.head = (local / np) % P.hkv;
-  r.qt = local / np / P.hkv;
-  r.j0 = e0 + r.qt * P.rows_q;
-  r.nq = min(P.rows_q, e1 - r.j0);
+  const int pq = local / np / P.hkv;
   r.ks = r.split * kCascadeSplitKeys;
-  r.kend = min(pb * kBlock, r.ks + kCascadeSplitKeys);
-  r.nt = (r.kend - r.ks + kTileKeys - 1) / kTileKeys;
-  r.valid = (r.nq > 0 && r.ks < r.kend) ? 1 : 0;
+  const int kend = min(pb * kBlock, r.ks + kCascadeSplitKeys);
+  const int nt = (kend - r.ks + kTileKeys - 1) / kTileKeys;
+  for (int w = 0; w < 2; ++w) {
+    r.qt[w] = 2 * pq + w;
+    r.j0[w] = e0 + r.qt[w] * P.rows_q;
+    r.nq[w] = min(P.rows_q, e1 - r.j0[w]);
+    if (r.nq[w] > 0) {
+      r.kend[w] = kend;
+      r.nt[w] = nt;
+    } else {
+      r.nq[w] = 0;
+      r.qt[w] = -1;
+    }
+  }
+  r.valid = (r.nq[0] > 0 && r.ks < kend) ? 1 : 0;
   return r;
 }
 
@@ -192,7 +281,8 @@ __device__ void producer_warp(const PrefillParams& P, const CUtensorMap* qmap, c
   const int lane = threadIdx.x & 31;
   const int total = kCas ? P.cas_prefix[P.cas_groups] : P.pre_prefix[P.num_seqs];
   volatile int* abort_flag = &c.abort_flag;
-  uint32_t it = 0, tk = 0, tv = 0, qc = 0;  // items; K and V tiles issued; query tiles
+  uint32_t it = 0, tk = 0, tv = 0;  // items; K and V tiles issued
+  uint32_t qc[2] = {0, 0};          // Q tiles loaded per tile slot
   bool ok = true;
   while (ok) {
     const int slot = it % kRing;
@@ -212,21 +302,29 @@ __device__ void producer_warp(const PrefillParams& P, const CUtensorMap* qmap, c
     if (info.idx < 0) break;
     if (!info.valid) continue;
     if (!kCas) {  // (cascade: the softmax warps gather Q)
-      if (!mbar_wait(&c.q_free, (qc & 1) ^ 1, abort_flag)) {
-        ok = false;
-        break;
+#pragma unroll
+      for (int w = 0; w < 2; ++w) {
+        if (!ok) break;
+        if (info.nt[w] == 0) continue;
+        if (!mbar_wait(&c.q_free[w], (qc[w] & 1) ^ 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          uint8_t* q = qbuf + w * kTileBytes;
+          mbar_arrive_expect_tx(&c.q_full[w], kTileBytes);
+          const int32_t y = info.head * P.group, z = info.t0 + info.j0[w];
+          tma_load_3d(q, qmap, &c.q_full[w], 0, y, z, l2_policy_evict_first());
+          tma_load_3d(q + kHalfBytes, qmap, &c.q_full[w], 64, y, z, l2_policy_evict_first());
+        }
+        __syncwarp();
+        ++qc[w];
       }
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&c.q_full, kTileBytes);
-        const int32_t y = info.head * P.group, z = info.t0 + info.j0;
-        tma_load_3d(qbuf, qmap, &c.q_full, 0, y, z, l2_policy_evict_first());
-        tma_load_3d(qbuf + kHalfBytes, qmap, &c.q_full, 64, y, z, l2_policy_evict_first());
-      }
-      ++qc;
+      if (!ok) break;
     }
     const int32_t* btrow = kCas ? P.cas_tables + static_cast<int64_t>(info.seq) * P.cas_max_blocks
                                 : P.bt + static_cast<int64_t>(info.seq) * P.max_blocks;
-    // V of tile j - 1 into its stage once that stage's previous P V is done
+    // V of tile j - 1 into its stage once that stage's previous P V MMAs are done
     auto load_v = [&](int id, int nblk) -> bool {
       const int st = tv % kStages;
       if (!mbar_wait(&c.vempty[st], ((tv / kStages) & 1) ^ 1, abort_flag)) return false;
@@ -241,15 +339,16 @@ __device__ void producer_warp(const PrefillParams& P, const CUtensorMap* qmap, c
       ++tv;
       return true;
     };
+    // the keys of tile 0 of the item cover those of tile 1
     int prev_id = 0, prev_nblk = 0;
-    for (int j = 0; j < info.nt; ++j) {
+    for (int j = 0; j < info.nt[0]; ++j) {
       const int st = tk % kStages;
       if (!mbar_wait(&c.kempty[st], ((tk / kStages) & 1) ^ 1, abort_flag)) {
         ok = false;
         break;
       }
       const int t0 = info.ks + j * kTileKeys;
-      const int nblk = min(kBlocksPerTile, (info.kend - t0 + kBlock - 1) / kBlock);
+      const int nblk = min(kBlocksPerTile, (info.kend[0] - t0 + kBlock - 1) / kBlock);
       int id = 0;
       bool bad = false;
       if (lane < nblk) {
@@ -280,7 +379,7 @@ __device__ void producer_warp(const PrefillParams& P, const CUtensorMap* qmap, c
       prev_id = id;
       prev_nblk = nblk;
     }
-    if (ok && info.nt > 0 && !load_v(prev_id, prev_nblk)) ok = false;
+    if (ok && info.nt[0] > 0 && !load_v(prev_id, prev_nblk)) ok = false;
   }
   if (!ok && !*abort_flag && lane == 0) raise_abort(c, P.err);
   if (*abort_flag) {
@@ -289,44 +388,21 @@ __device__ void producer_warp(const PrefillParams& P, const CUtensorMap* qmap, c
       mbar_wait(&c.kfull[cnt % kStages], (cnt / kStages) & 1, nullptr);
     for (uint32_t cnt = tv > static_cast<uint32_t>(kStages) ? tv - kStages : 0; cnt < tv; ++cnt)
       mbar_wait(&c.vfull[cnt % kStages], (cnt / kStages) & 1, nullptr);
-    if (qc > 0) mbar_wait(&c.q_full, (qc - 1) & 1, nullptr);
+#pragma unroll
+    for (int w = 0; w < 2; ++w)
+      if (qc[w] > 0) mbar_wait(&c.q_full[w], (qc[w] - 1) & 1, nullptr);
   }
 }
 
 // ------------------------------------------------------------------ MMA warp
-__device__ void mma_warp(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uint8_t* stages, uint8_t* pbuf,
-                         uint32_t tmem) {
+__device__ void mma_warp(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uint8_t* stages, uint32_t tmem) {
   const int lane = threadIdx.x & 31;
   const uint32_t idesc_s = umma_idesc_bf16(128, 128, false, false);
   const uint32_t idesc_o = umma_idesc_bf16(128, 128, false, true);
   volatile int* abort_flag = &c.abort_flag;
-  uint32_t it = 0, tc = 0, qc = 0, ic = 0;
+  uint32_t it = 0, tk = 0, tv = 0;
+  uint32_t qc[2] = {0, 0}, pc[2] = {0, 0}, ic[2] = {0, 0};  // per tile slot: Q tiles, P tiles, items
   bool issued = false, ok = true;
-
-  // O (+)= P_j V_j for tile counter cnt; `first` starts the accumulator of an item
-  auto pv = [&](uint32_t cnt, bool first) -> bool {
-    const int st = cnt % kStages, b = cnt & 1;
-    if (!mbar_wait(&c.p_full[b], (cnt >> 1) & 1, abort_flag)) return false;
-    if (!mbar_wait(&c.vfull[st], (cnt / kStages) & 1, abort_flag)) return false;
-    // the previous item's O must have been read out before its accumulator restarts
-    if (first && !mbar_wait(&c.o_free, (ic & 1) ^ 1, abort_flag)) return false;
-    tc_fence_after();
-    if (lane == 0) {
-      const uint64_t a = umma_smem_desc(smem_u32(pbuf + b * kTileBytes), 16, 1024, kLayout128B);
-      const uint64_t bd = umma_smem_desc(smem_u32(stages + st * kStageBytes + kTileBytes), kHalfBytes, 1024,
-                                         kLayout128B);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        umma_f16_ss(tmem + kOCol, umma_desc_advance(a, (kk >> 2) * kHalfBytes + (kk & 3) * 32),
-                    umma_desc_advance(bd, kk * 2048), idesc_o, (!first || kk > 0) ? 1u : 0u);
-      umma_commit(&c.o_full);
-      umma_commit(&c.p_free[b]);
-      umma_commit(&c.vempty[st]);
-    }
-    __syncwarp();
-    return true;
-  };
-
   while (ok) {
     const int slot = it % kRing;
     if (!mbar_wait(&c.item_full[slot], (it / kRing) & 1, abort_flag)) {
@@ -337,38 +413,74 @@ __device__ void mma_warp(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uint8_t*
     ++it;
     if (info.idx < 0) break;
     if (info.valid) {
-      if (!mbar_wait(&c.q_full, qc & 1, abort_flag)) {
-        ok = false;
-        break;
-      }
-      for (int j = 0; j < info.nt && ok; ++j) {
-        const int st = tc % kStages, sb = tc & 1;
-        if (!mbar_wait(&c.kfull[st], (tc / kStages) & 1, abort_flag) ||
-            !mbar_wait(&c.s_free[sb], ((tc >> 1) & 1) ^ 1, abort_flag)) {
+      const int nt0 = info.nt[0];
+#pragma unroll
+      for (int w = 0; w < 2; ++w)
+        if (ok && info.nt[w] > 0 && !mbar_wait(&c.q_full[w], qc[w] & 1, abort_flag)) ok = false;
+      // step j: P_w(j-1) V(j-1), then S_w(j) = Q_w K(j)^T, for w = 0, 1
+      for (int j = 0; j <= nt0 && ok; ++j) {
+        const int sk = tk % kStages, sv = tv % kStages;
+        if ((j < nt0 && !mbar_wait(&c.kfull[sk], (tk / kStages) & 1, abort_flag)) ||
+            (j > 0 && !mbar_wait(&c.vfull[sv], (tv / kStages) & 1, abort_flag))) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        if (lane == 0) {
-          const uint64_t a = umma_smem_desc(smem_u32(qbuf), 16, 1024, kLayout128B);
-          const uint64_t b = umma_smem_desc(smem_u32(stages + st * kStageBytes), 16, 1024, kLayout128B);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-            umma_f16_ss(tmem + 128 * sb, umma_desc_advance(a, off), umma_desc_advance(b, off), idesc_s, kk > 0);
+        for (int w = 0; w < 2; ++w) {
+          if (!ok) break;
+          const int ntw = info.nt[w];
+          if (j > 0 && j - 1 < ntw) {
+            // the item's first P V restarts O_w, once the previous item's O_w was read out
+            if (!mbar_wait(&c.p_full[w], pc[w] & 1, abort_flag) ||
+                (j == 1 && !mbar_wait(&c.o_free[w], (ic[w] & 1) ^ 1, abort_flag))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            if (lane == 0) {
+              const uint64_t bd = umma_smem_desc(smem_u32(stages + sv * kStageBytes + kTileBytes), kHalfBytes, 1024,
+                                                 kLayout128B);
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk)
+                umma_f16_ts(tmem + kOCol + 128 * w, tmem + 128 * w + 8 * kk, umma_desc_advance(bd, kk * 2048),
+                            idesc_o, (j > 1 || kk > 0) ? 1u : 0u);
+              if (j == ntw) umma_commit(&c.o_full[w]);
+            }
+            __syncwarp();
+            ++pc[w];
           }
-          umma_commit(&c.s_full[sb]);
-          umma_commit(&c.kempty[st]);
-          if (j == info.nt - 1) umma_commit(&c.q_free);
-          issued = true;
+          if (j < ntw) {
+            tc_fence_after();
+            if (lane == 0) {
+              const uint64_t a = umma_smem_desc(smem_u32(qbuf + w * kTileBytes), 16, 1024, kLayout128B);
+              const uint64_t b = umma_smem_desc(smem_u32(stages + sk * kStageBytes), 16, 1024, kLayout128B);
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+                umma_f16_ss(tmem + 128 * w, umma_desc_advance(a, off), umma_desc_advance(b, off), idesc_s, kk > 0);
+              }
+              umma_commit(&c.s_full[w]);
+              if (j == ntw - 1) umma_commit(&c.q_free[w]);
+              issued = true;
+            }
+            __syncwarp();
+          }
+        }
+        if (!ok) break;
+        if (lane == 0) {
+          if (j < nt0) umma_commit(&c.kempty[sk]);
+          if (j > 0) umma_commit(&c.vempty[sv]);
         }
         __syncwarp();
-        if (j > 0 && !pv(tc - 1, j == 1)) ok = false;
-        ++tc;
+        if (j < nt0) ++tk;
+        if (j > 0) ++tv;
       }
-      if (ok && !pv(tc - 1, info.nt == 1)) ok = false;
-      ++qc;
-      ++ic;
+#pragma unroll
+      for (int w = 0; w < 2; ++w)
+        if (info.nt[w] > 0) {
+          ++qc[w];
+          ++ic[w];
+        }
     }
     if (!ok) break;
     __syncwarp();
@@ -386,16 +498,20 @@ __device__ void mma_warp(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uint8_t*
 
 // ------------------------------------------------------------------ softmax warps
 template <bool kCas>
-__device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uint8_t* stages, uint8_t* pbuf,
-                              uint32_t tmem) {
+__device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uint8_t* stages, uint32_t tmem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int wq = warp & 3;
-  const int r = wq * 32 + lane;  // tile row
+  const int wq = warp & 3;        // TMEM lane quarter this warp may access
+  const int w = (warp - 2) >> 2;  // the item's query tile this warpgroup owns
+  const int r = wq * 32 + lane;   // tile row
   const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+  const uint32_t s_col = 128u * w, o_col = kOCol + 128u * w;
+  uint8_t* qtile = qbuf + w * kTileBytes;
   volatile int* abort_flag = &c.abort_flag;
-  uint32_t it = 0, tc = 0, qc = 0;
+  uint32_t it = 0, tc = 0, ic = 0, qc = 0, vc = 0;  // items, S tiles, own items, gathered Q tiles, V tiles
   bool ok = true;
   const int rj = r / P.gp, rg = r % P.gp;  // query offset and head of this row within a tile
+  const float scale = P.scale_log2;
+  const bool pos_scale = scale >= 0.f;
 
   while (ok) {
     const int slot = it % kRing;
@@ -406,35 +522,45 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uin
     const PItem info = c.ring[slot];
     ++it;
     if (info.idx < 0) break;
-    const int j_row = info.j0 + rj;
-    const bool row_out = info.nq > 0 && rj < info.nq && rg < P.group;  // a real (token, head) row
-    __nv_bfloat16* orow = P.out + ((static_cast<int64_t>(info.t0) + j_row) * P.hq +
-                                   static_cast<int64_t>(info.head) * P.group + rg) * 128;
-    if (kCas && !info.valid) {
-      if (r == 0) flag_error(P.err, kErrLength);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&c.item_empty[slot]);
-      continue;
-    }
     if (!info.valid) {
-      if (r == 0 && info.head == 0) flag_error(P.err, kErrLength);
-      const int64_t q0 = P.qsl[info.seq], q1 = P.qsl[info.seq + 1];
-      const int jj = info.qt * P.rows_q + rj;
-      if (q0 >= 0 && q1 <= P.num_tokens && q0 + jj < q1 && rg < P.group) {
-        __nv_bfloat16* zrow = P.out + ((q0 + jj) * P.hq + static_cast<int64_t>(info.head) * P.group + rg) * 128;
-        for (int k = 0; k < 16; ++k) reinterpret_cast<uint4*>(zrow)[k] = make_uint4(0, 0, 0, 0);
+      if (kCas) {
+        if (r == 0 && w == 0) flag_error(P.err, kErrLength);
+      } else {
+        if (r == 0 && w == 0 && info.head == 0) flag_error(P.err, kErrLength);
+        const int64_t q0 = P.qsl[info.seq], q1 = P.qsl[info.seq + 1];
+        const int qt = w ? info.qt[1] : info.qt[0];
+        const int64_t jj = static_cast<int64_t>(qt) * P.rows_q + rj;
+        if (qt >= 0 && q0 >= 0 && q1 <= P.num_tokens && q0 + jj < q1 && rg < P.group) {
+          __nv_bfloat16* zrow = P.out + ((q0 + jj) * P.hq + static_cast<int64_t>(info.head) * P.group + rg) * 128;
+          for (int k = 0; k < 16; ++k) reinterpret_cast<uint4*>(zrow)[k] = make_uint4(0, 0, 0, 0);
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&c.item_empty[slot]);
       continue;
     }
+    // this warpgroup's query tile of the item
+    const int nt = w ? info.nt[1] : info.nt[0];
+    const int tj0 = w ? info.j0[1] : info.j0[0];
+    const int tnq = w ? info.nq[1] : info.nq[0];
+    const int tkend = w ? info.kend[1] : info.kend[0];
+    if (nt == 0) {  // the item has one query tile only
+      vc += info.nt[0];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&c.item_empty[slot]);
+      continue;
+    }
+    const int j_row = tj0 + rj;
+    const bool row_out = rj < tnq && rg < P.group;  // a real (token, head) row
+    __nv_bfloat16* orow = P.out + ((static_cast<int64_t>(info.t0) + j_row) * P.hq +
+                                   static_cast<int64_t>(info.head) * P.group + rg) * 128;
     // this row's member entry (cascade) and whether it is stored
-    const int entry = info.j0 + rj;
-    const bool cas_live = kCas && rj < info.nq && P.member_ok[entry] != 0;
+    const int entry = tj0 + rj;
+    const bool cas_live = kCas && rj < tnq && P.member_ok[entry] != 0;
     if (kCas) {
       // gather the query row of (member, head) into the swizzled K-major Q tile once
-      // the previous item's last S = Q K^T has read it
-      if (!mbar_wait(&c.q_free, (qc & 1) ^ 1, abort_flag)) {
+      // the previous item's last S = Q K^T of this tile slot has read it
+      if (!mbar_wait(&c.q_free[w], (qc & 1) ^ 1, abort_flag)) {
         ok = false;
         break;
       }
@@ -451,91 +577,59 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uin
       }
 #pragma unroll
       for (int k = 0; k < 16; ++k)
-        *reinterpret_cast<uint4*>(qbuf + (k >> 3) * kHalfBytes + r * 128 + (((k & 7) ^ (r & 7)) << 4)) = qv[k];
+        *reinterpret_cast<uint4*>(qtile + (k >> 3) * kHalfBytes + r * 128 + (((k & 7) ^ (r & 7)) << 4)) = qv[k];
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&c.q_full);
+      if (lane == 0) mbar_arrive(&c.q_full[w]);
       ++qc;
     }
     // causal bound of this row (padding rows borrow the last real query's bound)
     const int pos = info.ctx + min(j_row, info.q_len - 1);
     const int L = info.ctx + info.q_len;
-    // V rows from here on are either past the context or not loaded this item:
-    // they are zeroed so that 0-weight keys cannot carry non-finite bytes into P V
-    const int zero_from = kCas ? info.kend : min(L, ((info.kend + kBlock - 1) / kBlock) * kBlock);
+    // V rows from here on are either past the context or not loaded this item: tile
+    // 0's warps zero them (tile 0 loads the item's keys) so that 0-weight keys cannot
+    // carry non-finite bytes into P V
+    const int zero_from = kCas ? info.kend[0] : min(L, ((info.kend[0] + kBlock - 1) / kBlock) * kBlock);
     float m_ref = -INFINITY, l_sum = 0.f;
 
-    for (int j = 0; j < info.nt && ok; ++j) {
-      const int st = tc % kStages, sb = tc & 1, pb = tc & 1;
+    for (int j = 0; j < nt && ok; ++j) {
+      const uint32_t vt = vc + j;
+      const int sv = vt % kStages;
       const int k0 = info.ks + j * kTileKeys;
-      if (!mbar_wait(&c.s_full[sb], (tc >> 1) & 1, abort_flag)) {
+      if (!mbar_wait(&c.s_full[w], tc & 1, abort_flag)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      float s[128];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {  // two 64-column loads, each waited for in its own statement
-        uint32_t v[64];
-        tmem_ld64_sync(tmem + lane_off + 128 * sb + 64 * h, v);
-#pragma unroll
-        for (int k = 0; k < 64; ++k) s[64 * h + k] = __uint_as_float(v[k]);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&c.s_free[sb]);
       // keys k0 .. k0 + nvis - 1 are visible to this row (cascade: the whole split).
       // The scores stay unscaled: the tile maximum of scale * s is scale times the
       // maximum of s (the minimum, for a negative scale), and each exponent takes
       // scale * s - m in one fused multiply-add.  Masked keys get the raw value that
       // scales to -inf.  Tiles every row of the warp sees whole skip the masking.
-      const float scale = P.scale_log2;
-      const bool pos_scale = scale >= 0.f;
-      const int nvis = kCas ? info.kend - k0 : pos - k0 + 1;
-      if (!__all_sync(0xffffffffu, nvis >= kTileKeys)) {
-        const float hidden = pos_scale ? -INFINITY : INFINITY;
-#pragma unroll
-        for (int k = 0; k < 128; ++k) s[k] = k < nvis ? s[k] : hidden;
-      }
-      float mx[8];  // eight independent running extrema keep the dependency chains short
-#pragma unroll
-      for (int k = 0; k < 8; ++k) mx[k] = s[k];
-      if (pos_scale) {
-#pragma unroll
-        for (int k = 8; k < 128; ++k) mx[k & 7] = fmaxf(mx[k & 7], s[k]);
-      } else {
-#pragma unroll
-        for (int k = 8; k < 128; ++k) mx[k & 7] = fminf(mx[k & 7], s[k]);
-      }
-      const float raw = pos_scale ? fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                          fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])))
-                                  : fminf(fminf(fminf(mx[0], mx[1]), fminf(mx[2], mx[3])),
-                                          fminf(fminf(mx[4], mx[5]), fminf(mx[6], mx[7])));
+      const int nvis = kCas ? tkend - k0 : pos - k0 + 1;
+      const bool whole = __all_sync(0xffffffffu, nvis >= kTileKeys);
+      const uint32_t srow = tmem + lane_off + s_col;
+      // first read of S: the row's extremum (a negative scale takes the masked form)
+      const float raw = !pos_scale ? row_extremum<false, true>(srow, nvis)
+                                   : whole ? row_extremum<true, false>(srow, nvis) : row_extremum<true, true>(srow, nvis);
       // (a fully masked row gives -inf either way: -inf * scale or +inf * a negative scale)
       const float tmax = raw * scale;
       if (j == 0) {
         m_ref = tmax;  // key 0 is visible to every row, so this is finite
       } else {
-        // Observe P V(j-1) complete before handing over P(j).  Every phase of o_full
-        // must be waited for in order: a parity wait that skips a phase could match
-        // the parity of an older completed phase and return before the MMA is done.
-        if (!mbar_wait(&c.o_full, (tc - 1) & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
+        // S_w(j) complete means P_w(j-1) V(j-1), issued before it, is complete: O_w
+        // holds every tile before j and may be rescaled
         const bool need = tmax > m_ref + kRescaleThreshold;
         if (__any_sync(0xffffffffu, need)) {
-          // rescale this warp's O rows (P V(j-1) has landed)
-          tc_fence_after();
           const float m_new = need ? tmax : m_ref;
           const float alpha = exp2f(m_ref - m_new);
 #pragma unroll
           for (int ch = 0; ch < 8; ++ch) {  // rare: 16 columns at a time keeps registers low
             uint32_t v[16];
-            tmem_ld16_sync(tmem + lane_off + kOCol + 16 * ch, v);
+            tmem_ld16_sync(tmem + lane_off + o_col + 16 * ch, v);
 #pragma unroll
             for (int k = 0; k < 16; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
-            tmem_st16(tmem + lane_off + kOCol + 16 * ch, v);
+            tmem_st16(tmem + lane_off + o_col + 16 * ch, v);
           }
           tmem_st_wait();
           l_sum *= alpha;
@@ -543,51 +637,35 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uin
         }
       }
       // V of this stage has landed (also orders the producer's bad-block flag)
-      if (!mbar_wait(&c.vfull[st], (tc / kStages) & 1, abort_flag)) {
+      if (!mbar_wait(&c.vfull[sv], (vt / kStages) & 1, abort_flag)) {
         ok = false;
         break;
       }
-      if (k0 + r >= zero_from) {
-        uint8_t* vrow = stages + st * kStageBytes + kTileBytes + r * 128;
+      if (w == 0 && k0 + r >= zero_from) {
+        uint8_t* vrow = stages + sv * kStageBytes + kTileBytes + r * 128;
 #pragma unroll
         for (int c16 = 0; c16 < 8; ++c16) {
           *reinterpret_cast<uint4*>(vrow + c16 * 16) = make_uint4(0, 0, 0, 0);
           *reinterpret_cast<uint4*>(vrow + kHalfBytes + c16 * 16) = make_uint4(0, 0, 0, 0);
         }
+        fence_proxy_async_smem();
       }
-      if (!mbar_wait(&c.p_free[pb], ((tc >> 1) & 1) ^ 1, abort_flag)) {
-        ok = false;
-        break;
-      }
-      uint8_t* prow = pbuf + pb * kTileBytes + r * 128;
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};  // the tile's row sum in four independent parts
-#pragma unroll
-      for (int kc = 0; kc < 16; ++kc) {
-        uint32_t w[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float a = ex2_approx(fmaf(s[8 * kc + 2 * q], scale, -m_ref));
-          const float b = ex2_approx(fmaf(s[8 * kc + 2 * q + 1], scale, -m_ref));
-          ls[q] += a + b;
-          __nv_bfloat162 h2 = __floats2bfloat162_rn(a, b);
-          w[q] = *reinterpret_cast<uint32_t*>(&h2);
-        }
-        const int half = kc >> 3, c8 = kc & 7;
-        *reinterpret_cast<uint4*>(prow + half * kHalfBytes + ((c8 ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-      }
-      l_sum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-      fence_proxy_async_smem();
+      // second read of S: the exponents, written as bf16 P over S's first 64 columns
+      l_sum += whole ? row_exp_to_p<false>(srow, nvis, scale, m_ref) : row_exp_to_p<true>(srow, nvis, scale, m_ref);
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&c.p_full[pb]);
+      if (lane == 0) mbar_arrive(&c.p_full[w]);
       ++tc;
     }
     if (!ok) break;
-    // final O of the item
-    if (!mbar_wait(&c.o_full, (tc - 1) & 1, abort_flag)) {
+    vc += info.nt[0];
+    // final O_w of the item
+    if (!mbar_wait(&c.o_full[w], ic & 1, abort_flag)) {
       ok = false;
       break;
     }
+    ++ic;
     tc_fence_after();
     const bool bad = c.bad[slot] != 0;
     if (kCas) {
@@ -597,7 +675,7 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uin
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t v[64];
-        tmem_ld64_sync(tmem + lane_off + kOCol + 64 * h, v);
+        tmem_ld64_sync(tmem + lane_off + o_col + 64 * h, v);
         if (cas_live) {
 #pragma unroll
           for (int q = 0; q < 16; ++q)
@@ -613,7 +691,7 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uin
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&c.o_free);
+        mbar_arrive(&c.o_free[w]);
         mbar_arrive(&c.item_empty[slot]);
       }
       continue;
@@ -622,25 +700,25 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uin
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       uint32_t v[64];
-      tmem_ld64_sync(tmem + lane_off + kOCol + 64 * h, v);
+      tmem_ld64_sync(tmem + lane_off + o_col + 64 * h, v);
       if (row_out) {
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch) {
-          uint32_t w[4];
+          uint32_t wv[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(v[8 * ch + 2 * q]) * inv,
                                                       __uint_as_float(v[8 * ch + 2 * q + 1]) * inv);
-            w[q] = *reinterpret_cast<uint32_t*>(&h2);
+            wv[q] = *reinterpret_cast<uint32_t*>(&h2);
           }
-          reinterpret_cast<uint4*>(orow)[8 * h + ch] = make_uint4(w[0], w[1], w[2], w[3]);
+          reinterpret_cast<uint4*>(orow)[8 * h + ch] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
         }
       }
     }
     tc_fence_before();
     __syncwarp();
     if (lane == 0) {
-      mbar_arrive(&c.o_free);
+      mbar_arrive(&c.o_free[w]);
       mbar_arrive(&c.item_empty[slot]);
     }
   }
@@ -655,10 +733,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* base = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  uint8_t* qbuf = base;
-  uint8_t* stages = qbuf + kTileBytes;
-  uint8_t* pbuf = stages + kStages * kStageBytes;
-  Ctl& c = *reinterpret_cast<Ctl*>(pbuf + 2 * kTileBytes);
+  uint8_t* qbuf = base;                          // Q tiles 0 and 1
+  uint8_t* stages = qbuf + 2 * kTileBytes;
+  Ctl& c = *reinterpret_cast<Ctl*>(stages + kStages * kStageBytes);
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -667,19 +744,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       mbar_init(&c.vfull[s], 1);
       mbar_init(&c.vempty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&c.s_full[b], 1);
-      mbar_init(&c.s_free[b], 4);
-      mbar_init(&c.p_full[b], 4);
-      mbar_init(&c.p_free[b], 1);
+    for (int w = 0; w < 2; ++w) {
+      mbar_init(&c.s_full[w], 1);
+      mbar_init(&c.p_full[w], 4);
+      mbar_init(&c.o_full[w], 1);
+      mbar_init(&c.o_free[w], 4);
+      mbar_init(&c.q_full[w], kCas ? 4 : 1);  // cascade: the tile's four softmax warps gather Q
+      mbar_init(&c.q_free[w], 1);
     }
-    mbar_init(&c.o_full, 1);
-    mbar_init(&c.o_free, 4);
-    mbar_init(&c.q_full, kCas ? 4 : 1);  // cascade: the four softmax warps gather Q
-    mbar_init(&c.q_free, 1);
     for (int s = 0; s < kRing; ++s) {
       mbar_init(&c.item_full[s], 1);
-      mbar_init(&c.item_empty[s], 5);
+      mbar_init(&c.item_empty[s], 9);  // the MMA warp and the eight softmax warps
     }
     mbar_init(&c.drain, 1);
     c.abort_flag = 0;
@@ -694,8 +769,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   tc_fence_after();
   const uint32_t tmem = c.tmem_base;
   if (warp == 0) producer_warp<kCas>(P, &qmap, &kmap, &vmap, c, qbuf, stages);
-  else if (warp == 1) mma_warp(P, c, qbuf, stages, pbuf, tmem);
-  else softmax_warps<kCas>(P, c, qbuf, stages, pbuf, tmem);
+  else if (warp == 1) mma_warp(P, c, qbuf, stages, tmem);
+  else softmax_warps<kCas>(P, c, qbuf, stages, tmem);
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {

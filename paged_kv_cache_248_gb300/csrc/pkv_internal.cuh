@@ -20,6 +20,7 @@ enum : uint32_t {
 };
 
 constexpr int kTileKeys = 128;       // keys per tensor-core tile (8 blocks)
+constexpr int kPrefillTilesPerItem = 2;  // query tiles of one prefill work item (sharing K/V)
 constexpr int kSplitKeys = 1024;     // decode key-split length (a multiple of kTileKeys)
 constexpr int kNoSplitKeys = 2048;   // decode contexts up to this length are never split
 
@@ -181,7 +182,7 @@ struct PlanArgs {
   int32_t max_blocks;
   int64_t max_seq_len;
   int32_t split_keys;
-  int32_t rows_per_tile;
+  int32_t rows_per_tile;  // query tokens per prefill item
   int32_t* counters;
   int32_t* dec_prefix;
   int32_t* pre_prefix;
@@ -191,7 +192,7 @@ struct PlanArgs {
   // shared-prefix groups (cas.num_groups == 0: none)
   const int32_t* bt = nullptr;
   CascadeArgs cas{};
-  int32_t cas_rows = 0;  // member requests per cascade tile
+  int32_t cas_rows = 0;  // member requests per cascade item
   int32_t* seq_prefix = nullptr;
   int32_t* seq_entry = nullptr;
   int32_t* member_ok = nullptr;
