@@ -51,10 +51,10 @@ namespace pkv {
 namespace {
 
 constexpr int kThreads = 320;
-constexpr int kStages = 2;
+constexpr int kKStages = 2;               // K tiles in flight
+constexpr int kVStages = 3;               // V tiles in flight (a V tile is needed later than its K)
 constexpr int kHalfBytes = 16384;          // 128 rows x 128 B
 constexpr int kTileBytes = 2 * kHalfBytes;  // 128 x 128 bf16, K-major, two 64-column halves
-constexpr int kStageBytes = 2 * kTileBytes; // K tile + V tile
 constexpr int kRing = 4;
 constexpr uint32_t kTmemCols = 512;         // S_0, S_1 (cols 0, 128; P_w over S_w's first 64), O_0, O_1 (256, 384)
 constexpr uint32_t kOCol = 256;
@@ -73,9 +73,9 @@ struct alignas(16) PItem {
 };
 
 struct Ctl {
-  // K and V of a stage have their own barriers: a K tile is released when the S MMAs
-  // of both query tiles have read it, a V tile when both P V MMAs have
-  uint64_t kfull[kStages], kempty[kStages], vfull[kStages], vempty[kStages];
+  // K and V tiles have rings of their own: a K tile is released when the S MMAs of
+  // both query tiles have read it, a V tile when both P V MMAs have
+  uint64_t kfull[kKStages], kempty[kKStages], vfull[kVStages], vempty[kVStages];
   uint64_t s_full[2], p_full[2], o_full[2], o_free[2];  // per query tile
   uint64_t q_full[2], q_free[2];
   uint64_t item_full[kRing], item_empty[kRing];
@@ -86,7 +86,7 @@ struct Ctl {
   int abort_flag;
 };
 
-constexpr int kSmemBytes = 2 * kTileBytes /*Q x2*/ + kStages * kStageBytes + static_cast<int>(sizeof(Ctl)) + 1024;
+constexpr int kSmemBytes = (2 /*Q*/ + kKStages + kVStages) * kTileBytes + static_cast<int>(sizeof(Ctl)) + 1024;
 static_assert(kSmemBytes <= 232448, "prefill shared memory");
 
 struct PrefillParams {
@@ -277,7 +277,7 @@ __device__ PItem make_cas_item(const PrefillParams& P, int idx, int total) {
 // ------------------------------------------------------------------ producer warp
 template <bool kCas>
 __device__ void producer_warp(const PrefillParams& P, const CUtensorMap* qmap, const CUtensorMap* kmap,
-                              const CUtensorMap* vmap, Ctl& c, uint8_t* qbuf, uint8_t* stages) {
+                              const CUtensorMap* vmap, Ctl& c, uint8_t* qbuf, uint8_t* kbuf, uint8_t* vbuf) {
   const int lane = threadIdx.x & 31;
   const int total = kCas ? P.cas_prefix[P.cas_groups] : P.pre_prefix[P.num_seqs];
   volatile int* abort_flag = &c.abort_flag;
@@ -324,26 +324,11 @@ __device__ void producer_warp(const PrefillParams& P, const CUtensorMap* qmap, c
     }
     const int32_t* btrow = kCas ? P.cas_tables + static_cast<int64_t>(info.seq) * P.cas_max_blocks
                                 : P.bt + static_cast<int64_t>(info.seq) * P.max_blocks;
-    // V of tile j - 1 into its stage once that stage's previous P V MMAs are done
-    auto load_v = [&](int id, int nblk) -> bool {
-      const int st = tv % kStages;
-      if (!mbar_wait(&c.vempty[st], ((tv / kStages) & 1) ^ 1, abort_flag)) return false;
-      if (lane == 0) mbar_arrive_expect_tx(&c.vfull[st], static_cast<uint32_t>(nblk) * 4096u);
-      __syncwarp();
-      if (lane < nblk) {
-        uint8_t* s = stages + st * kStageBytes + kTileBytes + lane * 2048;
-        const int32_t row = (id * P.hkv + info.head) * kBlock;
-        tma_load_2d(s, vmap, &c.vfull[st], 0, row);
-        tma_load_2d(s + kHalfBytes, vmap, &c.vfull[st], 64, row);
-      }
-      ++tv;
-      return true;
-    };
-    // the keys of tile 0 of the item cover those of tile 1
-    int prev_id = 0, prev_nblk = 0;
+    // per key tile of the item (tile 0's keys cover tile 1's): K, then V, each into
+    // its ring once the MMAs that read the ring slot's previous tile are done
     for (int j = 0; j < info.nt[0]; ++j) {
-      const int st = tk % kStages;
-      if (!mbar_wait(&c.kempty[st], ((tk / kStages) & 1) ^ 1, abort_flag)) {
+      const int sk = tk % kKStages;
+      if (!mbar_wait(&c.kempty[sk], ((tk / kKStages) & 1) ^ 1, abort_flag)) {
         ok = false;
         break;
       }
@@ -363,31 +348,37 @@ __device__ void producer_warp(const PrefillParams& P, const CUtensorMap* qmap, c
         if (lane == 0) c.bad[slot] = 1;
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive_expect_tx(&c.kfull[st], static_cast<uint32_t>(nblk) * 4096u);
+      const int32_t row = (id * P.hkv + info.head) * kBlock;
+      if (lane == 0) mbar_arrive_expect_tx(&c.kfull[sk], static_cast<uint32_t>(nblk) * 4096u);
       __syncwarp();
       if (lane < nblk) {
-        uint8_t* s = stages + st * kStageBytes + lane * 2048;
-        const int32_t row = (id * P.hkv + info.head) * kBlock;
-        tma_load_2d(s, kmap, &c.kfull[st], 0, row);
-        tma_load_2d(s + kHalfBytes, kmap, &c.kfull[st], 64, row);
+        uint8_t* d = kbuf + sk * kTileBytes + lane * 2048;
+        tma_load_2d(d, kmap, &c.kfull[sk], 0, row);
+        tma_load_2d(d + kHalfBytes, kmap, &c.kfull[sk], 64, row);
       }
       ++tk;
-      if (j > 0 && !load_v(prev_id, prev_nblk)) {  // K runs one tile ahead of V
+      const int sv = tv % kVStages;
+      if (!mbar_wait(&c.vempty[sv], ((tv / kVStages) & 1) ^ 1, abort_flag)) {
         ok = false;
         break;
       }
-      prev_id = id;
-      prev_nblk = nblk;
+      if (lane == 0) mbar_arrive_expect_tx(&c.vfull[sv], static_cast<uint32_t>(nblk) * 4096u);
+      __syncwarp();
+      if (lane < nblk) {
+        uint8_t* d = vbuf + sv * kTileBytes + lane * 2048;
+        tma_load_2d(d, vmap, &c.vfull[sv], 0, row);
+        tma_load_2d(d + kHalfBytes, vmap, &c.vfull[sv], 64, row);
+      }
+      ++tv;
     }
-    if (ok && info.nt[0] > 0 && !load_v(prev_id, prev_nblk)) ok = false;
   }
   if (!ok && !*abort_flag && lane == 0) raise_abort(c, P.err);
   if (*abort_flag) {
     // let copies already issued land before the CTA's shared memory goes away
-    for (uint32_t cnt = tk > static_cast<uint32_t>(kStages) ? tk - kStages : 0; cnt < tk; ++cnt)
-      mbar_wait(&c.kfull[cnt % kStages], (cnt / kStages) & 1, nullptr);
-    for (uint32_t cnt = tv > static_cast<uint32_t>(kStages) ? tv - kStages : 0; cnt < tv; ++cnt)
-      mbar_wait(&c.vfull[cnt % kStages], (cnt / kStages) & 1, nullptr);
+    for (uint32_t cnt = tk > static_cast<uint32_t>(kKStages) ? tk - kKStages : 0; cnt < tk; ++cnt)
+      mbar_wait(&c.kfull[cnt % kKStages], (cnt / kKStages) & 1, nullptr);
+    for (uint32_t cnt = tv > static_cast<uint32_t>(kVStages) ? tv - kVStages : 0; cnt < tv; ++cnt)
+      mbar_wait(&c.vfull[cnt % kVStages], (cnt / kVStages) & 1, nullptr);
 #pragma unroll
     for (int w = 0; w < 2; ++w)
       if (qc[w] > 0) mbar_wait(&c.q_full[w], (qc[w] - 1) & 1, nullptr);
@@ -395,7 +386,7 @@ __device__ void producer_warp(const PrefillParams& P, const CUtensorMap* qmap, c
 }
 
 // ------------------------------------------------------------------ MMA warp
-__device__ void mma_warp(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uint8_t* stages, uint32_t tmem) {
+__device__ void mma_warp(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uint8_t* kbuf, uint8_t* vbuf, uint32_t tmem) {
   const int lane = threadIdx.x & 31;
   const uint32_t idesc_s = umma_idesc_bf16(128, 128, false, false);
   const uint32_t idesc_o = umma_idesc_bf16(128, 128, false, true);
@@ -417,14 +408,14 @@ __device__ void mma_warp(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uint8_t*
 #pragma unroll
       for (int w = 0; w < 2; ++w)
         if (ok && info.nt[w] > 0 && !mbar_wait(&c.q_full[w], qc[w] & 1, abort_flag)) ok = false;
-      // step j: P_w(j-1) V(j-1), then S_w(j) = Q_w K(j)^T, for w = 0, 1
+      // Step j: P_w(j-1) V(j-1), then S_w(j) = Q_w K(j)^T, for w = 0, 1.  An MMA issue
+      // returns only as the tensor core takes it in, so the MMAs are issued back to back:
+      // the only wait between the last MMA of one step and the first of the next is for
+      // P_0; the K/V waits and the ring releases sit right after an MMA burst, where the
+      // tensor core still has queued work.  Ring releases are one step late: K(j-1)'s
+      // and V(j-2)'s after P_0(j-1) V(j-1), V(nt0-1)'s after the item.
       for (int j = 0; j <= nt0 && ok; ++j) {
-        const int sk = tk % kStages, sv = tv % kStages;
-        if ((j < nt0 && !mbar_wait(&c.kfull[sk], (tk / kStages) & 1, abort_flag)) ||
-            (j > 0 && !mbar_wait(&c.vfull[sv], (tv / kStages) & 1, abort_flag))) {
-          ok = false;
-          break;
-        }
+        const int sk = tk % kKStages, sv = tv % kVStages;  // K(j), V(j-1)
 #pragma unroll
         for (int w = 0; w < 2; ++w) {
           if (!ok) break;
@@ -438,22 +429,29 @@ __device__ void mma_warp(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uint8_t*
             }
             tc_fence_after();
             if (lane == 0) {
-              const uint64_t bd = umma_smem_desc(smem_u32(stages + sv * kStageBytes + kTileBytes), kHalfBytes, 1024,
-                                                 kLayout128B);
+              const uint64_t bd = umma_smem_desc(smem_u32(vbuf + sv * kTileBytes), kHalfBytes, 1024, kLayout128B);
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk)
                 umma_f16_ts(tmem + kOCol + 128 * w, tmem + 128 * w + 8 * kk, umma_desc_advance(bd, kk * 2048),
                             idesc_o, (j > 1 || kk > 0) ? 1u : 0u);
               if (j == ntw) umma_commit(&c.o_full[w]);
+              if (w == 0) {
+                if (j >= 1) umma_commit(&c.kempty[(tk - 1) % kKStages]);  // K(j-1): S_0, S_1(j-1) issued
+                if (j >= 2) umma_commit(&c.vempty[(tv - 1) % kVStages]);  // V(j-2): both P V issued
+              }
             }
             __syncwarp();
             ++pc[w];
           }
           if (j < ntw) {
+            if (w == 0 && !mbar_wait(&c.kfull[sk], (tk / kKStages) & 1, abort_flag)) {
+              ok = false;
+              break;
+            }
             tc_fence_after();
             if (lane == 0) {
               const uint64_t a = umma_smem_desc(smem_u32(qbuf + w * kTileBytes), 16, 1024, kLayout128B);
-              const uint64_t b = umma_smem_desc(smem_u32(stages + sk * kStageBytes), 16, 1024, kLayout128B);
+              const uint64_t b = umma_smem_desc(smem_u32(kbuf + sk * kTileBytes), 16, 1024, kLayout128B);
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk) {
                 const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
@@ -464,16 +462,24 @@ __device__ void mma_warp(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uint8_t*
               issued = true;
             }
             __syncwarp();
+            // V(j), read by the next step's P V, while the tensor core works on S_0(j)
+            if (w == 0) {
+              const uint32_t vn = tv + (j > 0 ? 1 : 0);
+              if (!mbar_wait(&c.vfull[vn % kVStages], (vn / kVStages) & 1, abort_flag)) {
+                ok = false;
+                break;
+              }
+            }
           }
         }
         if (!ok) break;
-        if (lane == 0) {
-          if (j < nt0) umma_commit(&c.kempty[sk]);
-          if (j > 0) umma_commit(&c.vempty[sv]);
-        }
-        __syncwarp();
         if (j < nt0) ++tk;
         if (j > 0) ++tv;
+      }
+      if (ok && nt0 > 0) {
+        // the last V tile's release; K(nt0-1)'s and V(nt0-2)'s went out in step nt0
+        if (lane == 0) umma_commit(&c.vempty[(tv - 1) % kVStages]);
+        __syncwarp();
       }
 #pragma unroll
       for (int w = 0; w < 2; ++w)
@@ -498,7 +504,7 @@ __device__ void mma_warp(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uint8_t*
 
 // ------------------------------------------------------------------ softmax warps
 template <bool kCas>
-__device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uint8_t* stages, uint32_t tmem) {
+__device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uint8_t* vbuf, uint32_t tmem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wq = warp & 3;        // TMEM lane quarter this warp may access
   const int w = (warp - 2) >> 2;  // the item's query tile this warpgroup owns
@@ -594,7 +600,7 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uin
 
     for (int j = 0; j < nt && ok; ++j) {
       const uint32_t vt = vc + j;
-      const int sv = vt % kStages;
+      const int sv = vt % kVStages;
       const int k0 = info.ks + j * kTileKeys;
       if (!mbar_wait(&c.s_full[w], tc & 1, abort_flag)) {
         ok = false;
@@ -636,13 +642,16 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uin
           m_ref = m_new;
         }
       }
-      // V of this stage has landed (also orders the producer's bad-block flag)
-      if (!mbar_wait(&c.vfull[sv], (vt / kStages) & 1, abort_flag)) {
+      // second read of S: the exponents, written as bf16 P over S's first 64 columns
+      l_sum += whole ? row_exp_to_p<false>(srow, nvis, scale, m_ref) : row_exp_to_p<true>(srow, nvis, scale, m_ref);
+      tmem_st_wait();
+      // V of this key tile has landed (also orders the producer's bad-block flag)
+      if (!mbar_wait(&c.vfull[sv], (vt / kVStages) & 1, abort_flag)) {
         ok = false;
         break;
       }
       if (w == 0 && k0 + r >= zero_from) {
-        uint8_t* vrow = stages + sv * kStageBytes + kTileBytes + r * 128;
+        uint8_t* vrow = vbuf + sv * kTileBytes + r * 128;
 #pragma unroll
         for (int c16 = 0; c16 < 8; ++c16) {
           *reinterpret_cast<uint4*>(vrow + c16 * 16) = make_uint4(0, 0, 0, 0);
@@ -650,9 +659,6 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uin
         }
         fence_proxy_async_smem();
       }
-      // second read of S: the exponents, written as bf16 P over S's first 64 columns
-      l_sum += whole ? row_exp_to_p<false>(srow, nvis, scale, m_ref) : row_exp_to_p<true>(srow, nvis, scale, m_ref);
-      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&c.p_full[w]);
@@ -734,13 +740,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* base = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   uint8_t* qbuf = base;                          // Q tiles 0 and 1
-  uint8_t* stages = qbuf + 2 * kTileBytes;
-  Ctl& c = *reinterpret_cast<Ctl*>(stages + kStages * kStageBytes);
+  uint8_t* kbuf = qbuf + 2 * kTileBytes;         // K ring
+  uint8_t* vbuf = kbuf + kKStages * kTileBytes;  // V ring
+  Ctl& c = *reinterpret_cast<Ctl*>(vbuf + kVStages * kTileBytes);
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kKStages; ++s) {
       mbar_init(&c.kfull[s], 1);
       mbar_init(&c.kempty[s], 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
       mbar_init(&c.vfull[s], 1);
       mbar_init(&c.vempty[s], 1);
     }
@@ -768,9 +777,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = c.tmem_base;
-  if (warp == 0) producer_warp<kCas>(P, &qmap, &kmap, &vmap, c, qbuf, stages);
-  else if (warp == 1) mma_warp(P, c, qbuf, stages, tmem);
-  else softmax_warps<kCas>(P, c, qbuf, stages, tmem);
+  if (warp == 0) producer_warp<kCas>(P, &qmap, &kmap, &vmap, c, qbuf, kbuf, vbuf);
+  else if (warp == 1) mma_warp(P, c, qbuf, kbuf, vbuf, tmem);
+  else softmax_warps<kCas>(P, c, qbuf, vbuf, tmem);
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
