@@ -337,9 +337,10 @@ int attention_impl(const void* q, const void* k_new, const void* v_new, const vo
     plan.vec_per_row = cache->head_dim * 2 / 16;
     plan.write_ctas = static_cast<int32_t>(want < 2 * ctx->num_sms ? want : 2 * ctx->num_sms);
   }
+  const int cas_tpi = casp ? cascade_tiles_per_item(cas.num_members, hkv, gp, cas.max_blocks, ctx->num_sms) : 1;
   if (casp) {
     plan.cas = cas;
-    plan.cas_rows = kPrefillTilesPerItem * (kTileKeys / gp);
+    plan.cas_rows = cas_tpi * (kTileKeys / gp);
     plan.seq_prefix = ws.seq_prefix;
     plan.seq_entry = ws.seq_entry;
     plan.member_ok = ws.member_ok;
@@ -348,7 +349,7 @@ int attention_impl(const void* q, const void* k_new, const void* v_new, const vo
   st = launch_plan(plan, s);
   if (st) return st;
   if (casp) {
-    st = launch_cascade_tc(a, cas, ws, ctx->num_sms, ctx->err, s);
+    st = launch_cascade_tc(a, cas, ws, ctx->num_sms, cas_tpi, ctx->err, s);
     if (st) return st;
   }
   st = launch_decode_tc(a, ws, ctx->num_sms, ctx->err, s);

@@ -107,15 +107,16 @@ struct DecodeParams {
 };
 
 // Folds one partial (running max m, sum l, accumulator o, per head) into a
-// log-sum-exp merge.
+// log-sum-exp merge.  (The exponents take the MUFU 2^x: their arguments are <= 0,
+// and -inf gives 0.)
 template <int GP>
 __device__ __forceinline__ void merge_fold(float (&M)[GP], float (&num)[GP], float (&den)[GP], const float (&ml)[2 * GP],
                                            const float (&ov)[GP]) {
 #pragma unroll
   for (int g = 0; g < GP; ++g) {
     const float m_new = fmaxf(M[g], ml[2 * g]);
-    const float a = exp2f(M[g] - m_new);
-    const float b = exp2f(ml[2 * g] - m_new);
+    const float a = ex2_approx(M[g] - m_new);
+    const float b = ex2_approx(ml[2 * g] - m_new);
     den[g] = fmaf(den[g], a, ml[2 * g + 1] * b);
     num[g] = fmaf(num[g], a, ov[g] * b);
     M[g] = m_new;
@@ -554,8 +555,8 @@ __device__ void softmax_warps(const DecodeParams& P, Ctl& c, uint8_t* stages, ui
       for (int g = 0; g < GP; ++g) {
         const float mt = fmaxf(fmaxf(c.red[rb][0][g], c.red[rb][1][g]), fmaxf(c.red[rb][2][g], c.red[rb][3][g]));
         const float m_new = fmaxf(m_run[g], mt);
-        alpha[g] = exp2f(m_run[g] - m_new);
-        p[g] = exp2f(x[g] - m_new);
+        alpha[g] = ex2_approx(m_run[g] - m_new);  // arguments <= 0; -inf gives 0
+        p[g] = ex2_approx(x[g] - m_new);
         l_run[g] = fmaf(l_run[g], alpha[g], p[g]);
         m_run[g] = m_new;
       }
@@ -633,10 +634,12 @@ __device__ void softmax_warps(const DecodeParams& P, Ctl& c, uint8_t* stages, ui
     const int64_t trow = info.trow;
     const int64_t unit = static_cast<int64_t>(info.seq) * P.hkv + info.head;
     __nv_bfloat16* orow = P.out + (trow * P.hq + static_cast<int64_t>(info.head) * G) * 128 + r;
+    // (the fast division is exact enough for a bf16 result; every denominator is at
+    // least 1, the term of the maximum itself)
     if (info.nsplit == 1 && !info.member) {
 #pragma unroll
       for (int g = 0; g < GP; ++g)
-        if (g < G) orow[g * 128] = __float2bfloat16_rn(bad ? 0.f : acc[g] / lt[g]);
+        if (g < G) orow[g * 128] = __float2bfloat16_rn(bad ? 0.f : __fdividef(acc[g], lt[g]));
     } else if (fold_prefix) {
       // the prefix partials in split order, then this item: the split merge's order
       float M[GP], num[GP], den[GP];
@@ -683,7 +686,7 @@ __device__ void softmax_warps(const DecodeParams& P, Ctl& c, uint8_t* stages, ui
       const bool any_bad = bad || __ldg(P.unit_bad + unit) != 0;
 #pragma unroll
       for (int g = 0; g < GP; ++g)
-        if (g < G) orow[g * 128] = __float2bfloat16_rn(any_bad ? 0.f : num[g] / den[g]);
+        if (g < G) orow[g * 128] = __float2bfloat16_rn(any_bad ? 0.f : __fdividef(num[g], den[g]));
     } else {
       // partials: accumulators [item][d][GP] (one float4 run per thread), max and sum
       // [item][GP][2]; the merge kernel that runs after this one combines them
@@ -856,7 +859,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeParams P) {
     __nv_bfloat16* orow = P.out + (trow * P.hq + static_cast<int64_t>(h) * P.group) * 128 + d;
 #pragma unroll
     for (int g = 0; g < GP; ++g)
-      if (g < P.group) orow[g * 128] = __float2bfloat16_rn(bad ? 0.f : num[g] / den[g]);
+      if (g < P.group) orow[g * 128] = __float2bfloat16_rn(bad ? 0.f : __fdividef(num[g], den[g]));
   }
 }
 

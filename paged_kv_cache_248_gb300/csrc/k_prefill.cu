@@ -113,6 +113,7 @@ struct PrefillParams {
   float* cas_ml;
   int32_t* unit_bad;
   int32_t cas_max_blocks, cas_groups, cas_np_max;
+  int32_t cas_tiles;  // query tiles per cascade item: 2, or 1 (tile 1 of every item absent)
 };
 
 // The extremum of one S row of 128 raw scores from TMEM (taddr: the row's first
@@ -254,14 +255,14 @@ __device__ PItem make_cas_item(const PrefillParams& P, int idx, int total) {
   const int local = idx - P.cas_prefix[lo];
   r.split = local % np;
   r.head = (local / np) % P.hkv;
-  const int pq = local / np / P.hkv;
+  const int pq = local / np / P.hkv;  // the item's tile group of member entries
   r.ks = r.split * kCascadeSplitKeys;
   const int kend = min(pb * kBlock, r.ks + kCascadeSplitKeys);
   const int nt = (kend - r.ks + kTileKeys - 1) / kTileKeys;
   for (int w = 0; w < 2; ++w) {
-    r.qt[w] = 2 * pq + w;
+    r.qt[w] = P.cas_tiles * pq + w;
     r.j0[w] = e0 + r.qt[w] * P.rows_q;
-    r.nq[w] = min(P.rows_q, e1 - r.j0[w]);
+    r.nq[w] = w < P.cas_tiles ? min(P.rows_q, e1 - r.j0[w]) : 0;
     if (r.nq[w] > 0) {
       r.kend[w] = kend;
       r.nt[w] = nt;
@@ -834,7 +835,8 @@ int launch_prefill_tc(const AttnArgs& a, const Workspace& ws, int num_sms, uint3
   return cuda_status(cudaGetLastError());
 }
 
-int launch_cascade_tc(const AttnArgs& a, const CascadeArgs& cas, const Workspace& ws, int num_sms, uint32_t* err,
+int launch_cascade_tc(const AttnArgs& a, const CascadeArgs& cas, const Workspace& ws, int num_sms, int tiles_per_item,
+                      uint32_t* err,
                       cudaStream_t s) {
   const int hkv = a.cache.num_kv_heads;
   const int group = a.num_q_heads / hkv;
@@ -877,6 +879,7 @@ int launch_cascade_tc(const AttnArgs& a, const CascadeArgs& cas, const Workspace
   p.cas_max_blocks = cas.max_blocks;
   p.cas_groups = cas.num_groups;
   p.cas_np_max = ws.cas_np_max;
+  p.cas_tiles = tiles_per_item;
   TraceScope trace(kTraceCascade, s);
   cudaError_t e =
       cudaFuncSetAttribute(prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);

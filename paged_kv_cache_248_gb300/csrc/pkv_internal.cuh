@@ -212,7 +212,15 @@ int launch_plan(const PlanArgs& p, cudaStream_t s);
 int launch_decode_tc(const AttnArgs& a, const Workspace& ws, int num_sms, uint32_t* err, cudaStream_t s);
 // Attends the member decodes of every prefix group to the group's shared prefix,
 // writing per-split partials for the merge (after launch_plan, before launch_decode_tc).
-int launch_cascade_tc(const AttnArgs& a, const CascadeArgs& cas, const Workspace& ws, int num_sms, uint32_t* err,
+// Query tiles per cascade item: pairs (sharing each K/V tile) when they still give
+// every SM an item, single tiles otherwise.  A function of the hint sizes only; how
+// member rows are grouped into tiles does not change any row's result.
+inline int cascade_tiles_per_item(int64_t num_members, int hkv, int gp, int64_t max_prefix_blocks, int num_sms) {
+  const int64_t rows = kTileKeys / gp;
+  const int64_t pairs = (num_members + 2 * rows - 1) / (2 * rows) * hkv * cascade_splits(max_prefix_blocks * kBlock);
+  return pairs >= num_sms ? 2 : 1;
+}
+int launch_cascade_tc(const AttnArgs& a, const CascadeArgs& cas, const Workspace& ws, int num_sms, int tiles_per_item, uint32_t* err,
                       cudaStream_t s);
 int launch_prefill_tc(const AttnArgs& a, const Workspace& ws, int num_sms, uint32_t* err, cudaStream_t s);
 int encode_tensor_map_3d(CUtensorMap* map, const void* base, const uint64_t dims[3], const uint64_t strides[2],

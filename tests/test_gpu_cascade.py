@@ -100,6 +100,21 @@ def test_long_prefixes_fold_every_prefix_split(pkv, group):
     compare(cas, ref, "bf16", w.name)
 
 
+def test_enough_members_for_paired_member_tiles(pkv):
+    # 70 members of a 4800-key prefix (10 prefix splits) over 8 kv heads give 2 x 8 x 10
+    # items of two 32-member tiles each: at least one per SM on a 152-SM part, so the
+    # cascade pairs its member tiles (fewer items would leave SMs idle and use one tile)
+    w, hints = wl.shared_prefix_case(18, prefix_blocks=(300,), members=(70,), group=4, num_kv_heads=8,
+                                     max_suffix=40, bystanders=2, bad_hints=False)
+    t_cpu = w.make_tensors("cpu")
+    t = {k: v.cuda() for k, v in t_cpu.items()}
+    _, cas, st = run_both(pkv, w, hints, t)
+    assert st == 0
+    ref = oracle.attention(bits(t_cpu["q"]), bits(t_cpu["k_cache"]), bits(t_cpu["v_cache"]), w.block_tables,
+                           w.seq_lens, w.query_start_loc, w.scale)
+    compare(cas, ref, "bf16", w.name)
+
+
 def test_malformed_hints_fall_back(pkv):
     w, hints = wl.shared_prefix_case(13, bad_hints=True)
     t_cpu = w.make_tensors("cpu")
