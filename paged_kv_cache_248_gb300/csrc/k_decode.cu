@@ -776,11 +776,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
 
 // ------------------------------------------------------------------ split merge
 // Combines the partials of every (request, kv head) that was cut into several key
-// splits -- the planner lists those requests -- by a log-sum-exp merge in split
-// order, one CTA per unit (thread d = head element), one pass with a running
-// maximum and float4 loads.  Requests of one split were written by the decode kernel.
-// A shared-prefix member's prefix partials (the cascade kernel's, stored [GP][128]
-// per split) come first, then its own key splits.
+// splits -- the planner lists those requests -- by a log-sum-exp merge, one CTA per
+// unit.  A shared-prefix member's prefix partials (the cascade kernel's, stored
+// [GP][128] per split) come first, then its own key splits: that list is cut into
+// kMergeGroups contiguous runs, each folded in order by one group of 128 threads
+// (thread d = head element, float4 loads), and the runs' results are folded in run
+// order -- a fixed tree, so the result does not depend on scheduling.  Requests of
+// one split were written by the decode kernel.
+constexpr int kMergeGroups = 4;
 struct MergeParams {
   __nv_bfloat16* out;
   const int32_t* counters;
@@ -799,8 +802,9 @@ struct MergeParams {
 };
 
 template <int GP>
-__global__ void __launch_bounds__(128) merge_kernel(const MergeParams P) {
-  const int d = threadIdx.x;
+__global__ void __launch_bounds__(128 * kMergeGroups) merge_kernel(const MergeParams P) {
+  __shared__ float xfer[GP][3][128];  // one run's (max, sum, accumulator) handed to run 0
+  const int d = threadIdx.x % 128, run = threadIdx.x / 128;
   const int64_t n_units = static_cast<int64_t>(P.counters[kMergeCountSlot]) * P.hkv;
   for (int64_t e = blockIdx.x; e < n_units; e += gridDim.x) {
     const int i = __ldg(P.merge_list + e / P.hkv), h = static_cast<int>(e % P.hkv);
@@ -810,6 +814,12 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeParams P) {
     const int pre = P.seq_prefix ? __ldg(P.seq_prefix + i) : 0;
     if (ns <= 1) continue;  // (a member of one split was finished by the decode kernel)
     const int64_t base = base_i + static_cast<int64_t>(h) * ns;
+    const int npre = pre > 0 ? static_cast<int>(cascade_splits(pre)) : 0;
+    const int64_t cbase = pre > 0 ? (static_cast<int64_t>(__ldg(P.seq_entry + i)) * P.hkv + h) * P.cas_np_max : 0;
+    // this run: entries [e0, e1) of prefix partials then splits
+    const int n_all = npre + ns;
+    const int per = (n_all + kMergeGroups - 1) / kMergeGroups;
+    const int e0 = min(n_all, run * per), e1 = min(n_all, e0 + per);
     float M[GP], num[GP], den[GP];
 #pragma unroll
     for (int g = 0; g < GP; ++g) {
@@ -817,49 +827,72 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeParams P) {
       num[g] = 0.f;
       den[g] = 0.f;
     }
-    if (pre > 0) {
-      const int npre = static_cast<int>(cascade_splits(pre));
-      const int64_t cbase = (static_cast<int64_t>(__ldg(P.seq_entry + i)) * P.hkv + h) * P.cas_np_max;
-      for (int s = 0; s < npre; ++s) {
-        const float* ml_p = P.cas_ml + (cbase + s) * GP * 2;
-        const float* o_p = P.cas_o + (cbase + s) * GP * 128 + d;
-        float ml[2 * GP], ov[GP];
-#pragma unroll
-        for (int k = 0; k < 2 * GP; ++k) ml[k] = __ldg(ml_p + k);
-#pragma unroll
-        for (int g = 0; g < GP; ++g) ov[g] = __ldg(o_p + g * 128);
-        merge_fold<GP>(M, num, den, ml, ov);
-      }
-    }
-#pragma unroll 4
-    for (int s = 0; s < ns; ++s) {
-      const float4* ml4 = reinterpret_cast<const float4*>(P.part_ml + (base + s) * GP * 2);
-      const float4* o4 = reinterpret_cast<const float4*>(P.part_o + ((base + s) * 128 + d) * GP);
+    for (int k = e0; k < min(e1, npre); ++k) {
+      const float* ml_p = P.cas_ml + (cbase + k) * GP * 2;
+      const float* o_p = P.cas_o + (cbase + k) * GP * 128 + d;
       float ml[2 * GP], ov[GP];
 #pragma unroll
-      for (int k = 0; k < GP / 2; ++k) {
-        const float4 t = __ldg(ml4 + k);
-        ml[4 * k] = t.x;
-        ml[4 * k + 1] = t.y;
-        ml[4 * k + 2] = t.z;
-        ml[4 * k + 3] = t.w;
+      for (int q = 0; q < 2 * GP; ++q) ml[q] = __ldg(ml_p + q);
+#pragma unroll
+      for (int g = 0; g < GP; ++g) ov[g] = __ldg(o_p + g * 128);
+      merge_fold<GP>(M, num, den, ml, ov);
+    }
+#pragma unroll 4
+    for (int k = max(e0, npre); k < e1; ++k) {
+      const int64_t it = base + (k - npre);
+      const float4* ml4 = reinterpret_cast<const float4*>(P.part_ml + it * GP * 2);
+      const float4* o4 = reinterpret_cast<const float4*>(P.part_o + (it * 128 + d) * GP);
+      float ml[2 * GP], ov[GP];
+#pragma unroll
+      for (int q = 0; q < GP / 2; ++q) {
+        const float4 t = __ldg(ml4 + q);
+        ml[4 * q] = t.x;
+        ml[4 * q + 1] = t.y;
+        ml[4 * q + 2] = t.z;
+        ml[4 * q + 3] = t.w;
       }
 #pragma unroll
-      for (int k = 0; k < GP / 4; ++k) {
-        const float4 t = __ldg(o4 + k);
-        ov[4 * k] = t.x;
-        ov[4 * k + 1] = t.y;
-        ov[4 * k + 2] = t.z;
-        ov[4 * k + 3] = t.w;
+      for (int q = 0; q < GP / 4; ++q) {
+        const float4 t = __ldg(o4 + q);
+        ov[4 * q] = t.x;
+        ov[4 * q + 1] = t.y;
+        ov[4 * q + 2] = t.z;
+        ov[4 * q + 3] = t.w;
       }
       merge_fold<GP>(M, num, den, ml, ov);
     }
-    const bool bad = __ldg(P.unit_bad + u) != 0;
-    const int64_t trow = __ldg(P.qsl + i);
-    __nv_bfloat16* orow = P.out + (trow * P.hq + static_cast<int64_t>(h) * P.group) * 128 + d;
+    // runs 1.. hand their results to run 0, which folds them in run order (run 0's
+    // list is never empty, so its maximum is finite; an empty run folds as nothing)
+    for (int k = 1; k < kMergeGroups; ++k) {
+      __syncthreads();
+      if (run == k) {
 #pragma unroll
-    for (int g = 0; g < GP; ++g)
-      if (g < P.group) orow[g * 128] = __float2bfloat16_rn(bad ? 0.f : __fdividef(num[g], den[g]));
+        for (int g = 0; g < GP; ++g) {
+          xfer[g][0][d] = M[g];
+          xfer[g][1][d] = den[g];
+          xfer[g][2][d] = num[g];
+        }
+      }
+      __syncthreads();
+      if (run == 0 && k * per < n_all) {
+        float ml[2 * GP], ov[GP];
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
+          ml[2 * g] = xfer[g][0][d];
+          ml[2 * g + 1] = xfer[g][1][d];
+          ov[g] = xfer[g][2][d];
+        }
+        merge_fold<GP>(M, num, den, ml, ov);
+      }
+    }
+    if (run == 0) {
+      const bool bad = __ldg(P.unit_bad + u) != 0;
+      const int64_t trow = __ldg(P.qsl + i);
+      __nv_bfloat16* orow = P.out + (trow * P.hq + static_cast<int64_t>(h) * P.group) * 128 + d;
+#pragma unroll
+      for (int g = 0; g < GP; ++g)
+        if (g < P.group) orow[g * 128] = __float2bfloat16_rn(bad ? 0.f : __fdividef(num[g], den[g]));
+    }
   }
 }
 
@@ -886,7 +919,7 @@ int launch_gp(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& v
   const int64_t cap = static_cast<int64_t>(grid) * 4;
   const int mgrid = static_cast<int>(n_units < cap ? n_units : cap);
   TraceScope trace(kTraceMerge, s);
-  merge_kernel<GP><<<mgrid, 128, 0, s>>>(m);
+  merge_kernel<GP><<<mgrid, 128 * kMergeGroups, 0, s>>>(m);
   return cuda_status(cudaGetLastError());
 }
 

@@ -267,6 +267,41 @@ def test_repeated_calls_match_oracle_and_each_other(pkv, seed, group, hkv):
         assert torch.equal(o, outs[0])
 
 
+def test_split_decodes_repeat_bitwise(pkv):
+    # Requests of 2 to 9 key splits next to unsplit ones: the split that finishes last
+    # merges its (request, kv head), and which split that is changes from call to call;
+    # the merge runs in split order all the same, so the rows must be identical.
+    lens = [2049, 3000, 4096, 5121, 9000, 300, 2048, 7777]
+    w = wl.sized_case(43, lens, [1] * len(lens), 16, 4, 128, "bf16")
+    t_cpu = w.make_tensors("cpu")
+    t = {k: v.cuda() for k, v in t_cpu.items()}
+    outs = [_attention_only(pkv, w, t) for _ in range(6)]
+    assert pkv.pkv_get_last_error() == 0
+    ref = oracle.attention(bits(t_cpu["q"]), bits(t_cpu["k_cache"]), bits(t_cpu["v_cache"]), w.block_tables,
+                           w.seq_lens, w.query_start_loc, w.scale)
+    for o in outs:
+        compare(o, ref, "bf16", w.name)
+        assert torch.equal(o, outs[0])
+
+
+def test_bad_block_in_one_split_zeroes_the_merged_row(pkv):
+    # a bad block id in the third split of a 5121-key request: that request's merged
+    # rows are zero, every other request is unaffected
+    w = wl.sized_case(44, [5121, 3000, 600], [1, 1, 1], 8, 2, 128, "bf16")
+    t_cpu = w.make_tensors("cpu")
+    t = {k: v.cuda() for k, v in t_cpu.items()}
+    bt = w.block_tables.copy()
+    bt[0, 2100 // 16] = w.num_blocks + 3
+    m = to_gpu_meta(w, bt)
+    out = pkv.paged_attention(t["q"], t["k_cache"], t["v_cache"], m["block_tables"], m["seq_lens"],
+                              m["query_start_loc"], w.scale, w.max_query_len, w.max_seq_len)
+    assert pkv.pkv_get_last_error() == pkv.PKV_ERR_INDEX
+    assert torch.count_nonzero(out[0]) == 0
+    ref = oracle.attention(bits(t_cpu["q"]), bits(t_cpu["k_cache"]), bits(t_cpu["v_cache"]), w.block_tables,
+                           w.seq_lens, w.query_start_loc, w.scale, rows=np.array([1, 2], np.int64))
+    compare(out[1:3], ref, "bf16")
+
+
 # --------------------------------------------------------------------------- device errors
 
 def test_bad_block_id_zeroes_only_that_request(pkv):
