@@ -116,6 +116,39 @@ struct PrefillParams {
   int32_t cas_tiles;  // query tiles per cascade item: 2, or 1 (tile 1 of every item absent)
 };
 
+// Three-input maximum / minimum (one instruction on sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+  float r;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+// (ya, yb) = (xa, xb) * s + t and (a0, a1) += (b0, b1): one packed fp32x2 instruction
+// each, rounded like the scalar forms lane by lane.
+__device__ __forceinline__ void ffma2(float& ya, float& yb, float xa, float xb, float s, float t) {
+  asm("{\n\t.reg .b64 x, y, m, c;\n\t"
+      "mov.b64 x, {%2, %3};\n\t"
+      "mov.b64 m, {%4, %4};\n\t"
+      "mov.b64 c, {%5, %5};\n\t"
+      "fma.rn.f32x2 y, x, m, c;\n\t"
+      "mov.b64 {%0, %1}, y;\n\t}"
+      : "=f"(ya), "=f"(yb)
+      : "f"(xa), "f"(xb), "f"(s), "f"(t));
+}
+__device__ __forceinline__ void fadd2(float& a0, float& a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 a, b;\n\t"
+      "mov.b64 a, {%0, %1};\n\t"
+      "mov.b64 b, {%2, %3};\n\t"
+      "add.rn.f32x2 a, a, b;\n\t"
+      "mov.b64 {%0, %1}, a;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(b0), "f"(b1));
+}
+
 // The extremum of one S row of 128 raw scores from TMEM (taddr: the row's first
 // column): the maximum, or for kPos false the minimum (a negative scale turns it into
 // the maximum of scale * s).  With kMask, keys from nvis on do not count.  Each
@@ -135,9 +168,11 @@ __device__ __forceinline__ float row_extremum(uint32_t taddr, int nvis) {
     uint32_t(&nxt)[32] = (h & 1) ? a : b;
     if (h < 3) tmem_ld32_issue(taddr + 32 * (h + 1), nxt);
 #pragma unroll
-    for (int k = 0; k < 32; ++k) {
-      const float x = (!kMask || 32 * h + k < nvis) ? __uint_as_float(cur[k]) : hidden;
-      mx[k & 7] = kPos ? fmaxf(mx[k & 7], x) : fminf(mx[k & 7], x);
+    for (int k = 0; k < 32; k += 2) {  // two scores per three-input instruction
+      const float xa = (!kMask || 32 * h + k < nvis) ? __uint_as_float(cur[k]) : hidden;
+      const float xb = (!kMask || 32 * h + k + 1 < nvis) ? __uint_as_float(cur[k + 1]) : hidden;
+      const int c = (k >> 1) & 7;
+      mx[c] = kPos ? fmax3(mx[c], xa, xb) : fmin3(mx[c], xa, xb);
     }
     if (h < 3) tmem_ld32_wait(nxt);
   }
@@ -152,7 +187,7 @@ __device__ __forceinline__ float row_extremum(uint32_t taddr, int nvis) {
 template <bool kMask>
 __device__ __forceinline__ float row_exp_to_p(uint32_t taddr, int nvis, float scale, float m_ref) {
   const float hidden = scale >= 0.f ? -INFINITY : INFINITY;  // raw score that scales to -inf
-  float ls[4] = {0.f, 0.f, 0.f, 0.f};  // the row sum in four independent parts
+  float ls[4] = {0.f, 0.f, 0.f, 0.f};  // the row sum in four independent parts (two packed pairs)
   uint32_t a[32], b[32];
   tmem_ld32_issue(taddr, a);
   tmem_ld32_wait(a);
@@ -167,9 +202,12 @@ __device__ __forceinline__ float row_exp_to_p(uint32_t taddr, int nvis, float sc
       const int k = 32 * h + 2 * q;
       const float xa = (!kMask || k < nvis) ? __uint_as_float(cur[2 * q]) : hidden;
       const float xb = (!kMask || k + 1 < nvis) ? __uint_as_float(cur[2 * q + 1]) : hidden;
-      const float pa = ex2_approx(fmaf(xa, scale, -m_ref));
-      const float pb = ex2_approx(fmaf(xb, scale, -m_ref));
-      ls[q & 3] += pa + pb;
+      float ya, yb;
+      ffma2(ya, yb, xa, xb, scale, -m_ref);
+      const float pa = ex2_approx(ya);
+      const float pb = ex2_approx(yb);
+      if (q & 1) fadd2(ls[2], ls[3], pa, pb);
+      else fadd2(ls[0], ls[1], pa, pb);
       __nv_bfloat162 h2 = __floats2bfloat162_rn(pa, pb);
       pw[q] = *reinterpret_cast<uint32_t*>(&h2);
     }
