@@ -73,7 +73,7 @@ int ensure_workspace(DeviceCtx* ctx, size_t bytes, cudaStream_t stream) {
 }
 
 size_t layout_workspace(void* base, int32_t num_seqs, int32_t hkv, int32_t group, int32_t head_dim,
-                        int64_t max_dec_items, Workspace* ws, const CascadeArgs* cas) {
+                        int64_t max_dec_items, int64_t max_pre_units, Workspace* ws, const CascadeArgs* cas) {
   size_t off = 0;
   auto take = [&](size_t bytes) -> void* {
     void* p = base ? static_cast<char*>(base) + off : nullptr;
@@ -84,6 +84,7 @@ size_t layout_workspace(void* base, int32_t num_seqs, int32_t hkv, int32_t group
   w.counters = static_cast<int32_t*>(take(kNumQueueCounters * sizeof(int32_t)));
   w.dec_prefix = static_cast<int32_t*>(take((static_cast<size_t>(num_seqs) + 1) * sizeof(int32_t)));
   w.pre_prefix = static_cast<int32_t*>(take((static_cast<size_t>(num_seqs) + 1) * sizeof(int32_t)));
+  w.pre_order = static_cast<int32_t*>(take(static_cast<size_t>(max_pre_units) * sizeof(int32_t)));
   w.unit_bad = static_cast<int32_t*>(take(static_cast<size_t>(num_seqs) * hkv * sizeof(int32_t)));
   w.merge_list = static_cast<int32_t*>(take(static_cast<size_t>(num_seqs) * sizeof(int32_t)));
   w.part_ml = static_cast<float*>(take(static_cast<size_t>(max_dec_items) * group * 2 * sizeof(float)));
@@ -316,15 +317,20 @@ int attention_impl(const void* q, const void* k_new, const void* v_new, const vo
     if (slots * gp >= (int64_t(1) << 31)) return PKV_ERR_UNSUPPORTED;
   }
   const CascadeArgs* casp = cas.num_groups > 0 ? &cas : nullptr;
-  const size_t need = layout_workspace(nullptr, num_seqs, hkv, gp, cache->head_dim, max_dec_items, nullptr, casp);
+  const int64_t max_pre_units = max_prefill_units(num_tokens, num_seqs, gp);
+  const size_t need =
+      layout_workspace(nullptr, num_seqs, hkv, gp, cache->head_dim, max_dec_items, max_pre_units, nullptr, casp);
   st = ensure_workspace(ctx, need, s);
   if (st) return st;
   Workspace ws;
-  layout_workspace(ctx->ws, num_seqs, hkv, gp, cache->head_dim, max_dec_items, &ws, casp);
+  layout_workspace(ctx->ws, num_seqs, hkv, gp, cache->head_dim, max_dec_items, max_pre_units, &ws, casp);
   PlanArgs plan{seq_lens, query_start_loc, num_seqs, num_tokens, hkv, max_blocks_per_seq, max_seq_len,
                 kSplitKeys, kPrefillTilesPerItem * (kTileKeys / gp), ws.counters, ws.dec_prefix, ws.pre_prefix, ws.unit_bad,
                 ws.merge_list, ctx->err};
   plan.bt = block_tables;
+  plan.pre_order = ws.pre_order;
+  plan.max_pre_units = max_pre_units;
+  plan.rows_q = kTileKeys / gp;
   if (write) {
     const int64_t warps_per_cta = 1024 / 32;
     const int64_t want = (num_tokens + warps_per_cta - 1) / warps_per_cta;

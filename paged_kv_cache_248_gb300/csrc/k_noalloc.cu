@@ -89,7 +89,9 @@ extern "C" PKV_API int paged_attention_noalloc(const void* q, const void* k_cach
   const int64_t max_splits = (static_cast<int64_t>(max_seq_len) + kSplitKeys - 1) / kSplitKeys;
   const int64_t max_dec_items = static_cast<int64_t>(num_seqs) * hkv * max_splits;
   if (max_dec_items >= (int64_t(1) << 31)) return PKV_ERR_NO_MEMORY;
-  const size_t need = layout_workspace(nullptr, num_seqs, hkv, gp, cache->head_dim, max_dec_items, nullptr);
+  const int64_t max_pre_units = max_prefill_units(num_tokens, num_seqs, gp);
+  const size_t need = layout_workspace(nullptr, num_seqs, hkv, gp, cache->head_dim, max_dec_items, max_pre_units,
+                                       nullptr);
   if (need > kNoAllocScratchBytes - kErrSlotBytes) return PKV_ERR_NO_MEMORY;
 
   int dev = 0;
@@ -101,13 +103,16 @@ extern "C" PKV_API int paged_attention_noalloc(const void* q, const void* k_cach
   uint32_t* err = error_bits ? error_bits : static_cast<uint32_t*>(scratch);
   Workspace ws;
   layout_workspace(static_cast<uint8_t*>(scratch) + kErrSlotBytes, num_seqs, hkv, gp, cache->head_dim,
-                   max_dec_items, &ws);
+                   max_dec_items, max_pre_units, &ws);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   AttnArgs a{q,        k_cache,    v_cache,       *cache,      block_tables, max_blocks_per_seq, seq_lens,
              query_start_loc, num_seqs, num_q_heads, num_tokens, max_query_len, max_seq_len, scale, out};
   PlanArgs plan{seq_lens, query_start_loc, num_seqs, num_tokens, hkv, max_blocks_per_seq, max_seq_len,
                 kSplitKeys, kPrefillTilesPerItem * (kTileKeys / gp), ws.counters, ws.dec_prefix, ws.pre_prefix, ws.unit_bad,
                 ws.merge_list, err};
+  plan.pre_order = ws.pre_order;
+  plan.max_pre_units = max_pre_units;
+  plan.rows_q = kTileKeys / gp;
   st = launch_plan(plan, s);
   if (st) return st;
   st = launch_decode_tc(a, ws, sms, err, s);

@@ -224,6 +224,60 @@ __device__ void write_new_tokens(const PlanArgs& p) {
   }
 }
 
+// Key tiles of the later query tile of prefill pair `pl` of a request (pl = 0: its
+// heaviest pair): the pair's cost, the same count the prefill kernel derives.
+__device__ __forceinline__ int pair_key_tiles(int64_t ctx, int64_t q_len, int rows_q, int pl) {
+  const int64_t nqt = (q_len + rows_q - 1) / rows_q;
+  const int64_t npair = (nqt + 1) / 2;
+  const int64_t pair = npair - 1 - pl;
+  const int64_t hi = 2 * pair + 1;
+  const int64_t t0 = hi < nqt ? hi : 2 * pair;
+  const int64_t j0 = t0 * rows_q;
+  const int64_t nq = q_len - j0 < rows_q ? q_len - j0 : rows_q;
+  const int64_t kend = ctx + j0 + nq;
+  return kend > 0 ? static_cast<int>((kend + kTileKeys - 1) / kTileKeys) : 0;
+}
+
+// The prefill pairs (request, pair) of the whole batch ordered heaviest first -- a
+// counting sort on the pair's key-tile count (clamped to the bucket range) -- so that
+// the pairs handed out last are the lightest and the CTAs run out of work together.
+// Ids are the pairs' positions in request order (pre_prefix / hkv + pl).  Pairs of
+// equal cost land in any order: which CTA runs a pair changes no result.
+constexpr int kOrderBuckets = kPlanThreads;
+__device__ void order_prefill_pairs(const PlanArgs& p) {
+  __shared__ int bucket[kOrderBuckets];
+  const int tid = threadIdx.x;
+  bucket[tid] = 0;
+  __syncthreads();
+  auto for_each_pair = [&](auto&& fn) {
+    for (int i = tid; i < p.num_seqs; i += blockDim.x) {
+      const int64_t q0 = p.qsl[i], q1 = p.qsl[i + 1];
+      const int64_t q_len = q1 - q0;
+      if (!(q0 >= 0 && q1 >= q0 && q1 <= p.num_tokens) || q_len <= 1) continue;
+      const int64_t ctx = static_cast<int64_t>(p.seq_lens[i]) - q_len;
+      const int base = p.pre_prefix[i] / p.hkv;
+      const int npair = (p.pre_prefix[i + 1] - p.pre_prefix[i]) / p.hkv;
+      for (int pl = 0; pl < npair; ++pl) {
+        const int key = min(pair_key_tiles(ctx, q_len, p.rows_q, pl), kOrderBuckets - 1);
+        fn(kOrderBuckets - 1 - key, base + pl);  // heavier pairs in lower buckets
+      }
+    }
+  };
+  for_each_pair([&](int b, int) { atomicAdd(&bucket[b], 1); });
+  __syncthreads();
+  {
+    const int v[3] = {bucket[tid], 0, 0};
+    int ex[3], tot[3];
+    block_scan3(v, ex, tot);
+    bucket[tid] = ex[0];  // first position of the bucket
+  }
+  __syncthreads();
+  for_each_pair([&](int b, int id) {
+    const int pos = atomicAdd(&bucket[b], 1);
+    if (pos < p.max_pre_units) p.pre_order[pos] = id;
+  });
+}
+
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs p) {
   if (blockIdx.x > 0) {  // writer CTAs never join the planner's block barriers
     write_new_tokens(p);
@@ -274,6 +328,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs p) {
   if (threadIdx.x == 0) {
     p.dec_prefix[p.num_seqs] = carry_d;
     p.pre_prefix[p.num_seqs] = carry_p;
+  }
+  if (carry_p > 0 && p.pre_order) order_prefill_pairs(p);  // (carry_p is the same in every thread)
+  if (threadIdx.x == 0) {
     p.counters[kMergeCountSlot] = carry_m;
   }
 }

@@ -95,6 +95,7 @@ struct PrefillParams {
   const int32_t* seq_lens;
   const int32_t* qsl;
   const int32_t* pre_prefix;
+  const int32_t* pre_order;  // pairs heaviest first: ids pre_prefix[i] / hkv + pl
   int32_t* queue;
   uint32_t* err;
   int64_t num_blocks;
@@ -229,10 +230,13 @@ __device__ PItem make_item(const PrefillParams& P, int idx, int total) {
     r.idx = -1;
     return r;
   }
+  // the planner's order of (request, pair) units, heaviest first; the kv heads of a
+  // unit are consecutive items
+  const int unit = P.pre_order[idx / P.hkv];
   int lo = 0, hi = P.num_seqs - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (P.pre_prefix[mid] <= idx) lo = mid; else hi = mid - 1;
+    if (P.pre_prefix[mid] <= unit * P.hkv) lo = mid; else hi = mid - 1;
   }
   const int i = lo;
   const int base = P.pre_prefix[i];
@@ -241,9 +245,9 @@ __device__ PItem make_item(const PrefillParams& P, int idx, int total) {
   r.idx = idx;
   r.seq = i;
   if (npair <= 0) return r;  // inconsistent plan: invalid item
-  const int local = idx - base;
-  const int pair = npair - 1 - local / P.hkv;  // heaviest (latest) query tiles first
-  r.head = local % P.hkv;
+  const int pl = unit - base / P.hkv;
+  const int pair = npair - 1 - pl;  // pl = 0: the request's latest (heaviest) query tiles
+  r.head = idx % P.hkv;
   const int64_t q0 = P.qsl[i], q1 = P.qsl[i + 1];
   const int64_t L = P.seq_lens[i];
   const int64_t q_len = q1 - q0;
@@ -853,6 +857,7 @@ int launch_prefill_tc(const AttnArgs& a, const Workspace& ws, int num_sms, uint3
   p.seq_lens = a.seq_lens;
   p.qsl = a.qsl;
   p.pre_prefix = ws.pre_prefix;
+  p.pre_order = ws.pre_order;
   p.queue = ws.counters + 1;
   p.err = err;
   p.num_blocks = a.cache.num_blocks;

@@ -142,6 +142,7 @@ struct Workspace {
   int32_t* counters;     // [kNumQueueCounters] work-queue heads
   int32_t* dec_prefix;   // [num_seqs + 1] exclusive prefix of decode items
   int32_t* pre_prefix;   // [num_seqs + 1] exclusive prefix of prefill items
+  int32_t* pre_order;    // [max_pre_units] prefill pairs, heaviest first (ids in request order)
   int32_t* unit_bad;     // [num_seqs * hkv] a split saw a bad block id
   int32_t* merge_list;   // [num_seqs] decode requests cut into several splits
   float* part_ml;        // [max_dec_items * GP * 2] split running max and sum
@@ -169,9 +170,16 @@ struct CascadeArgs {
 
 // Computes the layout at `base` (nullptr: only the size) and returns the bytes needed;
 // `group` is the padded head-group width GP the decode partials are stored with.
-// With `cas`, also the shared-prefix arrays.
+// `max_pre_units` bounds the prefill items' query-tile pairs.  With `cas`, also the
+// shared-prefix arrays.
 size_t layout_workspace(void* base, int32_t num_seqs, int32_t hkv, int32_t group, int32_t head_dim,
-                        int64_t max_dec_items, Workspace* ws, const CascadeArgs* cas = nullptr);
+                        int64_t max_dec_items, int64_t max_pre_units, Workspace* ws,
+                        const CascadeArgs* cas = nullptr);
+// Query-tile pairs of the prefill items of a batch: at most one per 2R query tokens plus
+// one per request (R = 128 / GP query tokens per tile).
+inline int64_t max_prefill_units(int64_t num_tokens, int32_t num_seqs, int32_t gp) {
+  return num_tokens / (kPrefillTilesPerItem * (kTileKeys / gp)) + num_seqs;
+}
 
 struct PlanArgs {
   const int32_t* seq_lens;
@@ -193,6 +201,9 @@ struct PlanArgs {
   const int32_t* bt = nullptr;
   CascadeArgs cas{};
   int32_t cas_rows = 0;  // member requests per cascade item
+  int32_t* pre_order = nullptr;  // heaviest-first order of the prefill pairs
+  int64_t max_pre_units = 0;
+  int32_t rows_q = 0;            // query tokens per prefill tile
   int32_t* seq_prefix = nullptr;
   int32_t* seq_entry = nullptr;
   int32_t* member_ok = nullptr;
