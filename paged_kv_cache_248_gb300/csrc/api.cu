@@ -85,6 +85,8 @@ size_t layout_workspace(void* base, int32_t num_seqs, int32_t hkv, int32_t group
   w.dec_prefix = static_cast<int32_t*>(take((static_cast<size_t>(num_seqs) + 1) * sizeof(int32_t)));
   w.pre_prefix = static_cast<int32_t*>(take((static_cast<size_t>(num_seqs) + 1) * sizeof(int32_t)));
   w.pre_order = static_cast<int32_t*>(take(static_cast<size_t>(max_pre_units) * sizeof(int32_t)));
+  w.dec_order = static_cast<int32_t*>(take(static_cast<size_t>(num_seqs) * sizeof(int32_t)));
+  w.dec_start = static_cast<int32_t*>(take((static_cast<size_t>(num_seqs) + 1) * sizeof(int32_t)));
   w.unit_bad = static_cast<int32_t*>(take(static_cast<size_t>(num_seqs) * hkv * sizeof(int32_t)));
   w.merge_list = static_cast<int32_t*>(take(static_cast<size_t>(num_seqs) * sizeof(int32_t)));
   w.part_ml = static_cast<float*>(take(static_cast<size_t>(max_dec_items) * group * 2 * sizeof(float)));
@@ -331,6 +333,9 @@ int attention_impl(const void* q, const void* k_new, const void* v_new, const vo
   plan.pre_order = ws.pre_order;
   plan.max_pre_units = max_pre_units;
   plan.rows_q = kTileKeys / gp;
+  plan.dec_order = ws.dec_order;
+  plan.dec_start = ws.dec_start;
+  plan.num_sms = ctx->num_sms;
   if (write) {
     const int64_t warps_per_cta = 1024 / 32;
     const int64_t want = (num_tokens + warps_per_cta - 1) / warps_per_cta;

@@ -90,6 +90,9 @@ struct DecodeParams {
   const int32_t* seq_lens;
   const int32_t* qsl;
   const int32_t* dec_prefix;
+  const int32_t* dec_order;   // when *order_flag: queue position order of the requests
+  const int32_t* dec_start;   //   and the items' exclusive prefix in that order
+  const int32_t* order_flag;
   int32_t* queue;
   int32_t* unit_bad;
   float* part_o;   // [items][128][GP]
@@ -185,6 +188,9 @@ __device__ void scheduler_warp(const DecodeParams& P, Ctl& c) {
   const int lane = threadIdx.x & 31;
   volatile int* abort_flag = &c.abort_flag;
   const int total = P.dec_prefix[P.num_seqs];
+  // queue positions follow the planner's order of the requests when it made one
+  const bool ordered = *P.order_flag != 0;
+  const int32_t* starts = ordered ? P.dec_start : P.dec_prefix;
   for (uint32_t it = 0;; ++it) {
     const int slot = it % kRing;
     if (!mbar_wait(&c.item_empty[slot], ((it / kRing) & 1) ^ 1, abort_flag)) {
@@ -203,31 +209,32 @@ __device__ void scheduler_warp(const DecodeParams& P, Ctl& c) {
       }
       break;
     }
-    // the request owning the item: last i with dec_prefix[i] <= idx, by a 32-way
+    // the request owning the queue position: last k with starts[k] <= idx, by a 32-way
     // search (each round the 32 lanes probe evenly spaced candidates)
     int lo = 0, hi = P.num_seqs - 1;
     while (hi > lo) {
       const int step = (hi - lo + 32) / 32;
       const int pos = lo + lane * step;
-      const bool le = pos <= hi && __ldg(P.dec_prefix + pos) <= idx;
-      const unsigned m = __ballot_sync(0xffffffffu, le);  // lane 0 always: dec_prefix[lo] <= idx
+      const bool le = pos <= hi && __ldg(starts + pos) <= idx;
+      const unsigned m = __ballot_sync(0xffffffffu, le);  // lane 0 always: starts[lo] <= idx
       lo += (31 - __clz(m)) * step;
       hi = min(hi, lo + step - 1);
     }
-    const int i = lo;
-    const int base = __ldg(P.dec_prefix + i);
+    const int i = ordered ? __ldg(P.dec_order + lo) : lo;
+    const int qbase = __ldg(starts + lo);
+    const int base = __ldg(P.dec_prefix + i);  // the request's items in request order
     const int cnt = __ldg(P.dec_prefix + i + 1) - base;
     const int64_t L = __ldg(P.seq_lens + i);
     const int64_t t = __ldg(P.qsl + i), t1 = __ldg(P.qsl + i + 1);
     const int nsplit = cnt / P.hkv;
     const int64_t pre = P.seq_prefix ? __ldg(P.seq_prefix + i) : 0;  // shared-prefix keys, done elsewhere
-    r.idx = idx;
+    r.idx = base + (idx - qbase);  // the item's index in request order: where its partial goes
     r.seq = i;
     r.row_ok = (t >= 0 && t < P.num_tokens && t1 == t + 1) ? 1 : 0;
     r.trow = r.row_ok ? static_cast<int32_t>(t) : 0;
     r.nsplit = 1;
     if (nsplit > 0) {  // always, for a consistent plan
-      const int local = idx - base;
+      const int local = idx - qbase;
       r.head = local / nsplit;
       r.split = local % nsplit;
       r.nsplit = nsplit;
@@ -950,6 +957,9 @@ int launch_decode_tc(const AttnArgs& a, const Workspace& ws, int num_sms, uint32
   p.seq_lens = a.seq_lens;
   p.qsl = a.qsl;
   p.dec_prefix = ws.dec_prefix;
+  p.dec_order = ws.dec_order;
+  p.dec_start = ws.dec_start;
+  p.order_flag = ws.counters + kDecOrderSlot;
   p.queue = ws.counters + 0;
   p.unit_bad = ws.unit_bad;
   p.part_o = ws.part_o;

@@ -113,6 +113,9 @@ extern "C" PKV_API int paged_attention_noalloc(const void* q, const void* k_cach
   plan.pre_order = ws.pre_order;
   plan.max_pre_units = max_pre_units;
   plan.rows_q = kTileKeys / gp;
+  plan.dec_order = ws.dec_order;
+  plan.dec_start = ws.dec_start;
+  plan.num_sms = sms;
   st = launch_plan(plan, s);
   if (st) return st;
   st = launch_decode_tc(a, ws, sms, err, s);

@@ -278,6 +278,68 @@ __device__ void order_prefill_pairs(const PlanArgs& p) {
   });
 }
 
+// A small decode batch -- at most kDecOrderMaxItemsPerSm items per SM, where the last
+// items decide when the kernel ends -- is handed out largest item first: the decode
+// requests sorted by the key tiles of their largest item (an unsplit request's whole
+// context, else one split), with the items' prefix in that order.  The decode kernel
+// maps a queue position through it and keeps storing partials by the request-order
+// item index.  Larger batches keep request order.
+constexpr int kDecOrderMaxItemsPerSm = 16;
+constexpr int kDecOrderBuckets = 32;
+__device__ void order_decode_requests(const PlanArgs& p, int total) {
+  __shared__ int bucket[kDecOrderBuckets];
+  const int tid = threadIdx.x;
+  if (tid < kDecOrderBuckets) bucket[tid] = 0;
+  __syncthreads();
+  auto for_each_request = [&](auto&& fn) {
+    for (int i = tid; i < p.num_seqs; i += blockDim.x) {
+      const int nd = p.dec_prefix[i + 1] - p.dec_prefix[i];
+      if (nd <= 0) continue;
+      const int ns = nd / p.hkv;
+      const bool cascade = p.cas.num_groups > 0 && p.cas.num_members > 0;
+      const int64_t keys = static_cast<int64_t>(p.seq_lens[i]) - (cascade ? p.seq_prefix[i] : 0);
+      const int64_t tiles = ns > 1 ? p.split_keys / kTileKeys : (keys + kTileKeys - 1) / kTileKeys;
+      const int key = static_cast<int>(tiles < kDecOrderBuckets - 1 ? (tiles > 0 ? tiles : 0) : kDecOrderBuckets - 1);
+      fn(kDecOrderBuckets - 1 - key, i);  // larger items in lower buckets
+    }
+  };
+  for_each_request([&](int b, int) { atomicAdd(&bucket[b], 1); });
+  __syncthreads();
+  if (tid < 32) {  // exclusive prefix over the buckets, one warp
+    const int v = bucket[tid];
+    int inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, inc, o);
+      if (tid >= o) inc += n;
+    }
+    bucket[tid] = inc - v;
+  }
+  __syncthreads();
+  for_each_request([&](int b, int i) { p.dec_order[atomicAdd(&bucket[b], 1)] = i; });
+  __syncthreads();
+  const int nreq = bucket[kDecOrderBuckets - 1];  // every decode request has a place
+  // the items' exclusive prefix in that order; positions past the last request hold the
+  // total, so a search over all num_seqs positions never lands there
+  int carry = 0;
+  for (int base = 0; base < p.num_seqs; base += blockDim.x) {
+    const int k = base + tid;
+    int v3[3] = {0, 0, 0};
+    if (k < nreq) {
+      const int i = p.dec_order[k];
+      v3[0] = p.dec_prefix[i + 1] - p.dec_prefix[i];
+    }
+    int ex[3], tot[3];
+    block_scan3(v3, ex, tot);
+    if (k < p.num_seqs) p.dec_start[k] = carry + ex[0];
+    carry += tot[0];
+  }
+  if (tid == 0) {
+    p.dec_start[p.num_seqs] = total;
+    p.counters[kDecOrderSlot] = 1;
+  }
+}
+
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs p) {
   if (blockIdx.x > 0) {  // writer CTAs never join the planner's block barriers
     write_new_tokens(p);
@@ -329,7 +391,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs p) {
     p.dec_prefix[p.num_seqs] = carry_d;
     p.pre_prefix[p.num_seqs] = carry_p;
   }
-  if (carry_p > 0 && p.pre_order) order_prefill_pairs(p);  // (carry_p is the same in every thread)
+  // (carry_p and carry_d are the same in every thread)
+  if (carry_p > 0 && p.pre_order) order_prefill_pairs(p);
+  if (carry_d > 0 && p.dec_order && carry_d <= kDecOrderMaxItemsPerSm * p.num_sms) order_decode_requests(p, carry_d);
   if (threadIdx.x == 0) {
     p.counters[kMergeCountSlot] = carry_m;
   }

@@ -32,6 +32,7 @@ __host__ __device__ inline int64_t decode_splits(int64_t L) {
 constexpr int kNumQueueCounters = 8; // work-queue counters in the workspace
 constexpr int kMergeCountSlot = 2;   // counters[2]: number of requests in the merge list
 constexpr int kCascadeQueueSlot = 3; // counters[3]: the shared-prefix kernel's work queue
+constexpr int kDecOrderSlot = 4;     // counters[4]: 1 when the decode items follow dec_order
 
 // Shared-prefix (cascade) key splits: a prefix of P tokens is attended in pieces of
 // kCascadeSplitKeys keys, a function of P alone.
@@ -143,6 +144,8 @@ struct Workspace {
   int32_t* dec_prefix;   // [num_seqs + 1] exclusive prefix of decode items
   int32_t* pre_prefix;   // [num_seqs + 1] exclusive prefix of prefill items
   int32_t* pre_order;    // [max_pre_units] prefill pairs, heaviest first (ids in request order)
+  int32_t* dec_order;    // [num_seqs] decode requests, largest item first (small batches)
+  int32_t* dec_start;    // [num_seqs + 1] exclusive prefix of decode items in that order
   int32_t* unit_bad;     // [num_seqs * hkv] a split saw a bad block id
   int32_t* merge_list;   // [num_seqs] decode requests cut into several splits
   float* part_ml;        // [max_dec_items * GP * 2] split running max and sum
@@ -202,6 +205,9 @@ struct PlanArgs {
   CascadeArgs cas{};
   int32_t cas_rows = 0;  // member requests per cascade item
   int32_t* pre_order = nullptr;  // heaviest-first order of the prefill pairs
+  int32_t* dec_order = nullptr;  // largest-item-first order of the decode requests
+  int32_t* dec_start = nullptr;
+  int32_t num_sms = 0;
   int64_t max_pre_units = 0;
   int32_t rows_q = 0;            // query tokens per prefill tile
   int32_t* seq_prefix = nullptr;
