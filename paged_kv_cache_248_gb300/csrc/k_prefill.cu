@@ -12,14 +12,16 @@
 // 4, 8 or 16), row r <-> (query j0 + r / GP, head r % GP).  An item is a pair of
 // query tiles of one (request, kv head) -- tiles 2p + 1 and 2p, the later one as
 // tile 0 of the item -- and every K/V tile it loads feeds both: the later tile sees
-// the earlier one's keys and at most one tile more.  Items, the heaviest pairs of a
-// request first, come from an atomic queue to persistent CTAs, one per SM.
+// the earlier one's keys and at most one tile more.  Items come from an atomic queue
+// to persistent CTAs, one per SM, in the planner's order: the heaviest pairs of the
+// whole batch first.
 //
 // Per CTA (320 threads):
 //   warp 0     producer: TMA-loads the two Q tiles (3-D boxes over [token][head][dim])
 //              and, per 128-key tile, 2 K and 2 V boxes per 16-token block from the
 //              block's physical location (the block-table gather), 128-byte swizzle.
-//              K and V have separate stage barriers and K runs one tile ahead of V.
+//              K tiles go into a 2-slot ring and V tiles into a 3-slot one, each tile's
+//              K and V issued together.
 //   warp 1     MMA issuer.  Per key tile j and query tile w it issues O_w += P_w(j-1)
 //              V(j-1), then S_w(j) = Q_w K(j)^T.  S_w lives in TMEM; the softmax writes
 //              P_w as bf16 over the first 64 of S_w's columns and the P V MMA reads its
@@ -32,7 +34,8 @@
 //              for the exponents -- so that no whole row is held in registers, applies the
 //              causal mask, and keeps a per-row reference maximum; only when a row's
 //              maximum grows by more than 2^8 does the warp rescale its O rows in TMEM.
-//              The final O / l is stored per row.
+//              Two scores go through each packed fp32x2 FMA and add, and each
+//              three-input max.  The final O / l is stored per row.
 // All waits are bounded (see ptx.cuh); a timeout raises the CTA abort flag.
 //
 // Shared-prefix (cascade) mode, kCas = true.  The same pipeline attends the member
