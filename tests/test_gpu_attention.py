@@ -109,14 +109,14 @@ def test_request_without_query_tokens(pkv):
     run_pair(pkv, w)
 
 
-@pytest.mark.parametrize("group,hkv", [(4, 8), (8, 4), (16, 2)])
-def test_many_short_decodes_with_invalid_items(pkv, group, hkv):
-    """3000 decodes of 1..400 keys: every CTA takes ~20 items, so the item ring wraps
-    many times and consecutive items alternate between softmax groups; every 97th
-    request has seq_len 0 (an invalid item: flagged, its rows zeroed) so that
-    invalid items fall on both groups.  Valid rows match the oracle."""
+@pytest.mark.parametrize("group,hkv,n", [(4, 8, 3000), (8, 4, 3000), (16, 2, 3000), (4, 1, 2000)])
+def test_many_short_decodes_with_invalid_items(pkv, group, hkv, n):
+    """n decodes of 1..400 keys: every CTA takes many items, so the item ring wraps
+    many times; every 97th request has seq_len 0 (an invalid item: flagged, its rows
+    zeroed).  With one kv head, 2000 items are few enough per SM for the planner to hand
+    them out largest first, over more requests than its block holds threads.  Valid
+    rows match the oracle."""
     rng = np.random.default_rng(31)
-    n = 3000
     L = rng.integers(1, 400, size=n, endpoint=True).astype(np.int32)
     w = wl.sized_case(32, L, np.ones(n, np.int32), group * hkv, hkv, 128, "bf16")
     bad = np.arange(5, n, 97)
