@@ -98,6 +98,18 @@ def test_prefill_head_folding_bf16(pkv, group, hkv):
     run_pair(pkv, w)
 
 
+def test_many_prefill_chunks_heaviest_first(pkv):
+    # 1200 chunks of 2..40 queries after 0..200 cached tokens, mixed with decodes: the
+    # planner orders ~1200 query-tile pairs over more requests than its block holds
+    # threads; every row matches the oracle whichever CTA ran its pair
+    rng = np.random.default_rng(27)
+    n = 1500
+    q = np.where(np.arange(n) % 5 == 4, 1, rng.integers(2, 40, size=n, endpoint=True)).astype(np.int32)
+    L = (q + rng.integers(0, 200, size=n, endpoint=True)).astype(np.int32)
+    w = wl.sized_case(28, L, q, 8, 2, 128, "bf16")
+    run_pair(pkv, w)
+
+
 def test_decode_large_scale_bf16(pkv):
     w = wl.sized_case(26, [3000, 2049, 77], [1, 1, 1], 64, 8, 128, "bf16", scale=0.5)
     run_pair(pkv, w)
