@@ -298,6 +298,13 @@ PKV_API const char* pkv_trace_kind_name(int kind);
  */
 PKV_API int pkv_umma_selftest(const int32_t* params, const void* a_img, const void* b_img, float* d_out, void* stream);
 PKV_API int pkv_tma_selftest(const void* src, int64_t rows, int32_t row0, void* dump, void* stream);
+/*
+ * pkv_wait_selftest launches one CTA that waits on an mbarrier nothing arrives on.
+ * The bounded wait every kernel of the library uses gives up after its limit (1 s),
+ * the CTA sets the timeout bit of the device error word and exits: the next
+ * pkv_get_last_error() returns PKV_ERR_TIMEOUT, and the context stays usable.
+ */
+PKV_API int pkv_wait_selftest(void* stream);
 
 #ifdef __cplusplus
 }

@@ -11,7 +11,7 @@ Functions carry the C names:
   pkv_slot_mapping, pkv_write, pkv_copy_blocks, paged_attention, paged_attention_cascade,
   paged_attention_step,
   pkv_get_last_error, pkv_peek_error_bits, pkv_trace_enable, pkv_trace_read,
-  pkv_num_workers, pkv_shutdown, pkv_umma_selftest, pkv_tma_selftest.
+  pkv_num_workers, pkv_shutdown, pkv_umma_selftest, pkv_tma_selftest, pkv_wait_selftest.
 """
 from __future__ import annotations
 
@@ -78,6 +78,7 @@ def lib():
                 "pkv_trace_read": [ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_double)],
                 "pkv_umma_selftest": [P, P, P, P, P],
                 "pkv_tma_selftest": [P, i64, i32, P, P],
+                "pkv_wait_selftest": [P],
             }
             for name, args in sig.items():
                 fn = getattr(L, name)
@@ -288,6 +289,10 @@ def pkv_umma_selftest(params, a_img: torch.Tensor, b_img: torch.Tensor, d_out: t
     arr = (ctypes.c_int32 * 29)(*[int(x) for x in params])
     _check(lib().pkv_umma_selftest(arr, _dev(a_img, "a_img"), _dev(b_img, "b_img"),
                                    _dev(d_out, "d_out", torch.float32), _stream(stream)), "pkv_umma_selftest")
+
+
+def pkv_wait_selftest(stream=None) -> None:
+    _check(lib().pkv_wait_selftest(_stream(stream)), "pkv_wait_selftest")
 
 
 def pkv_tma_selftest(src: torch.Tensor, row0: int, dump: torch.Tensor, stream=None) -> None:

@@ -533,4 +533,11 @@ int pkv_tma_selftest(const void* src, int64_t rows, int32_t row0, void* dump, vo
   return run_tma_selftest(src, rows, row0, dump, ctx->err, as_stream(stream));
 }
 
+int pkv_wait_selftest(void* stream) {
+  int st = PKV_OK;
+  DeviceCtx* ctx = device_ctx(&st);
+  if (!ctx) return st;
+  return run_wait_selftest(ctx->err, as_stream(stream));
+}
+
 }  // extern "C"

@@ -123,7 +123,24 @@ __global__ void __launch_bounds__(32) tma_probe_kernel(const __grid_constant__ C
   for (int i = threadIdx.x; i < 256; i += 32) dump[i] = reinterpret_cast<const uint4*>(buf)[i];
 }
 
+// One CTA waits on an mbarrier that nothing arrives on: the bounded wait every kernel
+// uses gives up after its limit, and the kernel reports a timeout and returns.
+__global__ void __launch_bounds__(32) wait_probe_kernel(uint32_t* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  if (!mbar_wait(&bar, 0, nullptr) && threadIdx.x == 0) flag_error(err, kErrTimeout);
+}
+
 }  // namespace
+
+int run_wait_selftest(uint32_t* err, cudaStream_t s) {
+  wait_probe_kernel<<<1, 32, 0, s>>>(err);
+  return cuda_status(cudaGetLastError());
+}
 
 int run_umma_selftest(const int32_t* params, const void* a_img, const void* b_img, float* d_out, uint32_t* err,
                       cudaStream_t s) {

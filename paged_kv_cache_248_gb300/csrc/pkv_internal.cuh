@@ -249,5 +249,6 @@ int encode_tensor_map_2d(CUtensorMap* map, const void* base, uint64_t inner, uin
 int run_umma_selftest(const int32_t* params, const void* a_img, const void* b_img, float* d_out, uint32_t* err,
                       cudaStream_t s);
 int run_tma_selftest(const void* src, int64_t rows, int32_t row0, void* dump, uint32_t* err, cudaStream_t s);
+int run_wait_selftest(uint32_t* err, cudaStream_t s);
 
 }  // namespace pkv

@@ -145,3 +145,33 @@ def test_tma_swizzle_128b(pkv, row0):
             for c in range(8):
                 np.testing.assert_array_equal(got[h, r, c ^ (r % 8)],
                                               src[row0 + r, 64 * h + 8 * c:64 * h + 8 * c + 8])
+
+
+def test_bounded_wait_times_out_and_the_context_stays_usable(pkv):
+    # A wait that nothing completes gives up after its limit (1 s): the kernel reports
+    # the timeout through the error word and returns -- no trap, no hang -- and the
+    # next call on the same context computes correctly.
+    import time
+
+    import oracle
+    import workloads as wl
+    from helpers import bits, compare
+
+    torch.cuda.synchronize()
+    assert pkv.pkv_get_last_error() == 0
+    t0 = time.time()
+    pkv.pkv_wait_selftest()
+    torch.cuda.synchronize()
+    took = time.time() - t0
+    assert pkv.pkv_get_last_error() == pkv.PKV_ERR_TIMEOUT
+    assert 0.5 < took < 30
+    w = wl.random_case(5, num_seqs=4, max_ctx=300, max_q=40, group=4, num_kv_heads=2, head_dim=128, dtype="bf16")
+    t_cpu = w.make_tensors("cpu")
+    t = {k: v.cuda() for k, v in t_cpu.items()}
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    out = pkv.paged_attention(t["q"], t["k_cache"], t["v_cache"], dev(w.block_tables), dev(w.seq_lens),
+                              dev(w.query_start_loc), w.scale, w.max_query_len, w.max_seq_len)
+    assert pkv.pkv_get_last_error() == 0
+    ref = oracle.attention(bits(t_cpu["q"]), bits(t_cpu["k_cache"]), bits(t_cpu["v_cache"]), w.block_tables,
+                           w.seq_lens, w.query_start_loc, w.scale)
+    compare(out, ref, "bf16", w.name)
