@@ -100,11 +100,13 @@ def test_long_prefixes_fold_every_prefix_split(pkv, group):
     compare(cas, ref, "bf16", w.name)
 
 
-def test_enough_members_for_paired_member_tiles(pkv):
-    # 70 members of a 4800-key prefix (10 prefix splits) over 8 kv heads give 2 x 8 x 10
-    # items of two 32-member tiles each: at least one per SM on a 152-SM part, so the
-    # cascade pairs its member tiles (fewer items would leave SMs idle and use one tile)
-    w, hints = wl.shared_prefix_case(18, prefix_blocks=(300,), members=(70,), group=4, num_kv_heads=8,
+@pytest.mark.parametrize("group,hkv,members", [(4, 8, 70), (8, 4, 100), (16, 2, 120)])
+def test_enough_members_for_paired_member_tiles(pkv, group, hkv, members):
+    # A 4800-key prefix (10 prefix splits) with enough members that the items of two
+    # member tiles each (128 / GP members per tile) are at least one per SM on a 152-SM
+    # part -- e.g. 70 members, group 4, 8 kv heads: 2 x 8 x 10 -- so the cascade pairs
+    # its member tiles (fewer items would leave SMs idle and use one tile)
+    w, hints = wl.shared_prefix_case(18, prefix_blocks=(300,), members=(members,), group=group, num_kv_heads=hkv,
                                      max_suffix=40, bystanders=2, bad_hints=False)
     t_cpu = w.make_tensors("cpu")
     t = {k: v.cuda() for k, v in t_cpu.items()}
