@@ -457,7 +457,7 @@ __device__ void mma_warp(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uint8_t*
       // Step j: P_w(j-1) V(j-1), then S_w(j) = Q_w K(j)^T, for w = 0, 1.  An MMA issue
       // returns only as the tensor core takes it in, so the MMAs are issued back to back:
       // the only wait between the last MMA of one step and the first of the next is for
-      // P_0; the K/V waits and the ring releases sit right after an MMA burst, where the
+      // P_0; the K wait and the ring releases sit right after an MMA burst, where the
       // tensor core still has queued work.  Ring releases are one step late: K(j-1)'s
       // and V(j-2)'s after P_0(j-1) V(j-1), V(nt0-1)'s after the item.
       for (int j = 0; j <= nt0 && ok; ++j) {
@@ -508,14 +508,9 @@ __device__ void mma_warp(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uint8_t*
               issued = true;
             }
             __syncwarp();
-            // V(j), read by the next step's P V, while the tensor core works on S_0(j)
-            if (w == 0) {
-              const uint32_t vn = tv + (j > 0 ? 1 : 0);
-              if (!mbar_wait(&c.vfull[vn % kVStages], (vn / kVStages) & 1, abort_flag)) {
-                ok = false;
-                break;
-              }
-            }
+            // V(j) needs no wait here: tile 0's softmax warps hand P_0(j) over only after
+            // they have seen V(j) land and zeroed its rows past the context, and P_1(j)
+            // V(j) is issued after P_0(j) V(j), so the wait for P_0(j) covers both
           }
         }
         if (!ok) break;
