@@ -457,9 +457,10 @@ __device__ void mma_warp(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uint8_t*
       // Step j: P_w(j-1) V(j-1), then S_w(j) = Q_w K(j)^T, for w = 0, 1.  An MMA issue
       // returns only as the tensor core takes it in, so the MMAs are issued back to back:
       // the only wait between the last MMA of one step and the first of the next is for
-      // P_0; the K wait and the ring releases sit right after an MMA burst, where the
-      // tensor core still has queued work.  Ring releases are one step late: K(j-1)'s
-      // and V(j-2)'s after P_0(j-1) V(j-1), V(nt0-1)'s after the item.
+      // P_0, and the K wait sits right after an MMA burst, where the tensor core still has
+      // queued work.  The K and V ring slots are released by the softmax warps, which
+      // learn from their own S and O barriers when the MMAs reading a slot are done; a
+      // commit here would hold this thread for a queue slot each time.
       for (int j = 0; j <= nt0 && ok; ++j) {
         const int sk = tk % kKStages, sv = tv % kVStages;  // K(j), V(j-1)
 #pragma unroll
@@ -481,10 +482,6 @@ __device__ void mma_warp(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uint8_t*
                 umma_f16_ts(tmem + kOCol + 128 * w, tmem + 128 * w + 8 * kk, umma_desc_advance(bd, kk * 2048),
                             idesc_o, (j > 1 || kk > 0) ? 1u : 0u);
               if (j == ntw) umma_commit(&c.o_full[w]);
-              if (w == 0) {
-                if (j >= 1) umma_commit(&c.kempty[(tk - 1) % kKStages]);  // K(j-1): S_0, S_1(j-1) issued
-                if (j >= 2) umma_commit(&c.vempty[(tv - 1) % kVStages]);  // V(j-2): both P V issued
-              }
             }
             __syncwarp();
             ++pc[w];
@@ -516,11 +513,6 @@ __device__ void mma_warp(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uint8_t*
         if (!ok) break;
         if (j < nt0) ++tk;
         if (j > 0) ++tv;
-      }
-      if (ok && nt0 > 0) {
-        // the last V tile's release; K(nt0-1)'s and V(nt0-2)'s went out in step nt0
-        if (lane == 0) umma_commit(&c.vempty[(tv - 1) % kVStages]);
-        __syncwarp();
       }
 #pragma unroll
       for (int w = 0; w < 2; ++w)
@@ -648,6 +640,14 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uin
         break;
       }
       tc_fence_after();
+      // S_w(j) is complete, and so is every MMA issued before it: S_0(j) (issued before
+      // S_1(j)) and P_w(j-1) V(j-1) (P_1 V is issued after P_0 V).  So K(j) and V(j-1)
+      // are free once the last query tile that reads them gets here: tile 1's group
+      // releases the key tiles both tiles read, tile 0's group the one only it reads.
+      if (r == 0) {
+        if (w == 1 || j >= info.nt[1]) mbar_arrive(&c.kempty[(vc + j) % kKStages]);
+        if (j >= 1 && (w == 1 || j - 1 >= info.nt[1])) mbar_arrive(&c.vempty[(vc + j - 1) % kVStages]);
+      }
       // keys k0 .. k0 + nvis - 1 are visible to this row (cascade: the whole split).
       // The scores stay unscaled: the tile maximum of scale * s is scale times the
       // maximum of s (the minimum, for a negative scale), and each exponent takes
@@ -706,14 +706,15 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uin
       ++tc;
     }
     if (!ok) break;
-    vc += info.nt[0];
-    // final O_w of the item
+    // final O_w of the item; its last P V is complete, so its last V tile is free
     if (!mbar_wait(&c.o_full[w], ic & 1, abort_flag)) {
       ok = false;
       break;
     }
     ++ic;
     tc_fence_after();
+    if (r == 0 && (w == 1 || nt - 1 >= info.nt[1])) mbar_arrive(&c.vempty[(vc + nt - 1) % kVStages]);
+    vc += info.nt[0];
     const bool bad = c.bad[slot] != 0;
     if (kCas) {
       // the row's partial: accumulator [slot][head][128], then max and sum
