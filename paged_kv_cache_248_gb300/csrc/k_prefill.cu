@@ -433,104 +433,121 @@ __device__ void producer_warp(const PrefillParams& P, const CUtensorMap* qmap, c
 
 // ------------------------------------------------------------------ MMA warp
 __device__ void mma_warp(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uint8_t* kbuf, uint8_t* vbuf, uint32_t tmem) {
-  const int lane = threadIdx.x & 31;
-  const uint32_t idesc_s = umma_idesc_bf16(128, 128, false, false);
-  const uint32_t idesc_o = umma_idesc_bf16(128, 128, false, true);
-  volatile int* abort_flag = &c.abort_flag;
-  uint32_t it = 0, tk = 0, tv = 0;
-  uint32_t qc[2] = {0, 0}, pc[2] = {0, 0}, ic[2] = {0, 0};  // per tile slot: Q tiles, P tiles, items
-  bool issued = false, ok = true;
-  while (ok) {
-    const int slot = it % kRing;
-    if (!mbar_wait(&c.item_full[slot], (it / kRing) & 1, abort_flag)) {
-      ok = false;
-      break;
-    }
-    const PItem info = c.ring[slot];
-    ++it;
-    if (info.idx < 0) break;
-    if (info.valid) {
-      const int nt0 = info.nt[0];
+  // One thread issues every MMA and runs this whole loop alone: the other lanes wait at
+  // the end, so no warp-wide convergence sits between two MMA bursts.
+  if ((threadIdx.x & 31) == 0) {
+    const uint32_t idesc_s = umma_idesc_bf16(128, 128, false, false);
+    const uint32_t idesc_o = umma_idesc_bf16(128, 128, false, true);
+    const uint64_t qdesc[2] = {umma_smem_desc(smem_u32(qbuf), 16, 1024, kLayout128B),
+                               umma_smem_desc(smem_u32(qbuf + kTileBytes), 16, 1024, kLayout128B)};
+    volatile int* abort_flag = &c.abort_flag;
+    uint32_t it = 0, tk = 0, tv = 0;
+    uint32_t qc0 = 0, qc1 = 0, pc0 = 0, pc1 = 0, ic0 = 0, ic1 = 0;  // per tile slot: Q tiles, P tiles, items
+    bool issued = false, ok = true;
+    // O_w += P_w V (acc false: O_w = P_w V), V in ring slot sv; P_w is bf16 over S_w's first 64 columns
+    auto issue_pv = [&](int w, int sv, bool acc) {
+      const uint64_t bd = umma_smem_desc(smem_u32(vbuf + sv * kTileBytes), kHalfBytes, 1024, kLayout128B);
 #pragma unroll
-      for (int w = 0; w < 2; ++w)
-        if (ok && info.nt[w] > 0 && !mbar_wait(&c.q_full[w], qc[w] & 1, abort_flag)) ok = false;
-      // Step j: P_w(j-1) V(j-1), then S_w(j) = Q_w K(j)^T, for w = 0, 1.  An MMA issue
-      // returns only as the tensor core takes it in, so the MMAs are issued back to back:
-      // the only wait between the last MMA of one step and the first of the next is for
-      // P_0, and the K wait sits right after an MMA burst, where the tensor core still has
-      // queued work.  The K and V ring slots are released by the softmax warps, which
-      // learn from their own S and O barriers when the MMAs reading a slot are done; a
-      // commit here would hold this thread for a queue slot each time.
-      for (int j = 0; j <= nt0 && ok; ++j) {
-        const int sk = tk % kKStages, sv = tv % kVStages;  // K(j), V(j-1)
+      for (int kk = 0; kk < 8; ++kk)
+        umma_f16_ts(tmem + kOCol + 128 * w, tmem + 128 * w + 8 * kk, umma_desc_advance(bd, kk * 2048), idesc_o,
+                    (acc || kk > 0) ? 1u : 0u);
+    };
+    // S_w = Q_w K^T, K in ring slot sk
+    auto issue_s = [&](int w, int sk) {
+      const uint64_t b = umma_smem_desc(smem_u32(kbuf + sk * kTileBytes), 16, 1024, kLayout128B);
 #pragma unroll
-        for (int w = 0; w < 2; ++w) {
-          if (!ok) break;
-          const int ntw = info.nt[w];
-          if (j > 0 && j - 1 < ntw) {
-            // the item's first P V restarts O_w, once the previous item's O_w was read out
-            if (!mbar_wait(&c.p_full[w], pc[w] & 1, abort_flag) ||
-                (j == 1 && !mbar_wait(&c.o_free[w], (ic[w] & 1) ^ 1, abort_flag))) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            if (lane == 0) {
-              const uint64_t bd = umma_smem_desc(smem_u32(vbuf + sv * kTileBytes), kHalfBytes, 1024, kLayout128B);
-#pragma unroll
-              for (int kk = 0; kk < 8; ++kk)
-                umma_f16_ts(tmem + kOCol + 128 * w, tmem + 128 * w + 8 * kk, umma_desc_advance(bd, kk * 2048),
-                            idesc_o, (j > 1 || kk > 0) ? 1u : 0u);
-              if (j == ntw) umma_commit(&c.o_full[w]);
-            }
-            __syncwarp();
-            ++pc[w];
-          }
-          if (j < ntw) {
-            if (w == 0 && !mbar_wait(&c.kfull[sk], (tk / kKStages) & 1, abort_flag)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            if (lane == 0) {
-              const uint64_t a = umma_smem_desc(smem_u32(qbuf + w * kTileBytes), 16, 1024, kLayout128B);
-              const uint64_t b = umma_smem_desc(smem_u32(kbuf + sk * kTileBytes), 16, 1024, kLayout128B);
-#pragma unroll
-              for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-                umma_f16_ss(tmem + 128 * w, umma_desc_advance(a, off), umma_desc_advance(b, off), idesc_s, kk > 0);
-              }
-              umma_commit(&c.s_full[w]);
-              if (j == ntw - 1) umma_commit(&c.q_free[w]);
-              issued = true;
-            }
-            __syncwarp();
-            // V(j) needs no wait here: tile 0's softmax warps hand P_0(j) over only after
-            // they have seen V(j) land and zeroed its rows past the context, and P_1(j)
-            // V(j) is issued after P_0(j) V(j), so the wait for P_0(j) covers both
-          }
-        }
-        if (!ok) break;
-        if (j < nt0) ++tk;
-        if (j > 0) ++tv;
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+        umma_f16_ss(tmem + 128 * w, umma_desc_advance(qdesc[w], off), umma_desc_advance(b, off), idesc_s, kk > 0);
       }
-#pragma unroll
-      for (int w = 0; w < 2; ++w)
-        if (info.nt[w] > 0) {
-          ++qc[w];
-          ++ic[w];
+    };
+    while (ok) {
+      const int slot = it % kRing;
+      if (!mbar_wait(&c.item_full[slot], (it / kRing) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      const PItem info = c.ring[slot];
+      ++it;
+      if (info.idx < 0) break;
+      if (info.valid) {
+        const int nt0 = info.nt[0], nt1 = info.nt[1];
+        ok = (nt0 == 0 || mbar_wait(&c.q_full[0], qc0 & 1, abort_flag)) &&
+             (nt1 == 0 || mbar_wait(&c.q_full[1], qc1 & 1, abort_flag));
+        // Step j: P_0(j-1) V(j-1), S_0(j), P_1(j-1) V(j-1), S_1(j).  An MMA issue returns
+        // only as the tensor core takes it in, so the MMAs are issued back to back: the
+        // only wait between the last MMA of one step and the first of the next is for
+        // P_0, and the K wait sits right after an MMA burst, where the tensor core still
+        // has queued work.  V needs no wait: tile 0's softmax warps hand P_0(j) over only
+        // after they have seen V(j) land and zeroed its rows past the context, and
+        // P_1(j) V(j) is issued after P_0(j) V(j).  The K and V ring slots are released
+        // by the softmax warps, which learn from their own S and O barriers when the MMAs
+        // reading a slot are done; a commit here would hold this thread for a queue slot
+        // each time.  The item's first P V restarts O_w, once the previous item's O_w was
+        // read out.
+        for (int j = 0; j <= nt0 && ok; ++j) {
+          const int sk = tk % kKStages, sv = tv % kVStages;  // K(j), V(j-1)
+          if (j > 0) {
+            if (!mbar_wait(&c.p_full[0], pc0 & 1, abort_flag) ||
+                (j == 1 && !mbar_wait(&c.o_free[0], (ic0 & 1) ^ 1, abort_flag))) {
+              ok = false;
+              break;
+            }
+            ++pc0;
+            tc_fence_after();
+            issue_pv(0, sv, j > 1);
+            if (j == nt0) umma_commit(&c.o_full[0]);
+          }
+          if (j < nt0) {
+            if (!mbar_wait(&c.kfull[sk], (tk / kKStages) & 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(0, sk);
+            umma_commit(&c.s_full[0]);
+            if (j == nt0 - 1) umma_commit(&c.q_free[0]);
+            issued = true;
+          }
+          if (j > 0 && j - 1 < nt1) {
+            if (!mbar_wait(&c.p_full[1], pc1 & 1, abort_flag) ||
+                (j == 1 && !mbar_wait(&c.o_free[1], (ic1 & 1) ^ 1, abort_flag))) {
+              ok = false;
+              break;
+            }
+            ++pc1;
+            tc_fence_after();
+            issue_pv(1, sv, j > 1);
+            if (j == nt1) umma_commit(&c.o_full[1]);
+          }
+          if (j < nt1) {
+            tc_fence_after();
+            issue_s(1, sk);
+            umma_commit(&c.s_full[1]);
+            if (j == nt1 - 1) umma_commit(&c.q_free[1]);
+          }
+          if (j < nt0) ++tk;
+          if (j > 0) ++tv;
         }
+        if (nt0 > 0) {
+          ++qc0;
+          ++ic0;
+        }
+        if (nt1 > 0) {
+          ++qc1;
+          ++ic1;
+        }
+      }
+      if (!ok) break;
+      mbar_arrive(&c.item_empty[slot]);
     }
-    if (!ok) break;
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&c.item_empty[slot]);
-  }
-  if (!ok && !*abort_flag && lane == 0) raise_abort(c, P.err);
-  if (issued && lane == 0) {
-    // every MMA issued so far, and the barrier arrivals its commits trigger, must be
-    // complete before TMEM is freed and the CTA's shared memory goes away
-    umma_commit(&c.drain);
-    mbar_wait(&c.drain, 0, nullptr);
+    if (!ok && !*abort_flag) raise_abort(c, P.err);
+    if (issued) {
+      // every MMA issued so far, and the barrier arrivals its commits trigger, must be
+      // complete before TMEM is freed and the CTA's shared memory goes away
+      umma_commit(&c.drain);
+      mbar_wait(&c.drain, 0, nullptr);
+    }
   }
   __syncwarp();
 }
