@@ -350,69 +350,65 @@ __device__ void producer_warp(const DecodeParams& P, const CUtensorMap* qmap, co
 // ------------------------------------------------------------------ MMA warp
 __device__ void mma_warp(const DecodeParams& P, Ctl& c, uint8_t* stages, uint8_t* qbuf, uint8_t* pbuf,
                          uint32_t tmem) {
-  const int lane = threadIdx.x & 31;
-  const uint32_t idesc_s = umma_idesc_bf16(128, 16, false, false);
-  const uint32_t idesc_o = umma_idesc_bf16(128, 16, true, true);
-  volatile int* abort_flag = &c.abort_flag;
-  uint32_t it = 0, tc = 0, qc = 0;
-  bool issued = false;
-  bool ok = true;
-  while (ok) {
-    const int slot = it % kRing;
-    if (!mbar_wait(&c.item_full[slot], (it / kRing) & 1, abort_flag)) {
-      ok = false;
-      break;
-    }
-    const ItemInfo info = c.ring[slot];
-    ++it;
-    if (info.idx < 0) break;
-    if (info.valid) {
-      const int qb = qc & 1;
-      if (!mbar_wait(&c.q_full[qb], (qc >> 1) & 1, abort_flag)) {
+  // One thread polls the barriers and issues every MMA, running this whole loop alone:
+  // the other lanes wait at the end, so no warp-wide exchange sits between two issues.
+  if ((threadIdx.x & 31) == 0) {
+    const uint32_t idesc_s = umma_idesc_bf16(128, 16, false, false);
+    const uint32_t idesc_o = umma_idesc_bf16(128, 16, true, true);
+    volatile int* abort_flag = &c.abort_flag;
+    uint32_t it = 0, tc = 0, qc = 0;
+    bool issued = false;
+    bool ok = true;
+    while (ok) {
+      const int slot = it % kRing;
+      if (!mbar_wait(&c.item_full[slot], (it / kRing) & 1, abort_flag)) {
         ok = false;
         break;
       }
-      // Issue S^T(j) as soon as tile j has landed and its TMEM buffer is free, and
-      // O^T(j) = V^T P^T as soon as the softmax has written P(j): polled, so that neither
-      // kind of MMA waits behind the other (a late tile must not hold back the P V
-      // that frees an earlier stage).
-      const int nt = (info.key_end - info.key_start + kTileKeys - 1) / kTileKeys;
-      int ns = 0, npv = 0;
-      uint64_t t_last = globaltimer_ns();
-      while (npv < nt) {
-        bool progress = false;
-        if (ns < nt) {
-          const uint32_t cnt = tc + ns;
-          const int st = cnt % kStages, sb = cnt & 1;
-          bool ready = mbar_test(&c.full[st], (cnt / kStages) & 1) && mbar_test(&c.s_free[sb], ((cnt >> 1) & 1) ^ 1);
-          ready = __shfl_sync(0xffffffffu, ready, 0);
-          if (ready) {
-            tc_fence_after();
-            if (lane == 0) {
+      const ItemInfo info = c.ring[slot];
+      ++it;
+      if (info.idx < 0) break;
+      if (info.valid) {
+        const int qb = qc & 1;
+        if (!mbar_wait(&c.q_full[qb], (qc >> 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const uint64_t qdesc = umma_smem_desc(smem_u32(qbuf + qb * kQBytes), 16, 1024, kLayout128B);
+        // Issue S^T(j) as soon as tile j has landed and its TMEM buffer is free, and
+        // O^T(j) = V^T P^T as soon as the softmax has written P(j): polled, so that neither
+        // kind of MMA waits behind the other (a late tile must not hold back the P V
+        // that frees an earlier stage).  The clock is read only while nothing is ready:
+        // the wait is bounded from the first poll that finds nothing to issue.
+        const int nt = (info.key_end - info.key_start + kTileKeys - 1) / kTileKeys;
+        int ns = 0, npv = 0;
+        bool idle = false;
+        uint64_t t_idle = 0;
+        while (npv < nt) {
+          bool progress = false;
+          if (ns < nt) {
+            const uint32_t cnt = tc + ns;
+            const int st = cnt % kStages, sb = cnt & 1;
+            if (mbar_test(&c.full[st], (cnt / kStages) & 1) && mbar_test(&c.s_free[sb], ((cnt >> 1) & 1) ^ 1)) {
+              tc_fence_after();
               const uint64_t a = umma_smem_desc(smem_u32(stages + st * kStageBytes), 16, 1024, kLayout128B);
-              const uint64_t b = umma_smem_desc(smem_u32(qbuf + qb * kQBytes), 16, 1024, kLayout128B);
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk)
                 umma_f16_ss(tmem + 16 * sb, umma_desc_advance(a, (kk >> 2) * kHalfBytes + (kk & 3) * 32),
-                            umma_desc_advance(b, (kk >> 2) * 2048 + (kk & 3) * 32), idesc_s, kk > 0);
+                            umma_desc_advance(qdesc, (kk >> 2) * 2048 + (kk & 3) * 32), idesc_s, kk > 0);
               umma_commit(&c.s_full[sb]);
               if (ns == nt - 1) umma_commit(&c.q_free[qb]);
               issued = true;
+              ++ns;
+              progress = true;
             }
-            __syncwarp();
-            ++ns;
-            progress = true;
           }
-        }
-        if (npv < ns) {
-          const uint32_t cnt = tc + npv;
-          const int st = cnt % kStages, b = cnt & 1;
-          const uint32_t ph = (cnt >> 1) & 1;
-          bool ready = mbar_test(&c.p_full[b], ph) && mbar_test(&c.o_free[b], ph ^ 1);
-          ready = __shfl_sync(0xffffffffu, ready, 0);
-          if (ready) {
-            tc_fence_after();
-            if (lane == 0) {
+          if (npv < ns) {
+            const uint32_t cnt = tc + npv;
+            const int st = cnt % kStages, b = cnt & 1;
+            const uint32_t ph = (cnt >> 1) & 1;
+            if (mbar_test(&c.p_full[b], ph) && mbar_test(&c.o_free[b], ph ^ 1)) {
+              tc_fence_after();
               const uint64_t a =
                   umma_smem_desc(smem_u32(stages + st * kStageBytes + kKBytes), kHalfBytes, 1024, kLayout128B);
               const uint64_t bd = umma_smem_desc(smem_u32(pbuf + b * kPBytes), 128, 2048, kLayoutNone);
@@ -423,32 +419,33 @@ __device__ void mma_warp(const DecodeParams& P, Ctl& c, uint8_t* stages, uint8_t
               umma_commit(&c.o_full[b]);
               umma_commit(&c.p_free[b]);
               umma_commit(&c.empty[st]);
+              ++npv;
+              progress = true;
             }
-            __syncwarp();
-            ++npv;
-            progress = true;
+          }
+          if (progress) {
+            idle = false;
+          } else if (!idle) {
+            idle = true;
+            t_idle = globaltimer_ns();
+          } else if (*abort_flag || globaltimer_ns() - t_idle > kWaitTimeoutNs) {
+            ok = false;
+            break;
           }
         }
-        if (progress) {
-          t_last = globaltimer_ns();
-        } else if (*abort_flag || globaltimer_ns() - t_last > kWaitTimeoutNs) {
-          ok = false;
-          break;
-        }
+        tc += nt;
+        ++qc;
       }
-      tc += nt;
-      ++qc;
+      if (!ok) break;
+      mbar_arrive(&c.item_empty[slot]);
     }
-    if (!ok) break;
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&c.item_empty[slot]);
-  }
-  if (!ok && !*abort_flag && lane == 0) raise_abort(c, P.err);
-  if (issued && lane == 0) {
-    // every MMA issued so far, and the barrier arrivals its commits trigger, must be
-    // complete before TMEM is freed and the CTA's shared memory goes away
-    umma_commit(&c.drain);
-    mbar_wait(&c.drain, 0, nullptr);
+    if (!ok && !*abort_flag) raise_abort(c, P.err);
+    if (issued) {
+      // every MMA issued so far, and the barrier arrivals its commits trigger, must be
+      // complete before TMEM is freed and the CTA's shared memory goes away
+      umma_commit(&c.drain);
+      mbar_wait(&c.drain, 0, nullptr);
+    }
   }
   __syncwarp();
 }
