@@ -84,7 +84,7 @@ size_t layout_workspace(void* base, int32_t num_seqs, int32_t hkv, int32_t group
   w.counters = static_cast<int32_t*>(take(kNumQueueCounters * sizeof(int32_t)));
   w.dec_prefix = static_cast<int32_t*>(take((static_cast<size_t>(num_seqs) + 1) * sizeof(int32_t)));
   w.pre_prefix = static_cast<int32_t*>(take((static_cast<size_t>(num_seqs) + 1) * sizeof(int32_t)));
-  w.pre_order = static_cast<int32_t*>(take(static_cast<size_t>(max_pre_units) * sizeof(int32_t)));
+  w.pre_order = static_cast<int32_t*>(take(static_cast<size_t>(max_pre_units) * 2 * sizeof(int32_t)));
   w.dec_order = static_cast<int32_t*>(take(static_cast<size_t>(num_seqs) * sizeof(int32_t)));
   w.dec_start = static_cast<int32_t*>(take((static_cast<size_t>(num_seqs) + 1) * sizeof(int32_t)));
   w.unit_bad = static_cast<int32_t*>(take(static_cast<size_t>(num_seqs) * hkv * sizeof(int32_t)));

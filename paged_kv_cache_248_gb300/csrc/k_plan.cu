@@ -259,11 +259,11 @@ __device__ void order_prefill_pairs(const PlanArgs& p) {
       const int npair = (p.pre_prefix[i + 1] - p.pre_prefix[i]) / p.hkv;
       for (int pl = 0; pl < npair; ++pl) {
         const int key = min(pair_key_tiles(ctx, q_len, p.rows_q, pl), kOrderBuckets - 1);
-        fn(kOrderBuckets - 1 - key, base + pl);  // heavier pairs in lower buckets
+        fn(kOrderBuckets - 1 - key, base + pl, i);  // heavier pairs in lower buckets
       }
     }
   };
-  for_each_pair([&](int b, int) { atomicAdd(&bucket[b], 1); });
+  for_each_pair([&](int b, int, int) { atomicAdd(&bucket[b], 1); });
   __syncthreads();
   {
     const int v[3] = {bucket[tid], 0, 0};
@@ -272,9 +272,11 @@ __device__ void order_prefill_pairs(const PlanArgs& p) {
     bucket[tid] = ex[0];  // first position of the bucket
   }
   __syncthreads();
-  for_each_pair([&](int b, int id) {
+  // each position gets the pair's id and its request, so that a CTA taking the pair
+  // needs no search for the request
+  for_each_pair([&](int b, int id, int i) {
     const int pos = atomicAdd(&bucket[b], 1);
-    if (pos < p.max_pre_units) p.pre_order[pos] = id;
+    if (pos < p.max_pre_units) reinterpret_cast<int2*>(p.pre_order)[pos] = make_int2(id, i);
   });
 }
 

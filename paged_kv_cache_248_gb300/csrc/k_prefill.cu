@@ -98,7 +98,7 @@ struct PrefillParams {
   const int32_t* seq_lens;
   const int32_t* qsl;
   const int32_t* pre_prefix;
-  const int32_t* pre_order;  // pairs heaviest first: ids pre_prefix[i] / hkv + pl
+  const int32_t* pre_order;  // pairs heaviest first: (id pre_prefix[i] / hkv + pl, request i) per position
   int32_t* queue;
   uint32_t* err;
   int64_t num_blocks;
@@ -233,22 +233,18 @@ __device__ PItem make_item(const PrefillParams& P, int idx, int total) {
     r.idx = -1;
     return r;
   }
-  // the planner's order of (request, pair) units, heaviest first; the kv heads of a
-  // unit are consecutive items
-  const int unit = P.pre_order[idx / P.hkv];
-  int lo = 0, hi = P.num_seqs - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (P.pre_prefix[mid] <= unit * P.hkv) lo = mid; else hi = mid - 1;
-  }
-  const int i = lo;
+  // the planner's order of (request, pair) units, heaviest first, with each unit's
+  // request; the kv heads of a unit are consecutive items
+  const int2 ord = reinterpret_cast<const int2*>(P.pre_order)[idx / P.hkv];
+  const int unit = ord.x;
+  const int i = ord.y >= 0 && ord.y < P.num_seqs ? ord.y : 0;
   const int base = P.pre_prefix[i];
   const int cnt = P.pre_prefix[i + 1] - base;
   const int npair = cnt / P.hkv;
+  const int pl = unit - base / P.hkv;
   r.idx = idx;
   r.seq = i;
-  if (npair <= 0) return r;  // inconsistent plan: invalid item
-  const int pl = unit - base / P.hkv;
+  if (npair <= 0 || ord.y != i || pl < 0 || pl >= npair) return r;  // inconsistent plan: invalid item
   const int pair = npair - 1 - pl;  // pl = 0: the request's latest (heaviest) query tiles
   r.head = idx % P.hkv;
   const int64_t q0 = P.qsl[i], q1 = P.qsl[i + 1];

@@ -143,7 +143,7 @@ struct Workspace {
   int32_t* counters;     // [kNumQueueCounters] work-queue heads
   int32_t* dec_prefix;   // [num_seqs + 1] exclusive prefix of decode items
   int32_t* pre_prefix;   // [num_seqs + 1] exclusive prefix of prefill items
-  int32_t* pre_order;    // [max_pre_units] prefill pairs, heaviest first (ids in request order)
+  int32_t* pre_order;    // [2 * max_pre_units] prefill pairs, heaviest first: (pair id in request order, its request)
   int32_t* dec_order;    // [num_seqs] decode requests, largest item first (small batches)
   int32_t* dec_start;    // [num_seqs + 1] exclusive prefix of decode items in that order
   int32_t* unit_bad;     // [num_seqs * hkv] a split saw a bad block id
@@ -204,7 +204,7 @@ struct PlanArgs {
   const int32_t* bt = nullptr;
   CascadeArgs cas{};
   int32_t cas_rows = 0;  // member requests per cascade item
-  int32_t* pre_order = nullptr;  // heaviest-first order of the prefill pairs
+  int32_t* pre_order = nullptr;  // heaviest-first order of the prefill pairs, two ints per position
   int32_t* dec_order = nullptr;  // largest-item-first order of the decode requests
   int32_t* dec_start = nullptr;
   int32_t num_sms = 0;
