@@ -104,6 +104,7 @@ struct PrefillParams {
   int64_t num_blocks;
   int64_t num_tokens;
   int32_t num_seqs, max_blocks, hkv, group, gp, rows_q, hq;
+  int32_t out_v8;  // out is 32-byte aligned (every row then is): whole-sector stores
   float scale_log2;
   // shared-prefix mode
   const __nv_bfloat16* q;
@@ -219,6 +220,13 @@ __device__ __forceinline__ float row_exp_to_p(uint32_t taddr, int nvis, float sc
     if (h < 3) tmem_ld32_wait(nxt);
   }
   return (ls[0] + ls[1]) + (ls[2] + ls[3]);
+}
+
+// One 32-byte global store (a whole sector) of eight 32-bit words; p is 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+               "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
 }
 
 __device__ __forceinline__ void raise_abort(Ctl& c, uint32_t* err) {
@@ -762,7 +770,21 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uin
     for (int h = 0; h < 2; ++h) {
       uint32_t v[64];
       tmem_ld64_sync(tmem + lane_off + o_col + 64 * h, v);
-      if (row_out) {
+      if (row_out && P.out_v8) {
+        // whole 32-byte sectors per store (the lanes of a warp write 32 different rows,
+        // so 16-byte stores would leave every sector half written)
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          uint32_t wv[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(v[16 * ch + 2 * q]) * inv,
+                                                      __uint_as_float(v[16 * ch + 2 * q + 1]) * inv);
+            wv[q] = *reinterpret_cast<uint32_t*>(&h2);
+          }
+          st_global_v8(orow + 64 * h + 16 * ch, wv);
+        }
+      } else if (row_out) {
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch) {
           uint32_t wv[4];
@@ -865,6 +887,7 @@ int launch_prefill_tc(const AttnArgs& a, const Workspace& ws, int num_sms, uint3
   if (st) return st;
   PrefillParams p;
   p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.out_v8 = (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0 ? 1 : 0;
   p.bt = a.block_tables;
   p.seq_lens = a.seq_lens;
   p.qsl = a.qsl;

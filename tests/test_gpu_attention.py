@@ -262,6 +262,35 @@ def test_mixed_batch_equals_separate_calls_bitwise(pkv):
         assert torch.equal(one, whole[qsl[i]:qsl[i + 1]]), i
 
 
+def test_output_aligned_to_16_bytes_only(pkv):
+    # The C ABI asks only 16-byte alignment of out; the prefill epilogue stores whole
+    # 32-byte sectors when out allows it and 16-byte pieces otherwise.  An out that
+    # starts 16 bytes past a 32-byte boundary takes the narrow stores; the values must
+    # be the same bits as with an aligned out, and the bytes around out untouched.
+    w = wl.random_case(41, num_seqs=8, max_ctx=900, max_q=300, group=4, num_kv_heads=2, head_dim=128,
+                       dtype="bf16", decode_frac=0.3)
+    t_cpu = w.make_tensors("cpu")
+    t = {k: v.cuda() for k, v in t_cpu.items()}
+    m = to_gpu_meta(w)
+    args = (t["q"], t["k_cache"], t["v_cache"], m["block_tables"], m["seq_lens"], m["query_start_loc"], w.scale,
+            w.max_query_len, w.max_seq_len)
+    aligned = pkv.paged_attention(*args)
+    assert pkv.pkv_get_last_error() == 0
+    n = t["q"].numel()
+    flat = torch.full((n + 32,), 7.0, dtype=torch.bfloat16, device="cuda")
+    assert flat.data_ptr() % 32 == 0
+    shifted = flat[8:8 + n].view(t["q"].shape)  # 8 bf16 = 16 bytes past the boundary
+    assert shifted.data_ptr() % 32 == 16
+    pkv.paged_attention(*args, out=shifted)
+    assert pkv.pkv_get_last_error() == 0
+    assert torch.equal(shifted, aligned)
+    assert torch.all(flat[:8] == 7.0) and torch.all(flat[8 + n:] == 7.0)
+    # attention alone read the pool as drawn (no new tokens were written)
+    ref = oracle.attention(bits(t_cpu["q"]), bits(t_cpu["k_cache"]), bits(t_cpu["v_cache"]), w.block_tables,
+                           w.seq_lens, w.query_start_loc, w.scale)
+    compare(shifted, ref, "bf16", w.name)
+
+
 @pytest.mark.parametrize("seed,group,hkv", [(13, 1, 4), (14, 2, 2), (16, 4, 8), (17, 8, 2)])
 def test_repeated_calls_match_oracle_and_each_other(pkv, seed, group, hkv):
     # Which CTA runs which item, and when, changes from call to call; the results must
