@@ -45,9 +45,9 @@ METRIC = "decode KV-read GB/s (% of HBM peak); mixed-step tokens/sec at 1 GB300"
 # It scales to other workloads by the bytes processed, and it is reported only while
 # the profiled sources are unchanged.
 NCU_TRAFFIC = {
-    "decode": {"ratio": 509.41 / 503.62,
+    "decode": {"ratio": 509.67 / 503.62,
                "sources": ("k_decode.cu", "ptx.cuh", "pkv_internal.cuh"),
-               "sha256": "2002c13c93bb771421ad1d0ba8e20d8572c61dff512cd88e9e2ac98afe77d180"},
+               "sha256": "906681adbc2859544a1f55c3f7f840087b3d419a4792f37d1198655acebb088f"},
 }
 
 

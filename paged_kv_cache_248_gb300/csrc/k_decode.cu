@@ -805,8 +805,10 @@ struct MergeParams {
   int32_t num_seqs, hkv, group, hq;
 };
 
+// Two CTAs per SM where the registers allow it (GP <= 8), so that a batch's (request, kv
+// head) units run in one wave rather than two.
 template <int GP>
-__global__ void __launch_bounds__(128 * kMergeGroups) merge_kernel(const MergeParams P) {
+__global__ void __launch_bounds__(128 * kMergeGroups, GP <= 8 ? 2 : 0) merge_kernel(const MergeParams P) {
   __shared__ float xfer[GP][3][128];  // one run's (max, sum, accumulator) handed to run 0
   const int d = threadIdx.x % 128, run = threadIdx.x / 128;
   const int64_t n_units = static_cast<int64_t>(P.counters[kMergeCountSlot]) * P.hkv;

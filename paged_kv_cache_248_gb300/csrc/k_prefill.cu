@@ -740,16 +740,19 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uin
     if (kCas) {
       // the row's partial: accumulator [slot][head][128], then max and sum
       const int64_t cslot = (static_cast<int64_t>(entry) * P.hkv + info.head) * P.cas_np_max + info.split;
-      float4* dst = reinterpret_cast<float4*>(P.cas_o + (cslot * P.gp + rg) * 128);
+      // whole 32-byte sectors per store (workspace rows are 512-byte multiples from a
+      // 256-byte aligned base)
+      float* dst = P.cas_o + (cslot * P.gp + rg) * 128;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t v[64];
         tmem_ld64_sync(tmem + lane_off + o_col + 64 * h, v);
         if (cas_live) {
 #pragma unroll
-          for (int q = 0; q < 16; ++q)
-            dst[16 * h + q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                          __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+          for (int q = 0; q < 8; ++q) {
+            const uint32_t(&w8)[8] = *reinterpret_cast<const uint32_t(*)[8]>(v + 8 * q);
+            st_global_v8(dst + 64 * h + 8 * q, w8);
+          }
         }
       }
       if (cas_live) {
