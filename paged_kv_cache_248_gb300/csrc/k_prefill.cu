@@ -743,17 +743,19 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uin
       // whole 32-byte sectors per store (workspace rows are 512-byte multiples from a
       // 256-byte aligned base)
       float* dst = P.cas_o + (cslot * P.gp + rg) * 128;
+      uint32_t v[4][32];  // the whole row from TMEM before any store
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t v[64];
-        tmem_ld64_sync(tmem + lane_off + o_col + 64 * h, v);
-        if (cas_live) {
+      for (int h = 0; h < 4; ++h) tmem_ld32_issue(tmem + lane_off + o_col + 32 * h, v[h]);
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const uint32_t(&w8)[8] = *reinterpret_cast<const uint32_t(*)[8]>(v + 8 * q);
-            st_global_v8(dst + 64 * h + 8 * q, w8);
+      for (int h = 0; h < 4; ++h) tmem_ld32_wait(v[h]);
+      if (cas_live) {
+#pragma unroll
+        for (int h = 0; h < 4; ++h)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t(&w8)[8] = *reinterpret_cast<const uint32_t(*)[8]>(v[h] + 8 * q);
+            st_global_v8(dst + 32 * h + 8 * q, w8);
           }
-        }
       }
       if (cas_live) {
         P.cas_ml[(cslot * P.gp + rg) * 2] = m_ref;
@@ -769,35 +771,40 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uin
       continue;
     }
     const float inv = bad ? 0.f : 1.f / l_sum;
+    // the whole O row is loaded from TMEM before any store: a load issued after stores
+    // waits behind them in the memory pipeline
+    uint32_t v[4][32];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      uint32_t v[64];
-      tmem_ld64_sync(tmem + lane_off + o_col + 64 * h, v);
+    for (int h = 0; h < 4; ++h) tmem_ld32_issue(tmem + lane_off + o_col + 32 * h, v[h]);
+#pragma unroll
+    for (int h = 0; h < 4; ++h) tmem_ld32_wait(v[h]);
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
       if (row_out && P.out_v8) {
         // whole 32-byte sectors per store (the lanes of a warp write 32 different rows,
         // so 16-byte stores would leave every sector half written)
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
+        for (int ch = 0; ch < 2; ++ch) {
           uint32_t wv[8];
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(v[16 * ch + 2 * q]) * inv,
-                                                      __uint_as_float(v[16 * ch + 2 * q + 1]) * inv);
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(v[h][16 * ch + 2 * q]) * inv,
+                                                      __uint_as_float(v[h][16 * ch + 2 * q + 1]) * inv);
             wv[q] = *reinterpret_cast<uint32_t*>(&h2);
           }
-          st_global_v8(orow + 64 * h + 16 * ch, wv);
+          st_global_v8(orow + 32 * h + 16 * ch, wv);
         }
       } else if (row_out) {
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
+        for (int ch = 0; ch < 4; ++ch) {
           uint32_t wv[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(v[8 * ch + 2 * q]) * inv,
-                                                      __uint_as_float(v[8 * ch + 2 * q + 1]) * inv);
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(v[h][8 * ch + 2 * q]) * inv,
+                                                      __uint_as_float(v[h][8 * ch + 2 * q + 1]) * inv);
             wv[q] = *reinterpret_cast<uint32_t*>(&h2);
           }
-          reinterpret_cast<uint4*>(orow)[8 * h + ch] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+          reinterpret_cast<uint4*>(orow)[4 * h + ch] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
         }
       }
     }
