@@ -22,8 +22,9 @@
 //              block's physical location (the block-table gather), 128-byte swizzle.
 //              K tiles go into a 2-slot ring and V tiles into a 3-slot one, each tile's
 //              K and V issued together.
-//   warp 1     MMA issuer.  Per key tile j and query tile w it issues O_w += P_w(j-1)
-//              V(j-1), then S_w(j) = Q_w K(j)^T.  S_w lives in TMEM; the softmax writes
+//   warp 1     MMA issuer; one thread runs the whole loop, so no warp convergence sits
+//              between two MMA bursts.  Per key tile j and query tile w it issues O_w +=
+//              P_w(j-1) V(j-1), then S_w(j) = Q_w K(j)^T.  S_w lives in TMEM; the softmax writes
 //              P_w as bf16 over the first 64 of S_w's columns and the P V MMA reads its
 //              A operand from there.  MMAs issued by one thread complete in order, so
 //              S_w(j+1) cannot overwrite P_w(j) before P_w(j) V(j) has read it, and S_w(j)
@@ -35,7 +36,9 @@
 //              causal mask, and keeps a per-row reference maximum; only when a row's
 //              maximum grows by more than 2^8 does the warp rescale its O rows in TMEM.
 //              Two scores go through each packed fp32x2 FMA and add, and each
-//              three-input max.  The final O / l is stored per row.
+//              three-input max.  The softmax warps also release the K and V ring slots
+//              (plain arrivals: S_w(j) complete means every earlier MMA is).  The final
+//              O / l is stored per row, the whole row loaded from TMEM first.
 // All waits are bounded (see ptx.cuh); a timeout raises the CTA abort flag.
 //
 // Shared-prefix (cascade) mode, kCas = true.  The same pipeline attends the member
