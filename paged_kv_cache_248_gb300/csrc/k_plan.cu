@@ -127,7 +127,18 @@ __device__ void plan_cascade(const PlanArgs& p) {
     const int32_t* pre = g.tables + static_cast<int64_t>(group_of(k)) * g.max_blocks;
     const int j1 = min(pb, j0 + kChunk);
     int diff = 0;
-    for (int j = j0; j < j1; ++j) diff |= __ldg(own + j) != __ldg(pre + j);
+    if (j1 - j0 == kChunk && ((reinterpret_cast<uintptr_t>(own + j0) | reinterpret_cast<uintptr_t>(pre + j0)) & 15) == 0) {
+      // a whole chunk of both rows in four 16-byte loads each: the warp's lanes read 32
+      // different rows, so fewer, wider requests matter
+#pragma unroll
+      for (int q = 0; q < kChunk / 4; ++q) {
+        const int4 a = __ldg(reinterpret_cast<const int4*>(own + j0) + q);
+        const int4 b = __ldg(reinterpret_cast<const int4*>(pre + j0) + q);
+        diff |= (a.x != b.x) | (a.y != b.y) | (a.z != b.z) | (a.w != b.w);
+      }
+    } else {
+      for (int j = j0; j < j1; ++j) diff |= __ldg(own + j) != __ldg(pre + j);
+    }
     if (diff) *reinterpret_cast<volatile int32_t*>(p.member_ok + k) = 0;
   }
   __syncthreads();
