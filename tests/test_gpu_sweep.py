@@ -56,7 +56,7 @@ def draw_mixed(seed: int):
         num_seqs -= 1
 
 
-@pytest.mark.parametrize("seed", range(48))
+@pytest.mark.parametrize("seed", range(96))
 def test_mixed_step_sweep(pkv, seed):
     w = draw_mixed(seed)
     t_cpu = w.make_tensors("cpu")
@@ -93,7 +93,7 @@ def dev(a):
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
 
-@pytest.mark.parametrize("seed", range(24))
+@pytest.mark.parametrize("seed", range(48))
 def test_shared_prefix_sweep(pkv, seed):
     w, hints = draw_shared(seed)
     t_cpu = w.make_tensors("cpu")
