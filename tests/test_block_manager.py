@@ -226,3 +226,109 @@ def test_prefix_groups_limits_and_errors(pkv):
     assert len(single[1]) == 0 and single[2].tolist() == [0]
     with pytest.raises(ValueError):
         bm.prefix_groups([0, 99], max_prefix_blocks=4)
+
+
+def _check_pool(bm, live, n_blocks):
+    """Invariants of the pool against the model ``live`` (request -> its token ids)."""
+    refs = {}
+    unused = 0
+    for r, toks in live.items():
+        table = bm.block_table(r)
+        assert len(table) == (toks.size + BLOCK - 1) // BLOCK, r
+        assert len(set(table)) == len(table), r                      # no block twice in one table
+        unused += len(table) * BLOCK - toks.size
+        for k, b in enumerate(table):
+            assert 0 <= b < n_blocks
+            refs.setdefault(b, []).append((r, k))
+    # blocks in use are exactly the referenced ones; every other block is in the free queue
+    assert bm.num_free == n_blocks - len(refs)
+    u = bm.usage()
+    assert u["blocks_in_use"] == len(refs)
+    assert u["tokens_held"] == sum(t.size for t in live.values())
+    assert u["unused_slots"] == unused
+    # every reference to a block sees the same token ids in the slots it has filled
+    for b, holders in refs.items():
+        first = None
+        for r, k in holders:
+            content = live[r][k * BLOCK:(k + 1) * BLOCK]
+            if first is None:
+                first = content
+            m = min(first.size, content.size)
+            assert np.array_equal(first[:m], content[:m]), (b, holders)
+    return refs
+
+
+@pytest.mark.parametrize("seed", [21, 22, 23, 24])
+def test_random_walk_keeps_the_pool_consistent(pkv, seed):
+    # New requests (often extending a known prompt, so prefix hashes hit), appends,
+    # forks, copy-on-write and frees, in a seeded random order on a small pool so that
+    # allocation also fails; the pool is checked against a model after every operation.
+    rng = np.random.default_rng(seed)
+    n_blocks = 48
+    bm = pkv.BlockManager(n_blocks)
+    vocab = 5  # few distinct token ids: equal blocks are common
+    prompts = [rng.integers(0, vocab, size=int(rng.integers(1, 90))).astype(np.int32) for _ in range(6)]
+    live, next_id, hits = {}, 0, 0
+    for _ in range(600):
+        op = rng.random()
+        if op < 0.35 or not live:
+            base = prompts[int(rng.integers(len(prompts)))]
+            toks = np.concatenate([base[:int(rng.integers(0, base.size + 1))],
+                                   rng.integers(0, vocab, size=int(rng.integers(0, 40)))]).astype(np.int32)
+            if toks.size == 0:
+                continue
+            r, next_id = next_id, next_id + 1
+            hit = bm.get_computed_blocks(r, toks)
+            assert 0 <= hit <= toks.size // BLOCK
+            hits += hit
+            if bm.allocate_slots(r, toks.size) is None:
+                bm.free(r)                                    # gives back the blocks it hit
+            else:
+                bm.cache_full_blocks(r, toks)
+                live[r] = toks
+        elif op < 0.55:
+            r = list(live)[int(rng.integers(len(live)))]
+            toks = live[r]
+            add = rng.integers(0, vocab, size=int(rng.integers(1, 24))).astype(np.int32)
+            table = bm.block_table(r)
+            shared = sum(table[-1] in bm.block_table(o) for o in live if o != r) > 0
+            if toks.size % BLOCK and shared:                  # the write would land in a shared block
+                if bm.cow(r, len(table) - 1) is None:
+                    continue
+            if bm.allocate_slots(r, toks.size + add.size) is None:
+                continue
+            live[r] = np.concatenate([toks, add])
+            bm.cache_full_blocks(r, live[r])
+        elif op < 0.68:
+            p = list(live)[int(rng.integers(len(live)))]
+            c, next_id = next_id, next_id + 1
+            bm.fork(p, c)
+            live[c] = live[p].copy()
+            assert bm.block_table(c) == bm.block_table(p)
+        elif op < 0.8:
+            r = list(live)[int(rng.integers(len(live)))]
+            before = bm.block_table(r)
+            k = int(rng.integers(len(before)))
+            others = [o for o in live if o != r]
+            shared = any(before[k] in bm.block_table(o) for o in others)
+            free_before = bm.num_free
+            res = bm.cow(r, k)
+            after = bm.block_table(r)
+            if not shared:
+                assert res == () and after == before
+            elif res is None:
+                assert free_before == 0 and after == before
+            else:
+                src, dst = res
+                assert src == before[k] and after[k] == dst and after[:k] == before[:k] and after[k + 1:] == before[k + 1:]
+                assert all(dst not in bm.block_table(o) for o in others)
+                assert bm.num_free == free_before - 1
+        else:
+            r = list(live)[int(rng.integers(len(live)))]
+            bm.free(r)
+            del live[r]
+        _check_pool(bm, live, n_blocks)
+    assert hits > 0                                           # prefix reuse was exercised
+    for r in list(live):
+        bm.free(r)
+    assert bm.num_free == n_blocks
