@@ -332,3 +332,59 @@ def test_random_walk_keeps_the_pool_consistent(pkv, seed):
     for r in list(live):
         bm.free(r)
     assert bm.num_free == n_blocks
+
+
+@pytest.mark.parametrize("seed", [31, 32, 33])
+def test_prefix_groups_properties_on_random_batches(pkv, seed):
+    # Sharing made by prefix-cache hits and forks; for random batches, the groups must
+    # be exactly the batch's requests that share a first block (in order of first
+    # appearance), each group's prefix the longest run of leading blocks all its
+    # members share (capped), and the member lists a partition of those requests.
+    rng = np.random.default_rng(seed)
+    bm = pkv.BlockManager(4000)
+    prompts = [rng.integers(0, 3, size=int(rng.integers(16, 200))).astype(np.int32) for _ in range(5)]
+    live = []
+    for r in range(120):
+        if live and rng.random() < 0.3:
+            p = live[int(rng.integers(len(live)))]
+            bm.fork(p, r)
+        else:
+            base = prompts[int(rng.integers(len(prompts)))]
+            toks = np.concatenate([base[:int(rng.integers(1, base.size + 1))],
+                                   rng.integers(0, 3, size=int(rng.integers(0, 50)))]).astype(np.int32)
+            bm.get_computed_blocks(r, toks)
+            assert bm.allocate_slots(r, toks.size) is not None
+            bm.cache_full_blocks(r, toks)
+        live.append(r)
+    tables = {r: bm.block_table(r) for r in live}
+    formed = 0
+    for trial in range(20):
+        batch = [live[i] for i in rng.choice(len(live), size=int(rng.integers(1, 60)), replace=False)]
+        cap = int(rng.integers(1, 16))
+        max_groups = int(rng.integers(1, 12))
+        pt, pn, ms, mseq = bm.prefix_groups(batch, cap, max_groups)
+        G = len(pn)
+        formed += G
+        assert G <= max_groups and ms[0] == 0 and len(ms) == G + 1
+        first = [tables[batch[k]][0] for k in range(len(batch))]
+        # groups in order of their first member's batch position, distinct first blocks
+        firsts_seen = []
+        for k, b in enumerate(first):
+            if b not in firsts_seen:
+                firsts_seen.append(b)
+        shared = [b for b in firsts_seen if first.count(b) >= 2]
+        assert G == min(len(shared), max_groups)
+        for g in range(G):
+            members = list(mseq[ms[g]:ms[g + 1]])
+            assert members == [k for k, b in enumerate(first) if b == shared[g]]   # all of them, batch order
+            n = int(pn[g])
+            assert 1 <= n <= cap
+            pre = list(pt[g][:n])
+            assert all(x == -1 for x in pt[g][n:])
+            for k in members:
+                assert tables[batch[k]][:n] == pre
+            # longest: at the cap, or some member ends there, or two members differ there
+            if n < cap:
+                nxt = [tables[batch[k]][n] if len(tables[batch[k]]) > n else None for k in members]
+                assert None in nxt or len(set(nxt)) > 1
+    assert formed > 0
