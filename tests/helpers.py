@@ -106,3 +106,41 @@ def sub_batch(w, t_gpu, seq_ids):
                              query_start_loc=np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32),
                              block_tables=bt2)
     return w2, t_sub, rows
+
+
+def host_requests(w, pool_k, pool_v, t_gpu, seq_ids):
+    """Requests ``seq_ids`` of a batch as a self-contained host batch for the oracle.
+
+    Only the blocks those requests reference (their tables, and the sources of their
+    copy-on-write pairs) are copied from ``pool_k``/``pool_v`` -- device pools as
+    they were before the GPU step -- and renumbered 0..n-1; the oracle's result does
+    not depend on physical ids.  Returns (workload, host tensors, the requests' query
+    rows in the full batch, the original ids of the copied blocks)."""
+    seq_ids = np.asarray(seq_ids, np.int64)
+    bt = w.block_tables[seq_ids]
+    ids = [bt[bt >= 0]]
+    cow = w.cow_src is not None
+    if cow:
+        ids += [w.cow_src[seq_ids], w.cow_dst[seq_ids]]
+    used = np.unique(np.concatenate(ids)).astype(np.int64)
+    remap = np.full(w.num_blocks, -1, np.int32)
+    remap[used] = np.arange(len(used), dtype=np.int32)
+    bt2 = np.where(bt >= 0, remap[np.maximum(bt, 0)], -1).astype(np.int32)
+    qsl = w.query_start_loc
+    rows = np.concatenate([np.arange(qsl[i], qsl[i + 1]) for i in seq_ids]).astype(np.int64)
+    q_lens = (qsl[seq_ids + 1] - qsl[seq_ids]).astype(np.int32)
+    idx = torch.from_numpy(used).to(pool_k.device)
+    ridx = torch.from_numpy(rows).to(pool_k.device)
+    t_sub = {"k_cache": pool_k.index_select(0, idx).cpu(),
+             "v_cache": pool_v.index_select(0, idx).cpu(),
+             "q": t_gpu["q"].index_select(0, ridx).cpu(),
+             "k_new": t_gpu["k_new"].index_select(0, ridx).cpu(),
+             "v_new": t_gpu["v_new"].index_select(0, ridx).cpu()}
+    extra = {}
+    if cow:
+        extra = dict(cow_src=remap[w.cow_src[seq_ids]].astype(np.int32),
+                     cow_dst=remap[w.cow_dst[seq_ids]].astype(np.int32))
+    w2 = dataclasses.replace(w, num_blocks=len(used), seq_lens=w.seq_lens[seq_ids].copy(),
+                             query_start_loc=np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32),
+                             block_tables=bt2, block_tables_before_cow=None, **extra)
+    return w2, t_sub, rows, used
