@@ -2,22 +2,21 @@
  * pkv_blocks.h -- C ABI of the host-side KV block manager in libpkv.
  *
  * This is the bookkeeping that produces the block tables the GPU path consumes.
- * It follows the "vLLM's PagedAttention" teardown (arcyou-site):
- *  - section "PagedAttention: the KV cache is paged, like virtual memory":
- *    - the pool is sized once and cut into 16-token blocks;
- *    - allocate_slots takes ceil(new tokens / 16) blocks off a free queue, or returns
- *      None when the pool cannot cover them;
- *    - every full block is hashed by chaining the previous block's hash with this
- *      block's token ids, so a hash covers the whole prefix;
- *    - a request whose prefix hashes match reuses those physical blocks (reference
- *      count + 1, no copy);
- *    - a block returns to the free queue when its count reaches zero, and
- *      cached-but-free blocks sit at its tail so they are evicted last (LRU);
- *  - section "What happens when the blocks run out": freeing a request releases its
- *    tail blocks first, so its prompt prefix tends to survive in the cache;
- *  - "The 1960s Operating System Trick ..." page, Technical Details: parallel samples
- *    share blocks until they diverge; copy-on-write duplicates only the block that
- *    changes.
+ * What it implements, and where the pages state it:
+ *  - "vLLM's PagedAttention" teardown (arcyou-site), section "PagedAttention: the KV
+ *    cache is paged, like virtual memory":
+ *    - one fixed pool of 16-token blocks;
+ *    - allocate_slots hands out ceil(new tokens / 16) blocks, or nothing at all (None,
+ *      here -1) if the pool is short;
+ *    - the hash of a request's block i depends on blocks 0..i, so two requests
+ *      with equal hashes at block i have equal prefixes up to there;
+ *    - a hit hands out the cached physical block again and counts one more user;
+ *    - at zero users a block is free again, but freed blocks that still carry a
+ *      hash are handed out only after blocks that never did, oldest first;
+ *  - same page, section "What happens when the blocks run out": a freed request's
+ *    blocks are queued last block first, so its first blocks are the last reused;
+ *  - "The 1960s Operating System Trick ..." page, Technical Details: samples of one
+ *    prompt use the same blocks, and the one block about to change is copied first.
  *
  * All calls are host-only and not thread-safe (one manager per scheduler thread).
  * Requests are named by caller-chosen int64 ids.  Functions returning int return

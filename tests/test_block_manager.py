@@ -1,17 +1,17 @@
 """Host block manager (libpkv, include/pkv_blocks.h) against what the pages state.
 
 "vLLM's PagedAttention" teardown, section "PagedAttention: the KV cache is paged":
-  * allocate_slots takes ceil(new tokens / 16) blocks, or returns None when the pool
-    cannot cover them;
-  * full blocks are hashed by chaining the parent block's hash with the block's token
-    ids, so equal prefixes give equal hashes and a new request with the same prompt
-    prefix reuses the physical blocks (reference count + 1, no copy);
-  * a block returns to the free pool at reference count zero, and cached-but-free
-    blocks sit at the tail of the free queue so they are evicted last.
-Section "What happens when the blocks run out": freeing evicts a request's tail
-blocks first, so its prompt prefix tends to survive.
-"The 1960s Operating System Trick ..." page, Technical Details: samples share blocks
-until they diverge; copy-on-write duplicates only the block that changes.
+  * a request gets ceil(new tokens / 16) blocks, or none at all (None) if the pool is
+    short;
+  * block i's hash depends on blocks 0..i, so a second request with the same first
+    tokens finds the first one's physical blocks and uses them too (one more user,
+    nothing copied);
+  * a block with no users is free again; freed blocks that still carry a hash are
+    reused only after blocks that never did.
+Section "What happens when the blocks run out": a freed request's blocks are queued
+last block first, so its first blocks survive longest.
+"The 1960s Operating System Trick ..." page, Technical Details: samples of one prompt
+use the same blocks; only the block about to change is copied.
 """
 import numpy as np
 import pytest
