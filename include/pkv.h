@@ -223,19 +223,20 @@ PKV_API int paged_attention_step(const void* q, const void* k_new, const void* v
  * paged_attention_noalloc -- paged_attention() for callers that cannot let a library
  * allocate device memory.  The pages have no counterpart for this call; it exists
  * for deployment.  paged_attention() grows a workspace with cudaMalloc when a batch
- * needs more split-KV scratch; a caller whose allocator must own every byte of
- * device memory, a runtime that captures the step into a CUDA graph (allocation is
- * not allowed inside a capture), or a service that forbids allocation after start-up
- * cannot accept that.  This call computes the same result with its scratch in a
- * fixed 16 MiB static device array that the library holds on every GPU that loads
- * it, until the process exits.
+ * needs more split-KV scratch; a caller whose allocator must account for every byte
+ * of device memory, or a service that reserves its memory at start-up and forbids
+ * allocation afterwards, cannot accept that.  This call computes the same result
+ * with its scratch in a fixed 16 MiB static device array that the library holds on
+ * every GPU that loads it, until the process exits.
  *  - Same arguments and results as paged_attention(), bf16 with head_dim 128 only.
  *  - error_bits: optional device uint32 the kernels OR their data-error bits into
  *    (the bits of pkv_peek_error_bits); NULL discards them.  The caller clears it.
  *  - A batch whose scratch need exceeds the array returns PKV_ERR_NO_MEMORY and
  *    launches nothing.  The need is about num_seqs * num_kv_heads *
  *    ceil(max_seq_len / 1024) * GP * 520 bytes plus a few arrays per request, GP
- *    being the query-head group size rounded up to 4, 8 or 16.
+ *    being the query-head group size rounded up to 4, 8 or 16.  A batch that
+ *    paged_attention() refuses as unsupported (2^31 or more split items) returns
+ *    PKV_ERR_UNSUPPORTED here too.
  *  - The first call on a device looks up the array's device address (with that
  *    device current); make it before any stream capture.
  *  - All calls share the array and the library re-zeroes what each call needs, but

@@ -283,6 +283,13 @@ int attention_impl(const void* q, const void* k_new, const void* v_new, const vo
   if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !query_start_loc || !out)
     return PKV_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return PKV_ERR_INVALID_ARG;
+  if (cache->dtype == PKV_BF16) {  // sizes the tensor-core path cannot index, refused before any CUDA call
+    const int32_t group = num_q_heads / cache->num_kv_heads;
+    if (group > 16) return PKV_ERR_UNSUPPORTED;
+    const int64_t splits = (static_cast<int64_t>(max_seq_len) + kSplitKeys - 1) / kSplitKeys;
+    if (static_cast<int64_t>(num_seqs) * cache->num_kv_heads * splits >= (int64_t(1) << 31))
+      return PKV_ERR_UNSUPPORTED;
+  }
   DeviceCtx* ctx = device_ctx(&st);
   if (!ctx) return st;
   AttnArgs a{q,        k_cache,    v_cache,       *cache,      block_tables, max_blocks_per_seq, seq_lens,

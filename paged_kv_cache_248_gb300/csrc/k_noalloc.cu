@@ -3,12 +3,13 @@
 // allocated on demand.
 //
 // Who needs this.  paged_attention() grows a device workspace with cudaMalloc the
-// first time a batch needs more split-KV scratch.  Some callers cannot let a
-// library allocate: code running under a custom or pooled allocator that must own
-// every byte of device memory, runtimes that record a CUDA graph once and replay it
-// (an allocation inside the captured region is not allowed), and environments that
-// forbid allocation after start-up.  This entry point gives them the same attention
-// with scratch that exists from the moment the library is loaded.
+// first time a batch needs more split-KV scratch than it has.  Some callers cannot
+// let a library allocate: a serving process whose pooled or custom allocator must
+// account for every byte of device memory (memory taken behind its back can make
+// its own later allocations fail at the worst moment), and deployments that reserve
+// all device memory at start-up and allow no allocation afterwards.  This entry
+// point gives them the same attention with scratch that exists from the moment the
+// library is loaded.
 //
 // The scratch is g_noalloc_scratch below: kNoAllocScratchBytes (16 MiB) of device
 // memory that every GPU which loads the library holds until the process exits.  A
@@ -88,7 +89,7 @@ extern "C" PKV_API int paged_attention_noalloc(const void* q, const void* k_cach
   const int32_t gp = group <= 4 ? 4 : (group <= 8 ? 8 : 16);
   const int64_t max_splits = (static_cast<int64_t>(max_seq_len) + kSplitKeys - 1) / kSplitKeys;
   const int64_t max_dec_items = static_cast<int64_t>(num_seqs) * hkv * max_splits;
-  if (max_dec_items >= (int64_t(1) << 31)) return PKV_ERR_NO_MEMORY;
+  if (max_dec_items >= (int64_t(1) << 31)) return PKV_ERR_UNSUPPORTED;  // as paged_attention()
   const int64_t max_pre_units = max_prefill_units(num_tokens, num_seqs, gp);
   const size_t need = layout_workspace(nullptr, num_seqs, hkv, gp, cache->head_dim, max_dec_items, max_pre_units,
                                        nullptr);

@@ -105,3 +105,21 @@ def test_cascade_host_checks_fail_without_launching(lib):
     assert lib.paged_attention_cascade(*args, ctypes.byref(g), fake, None) == pkv.PKV_ERR_INVALID_ARG
     bad_scale = args[:-1] + (ctypes.c_float(float("nan")),)
     assert lib.paged_attention_cascade(*bad_scale, None, fake, None) == pkv.PKV_ERR_INVALID_ARG
+
+
+def test_noalloc_refuses_too_many_split_items_like_paged_attention(lib):
+    # 2^20 requests x 8 kv heads x ceil(2^18 / 1024) splits = 2^31 items: both calls
+    # refuse the batch as unsupported on the host, before any CUDA call
+    import paged_kv_cache_248_gb300 as pkv
+    P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    fn = lib.paged_attention_noalloc
+    fn.argtypes = [P, P, P, ctypes.POINTER(pkv._CacheDesc), P, i32, P, P, i32, i32, i64, i32, i32,
+                   ctypes.c_float, P, P, P]
+    fn.restype = ctypes.c_int
+    fake = P(0x1000)
+    desc = _desc(pkv, nb=1 << 20, hkv=8, d=128, dt=1)
+    n, max_len = 1 << 20, 1 << 18
+    args = (fake, fake, fake, ctypes.byref(desc), fake, max_len // 16, fake, fake, n, 32, n, 1, max_len,
+            ctypes.c_float(0.1), fake)
+    assert fn(*args, None, None) == pkv.PKV_ERR_UNSUPPORTED
+    assert lib.paged_attention(*args, None) == pkv.PKV_ERR_UNSUPPORTED

@@ -1,11 +1,11 @@
 """paged_attention_noalloc: the attention entry point for callers that cannot let a
-library allocate device memory (their allocator must own all device memory, or
-they capture the step into a CUDA graph, or allocation after start-up is
-forbidden).  It keeps its split-KV scratch in a fixed static device array.
+library allocate device memory (their allocator must account for every byte, or
+their service forbids allocation after start-up).  It keeps its split-KV scratch
+in a fixed static device array.
 
-Checked through the C ABI against paged_attention on the same inputs, for two
-calls in a row (the array keeps the previous call's contents), within the bf16
-tolerance the other parity tests use.  This file is collected last so that a
+Checked through the C ABI, for two calls in a row (the array keeps the previous
+call's contents), against the fp64 oracle and against paged_attention on the same
+inputs, within the bf16 tolerance the other parity tests use.  This file is collected last so that a
 failure here cannot hide the result of any other test; it also passes when run
 alone in a fresh process.
 """
@@ -15,8 +15,9 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads as wl
-from helpers import TOL
+from helpers import TOL, bits, compare
 
 pytestmark = pytest.mark.gpu
 
@@ -35,9 +36,10 @@ def api():
 
 
 def _inputs(w):
-    t = {k: v.cuda() for k, v in w.make_tensors("cpu").items()}
+    t_cpu = w.make_tensors("cpu")
+    t = {k: v.cuda() for k, v in t_cpu.items()}
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
-    return t, dev(w.block_tables), dev(w.seq_lens), dev(w.query_start_loc)
+    return t_cpu, t, dev(w.block_tables), dev(w.seq_lens), dev(w.query_start_loc)
 
 
 def _call_noalloc(pkv, fn, w, t, bt, sl, qsl, out, err_word):
@@ -58,14 +60,16 @@ def _close(a: torch.Tensor, b: torch.Tensor):
 
 
 @pytest.mark.parametrize("case", ["decode", "mixed_small"])
-def test_noalloc_matches_paged_attention_twice(api, case):
+def test_noalloc_matches_the_oracle_and_paged_attention_twice(api, case):
     pkv, fn = api
     if case == "decode":
         w = wl.make("decode")                 # 64 requests up to 4096 tokens: multi-split decode
     else:
         w = wl.random_case(5, num_seqs=10, max_ctx=2500, max_q=300, group=4, num_kv_heads=8, head_dim=128,
                            dtype="bf16")       # chunked prefills and decodes in one batch
-    t, bt, sl, qsl = _inputs(w)
+    t_cpu, t, bt, sl, qsl = _inputs(w)
+    exact = oracle.attention(bits(t_cpu["q"]), bits(t_cpu["k_cache"]), bits(t_cpu["v_cache"]), w.block_tables,
+                             w.seq_lens, w.query_start_loc, w.scale)
     ref = pkv.paged_attention(t["q"], t["k_cache"], t["v_cache"], bt, sl, qsl, w.scale, w.max_query_len,
                               w.max_seq_len)
     assert pkv.pkv_get_last_error() == 0
@@ -75,6 +79,7 @@ def test_noalloc_matches_paged_attention_twice(api, case):
         st = _call_noalloc(pkv, fn, w, t, bt, sl, qsl, out, err_word if call == 0 else None)
         assert st == 0, pkv.status_string(st)
         torch.cuda.synchronize()
+        compare(out, exact, "bf16", f"{case}, call {call}")
         _close(out, ref)
     assert int(err_word.item()) == 0
 
