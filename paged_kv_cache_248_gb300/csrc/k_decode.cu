@@ -571,12 +571,15 @@ __device__ void softmax_warps(const DecodeParams& P, Ctl& c, uint8_t* stages, ui
         break;
       }
       if (!valid_key) {
+        // rows are 128 bytes apart: each lane starts at chunk r mod 8, so eight lanes
+        // cover all 32 banks instead of sharing four
         uint8_t* vrow = stages + st * kStageBytes + kKBytes + r * 128;
         const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
         for (int c16 = 0; c16 < 8; ++c16) {
-          *reinterpret_cast<uint4*>(vrow + c16 * 16) = z;
-          *reinterpret_cast<uint4*>(vrow + kHalfBytes + c16 * 16) = z;
+          const int off = ((c16 + r) & 7) * 16;
+          *reinterpret_cast<uint4*>(vrow + off) = z;
+          *reinterpret_cast<uint4*>(vrow + kHalfBytes + off) = z;
         }
       }
       // P^T row r (MN-major, unswizzled): heads 0-7 in one 16-byte chunk, 8-15 in another
@@ -763,6 +766,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = c.tmem_base;
+  grid_dep_wait();  // the plan (and new tokens) of this call, from the kernels before
+  grid_dep_launch();
 
   if (warp == 0) producer_warp(P, &qmap, &kmap, &vmap, c, stages, qbuf);
   else if (warp == 1) mma_warp(P, c, stages, qbuf, pbuf, tmem);
@@ -810,6 +815,8 @@ struct MergeParams {
 template <int GP>
 __global__ void __launch_bounds__(128 * kMergeGroups, GP <= 8 ? 2 : 0) merge_kernel(const MergeParams P) {
   __shared__ float xfer[GP][3][128];  // one run's (max, sum, accumulator) handed to run 0
+  grid_dep_wait();
+  grid_dep_launch();
   const int d = threadIdx.x % 128, run = threadIdx.x / 128;
   const int64_t n_units = static_cast<int64_t>(P.counters[kMergeCountSlot]) * P.hkv;
   for (int64_t e = blockIdx.x; e < n_units; e += gridDim.x) {
@@ -907,12 +914,13 @@ int launch_gp(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& v
               const Workspace& ws, bool may_split, cudaStream_t s) {
   const int32_t* counters = ws.counters;
   const int32_t* merge_list = ws.merge_list;
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<GP>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e != cudaSuccess) return cuda_status(e);
+  static uint64_t smem_set = 0;
+  const int st = set_smem_once(reinterpret_cast<const void*>(decode_kernel<GP>), kSmemBytes, &smem_set);
+  if (st) return st;
+  cudaError_t e;
   {
     TraceScope trace(kTraceDecode, s);
-    decode_kernel<GP><<<grid, kThreads, kSmemBytes, s>>>(qm, km, vm, p);
-    e = cudaGetLastError();
+    e = launch_k(decode_kernel<GP>, dim3(grid), dim3(kThreads), kSmemBytes, s, qm, km, vm, p);
     if (e != cudaSuccess) return cuda_status(e);
   }
   if (!may_split) return PKV_OK;  // no context is long enough to be split: nothing to merge
@@ -925,8 +933,7 @@ int launch_gp(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& v
   const int64_t cap = static_cast<int64_t>(grid) * 4;
   const int mgrid = static_cast<int>(n_units < cap ? n_units : cap);
   TraceScope trace(kTraceMerge, s);
-  merge_kernel<GP><<<mgrid, 128 * kMergeGroups, 0, s>>>(m);
-  return cuda_status(cudaGetLastError());
+  return cuda_status(launch_k(merge_kernel<GP>, dim3(mgrid), dim3(128 * kMergeGroups), 0, s, m));
 }
 
 }  // namespace

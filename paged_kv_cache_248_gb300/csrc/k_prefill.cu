@@ -716,11 +716,14 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uin
         break;
       }
       if (w == 0 && k0 + r >= zero_from) {
+        // rows are 128 bytes apart, so every lane's k-th chunk would sit in the same four
+        // banks; starting each lane at chunk r mod 8 spreads eight lanes over all 32
         uint8_t* vrow = vbuf + sv * kTileBytes + r * 128;
 #pragma unroll
         for (int c16 = 0; c16 < 8; ++c16) {
-          *reinterpret_cast<uint4*>(vrow + c16 * 16) = make_uint4(0, 0, 0, 0);
-          *reinterpret_cast<uint4*>(vrow + kHalfBytes + c16 * 16) = make_uint4(0, 0, 0, 0);
+          const int off = ((c16 + r) & 7) * 16;
+          *reinterpret_cast<uint4*>(vrow + off) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(vrow + kHalfBytes + off) = make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async_smem();
       }
@@ -751,6 +754,12 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uin
       for (int h = 0; h < 4; ++h) tmem_ld32_issue(tmem + lane_off + o_col + 32 * h, v[h]);
 #pragma unroll
       for (int h = 0; h < 4; ++h) tmem_ld32_wait(v[h]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&c.o_free[w]);
+        mbar_arrive(&c.item_empty[slot]);
+      }
       if (cas_live) {
 #pragma unroll
         for (int h = 0; h < 4; ++h)
@@ -765,12 +774,6 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uin
         P.cas_ml[(cslot * P.gp + rg) * 2 + 1] = l_sum;
         if (bad && rg == 0) P.unit_bad[static_cast<int64_t>(P.cas_members[entry]) * P.hkv + info.head] = 1;
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&c.o_free[w]);
-        mbar_arrive(&c.item_empty[slot]);
-      }
       continue;
     }
     const float inv = bad ? 0.f : 1.f / l_sum;
@@ -781,6 +784,14 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uin
     for (int h = 0; h < 4; ++h) tmem_ld32_issue(tmem + lane_off + o_col + 32 * h, v[h]);
 #pragma unroll
     for (int h = 0; h < 4; ++h) tmem_ld32_wait(v[h]);
+    // O_w is in registers: the next item's first P V may overwrite it while the rows
+    // are stored, and the item slot is no longer read
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(&c.o_free[w]);
+      mbar_arrive(&c.item_empty[slot]);
+    }
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
       if (row_out && P.out_v8) {
@@ -810,12 +821,6 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uin
           reinterpret_cast<uint4*>(orow)[4 * h + ch] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
         }
       }
-    }
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) {
-      mbar_arrive(&c.o_free[w]);
-      mbar_arrive(&c.item_empty[slot]);
     }
   }
   if (!ok && !*abort_flag && lane == 0) raise_abort(c, P.err);
@@ -867,6 +872,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = c.tmem_base;
+  grid_dep_wait();  // the plan, the new tokens and the earlier kernels of this call
+  grid_dep_launch();
   if (warp == 0) producer_warp<kCas>(P, &qmap, &kmap, &vmap, c, qbuf, kbuf, vbuf);
   else if (warp == 1) mma_warp(P, c, qbuf, kbuf, vbuf, tmem);
   else softmax_warps<kCas>(P, c, qbuf, vbuf, tmem);
@@ -918,12 +925,11 @@ int launch_prefill_tc(const AttnArgs& a, const Workspace& ws, int num_sms, uint3
   p.rows_q = kTileKeys / gp;
   p.hq = a.num_q_heads;
   p.scale_log2 = a.scale * 1.4426950408889634f;
+  static uint64_t smem_set = 0;
+  st = set_smem_once(reinterpret_cast<const void*>(prefill_kernel<false>), kSmemBytes, &smem_set);
+  if (st) return st;
   TraceScope trace(kTracePrefill, s);
-  cudaError_t e =
-      cudaFuncSetAttribute(prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e != cudaSuccess) return cuda_status(e);
-  prefill_kernel<false><<<num_sms, kThreads, kSmemBytes, s>>>(qm, km, vm, p);
-  return cuda_status(cudaGetLastError());
+  return cuda_status(launch_k(prefill_kernel<false>, dim3(num_sms), dim3(kThreads), kSmemBytes, s, qm, km, vm, p));
 }
 
 int launch_cascade_tc(const AttnArgs& a, const CascadeArgs& cas, const Workspace& ws, int num_sms, int tiles_per_item,
@@ -971,13 +977,12 @@ int launch_cascade_tc(const AttnArgs& a, const CascadeArgs& cas, const Workspace
   p.cas_groups = cas.num_groups;
   p.cas_np_max = ws.cas_np_max;
   p.cas_tiles = tiles_per_item;
+  static uint64_t smem_set = 0;
+  st = set_smem_once(reinterpret_cast<const void*>(prefill_kernel<true>), kSmemBytes, &smem_set);
+  if (st) return st;
   TraceScope trace(kTraceCascade, s);
-  cudaError_t e =
-      cudaFuncSetAttribute(prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e != cudaSuccess) return cuda_status(e);
   // the Q tensor map is unused in this mode (Q rows are gathered); K's stands in
-  prefill_kernel<true><<<num_sms, kThreads, kSmemBytes, s>>>(km, km, vm, p);
-  return cuda_status(cudaGetLastError());
+  return cuda_status(launch_k(prefill_kernel<true>, dim3(num_sms), dim3(kThreads), kSmemBytes, s, km, km, vm, p));
 }
 
 }  // namespace pkv
