@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 
 #include <cmath>
+#include <cstdlib>
 #include <mutex>
 #include <vector>
 
@@ -110,48 +111,95 @@ size_t layout_workspace(void* base, int32_t num_seqs, int32_t hkv, int32_t group
 namespace {
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
+
+// The maps the last calls of this host thread encoded, by everything that goes into
+// one: a step reuses its pools and usually its q buffer, so most launches find their
+// map here instead of calling the driver's encoder.
+struct MapKey {
+  const void* base;
+  uint64_t dims[3], strides[2];
+  uint32_t box[3], rank;
+  bool operator==(const MapKey& o) const {
+    return base == o.base && rank == o.rank && dims[0] == o.dims[0] && dims[1] == o.dims[1] &&
+           dims[2] == o.dims[2] && strides[0] == o.strides[0] && strides[1] == o.strides[1] &&
+           box[0] == o.box[0] && box[1] == o.box[1] && box[2] == o.box[2];
+  }
+};
+constexpr int kMapCacheSlots = 16;
+struct MapCache {
+  MapKey key[kMapCacheSlots];
+  CUtensorMap map[kMapCacheSlots];
+  int used = 0, next = 0;
+};
+thread_local MapCache t_maps;
+
+int encode_tiled(CUtensorMap* map, const MapKey& k) {
+  for (int i = 0; i < t_maps.used; ++i) {
+    if (t_maps.key[i] == k) {
+      *map = t_maps.map[i];
+      return PKV_OK;
+    }
+  }
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) return PKV_ERR_CUDA;
+  const cuuint64_t dims[3] = {k.dims[0], k.dims[1], k.dims[2]};
+  const cuuint64_t strides[2] = {k.strides[0], k.strides[1]};
+  const cuuint32_t box[3] = {k.box[0], k.box[1], k.box[2]};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, k.rank, const_cast<void*>(k.base), dims, strides, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return PKV_ERR_INVALID_ARG;
+  const int slot = t_maps.next;
+  t_maps.key[slot] = k;
+  t_maps.map[slot] = *map;
+  t_maps.next = (slot + 1) % kMapCacheSlots;
+  if (t_maps.used < kMapCacheSlots) ++t_maps.used;
+  return PKV_OK;
+}
 }  // namespace
 
 int encode_tensor_map_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
                          uint32_t box_inner, uint32_t box_outer) {
-  std::call_once(g_encode_once, [] {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  });
-  if (!g_encode) return PKV_ERR_CUDA;
-  const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {row_bytes};
-  const cuuint32_t box[2] = {box_inner, box_outer};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_INVALID_ARG;
+  const MapKey k{base, {inner, outer, 0}, {row_bytes, 0}, {box_inner, box_outer, 0}, 2};
+  return encode_tiled(map, k);
 }
 
 int encode_tensor_map_3d(CUtensorMap* map, const void* base, const uint64_t dims_in[3], const uint64_t strides_in[2],
                          const uint32_t box_in[3]) {
-  std::call_once(g_encode_once, [] {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  });
-  if (!g_encode) return PKV_ERR_CUDA;
-  const cuuint64_t dims[3] = {dims_in[0], dims_in[1], dims_in[2]};
-  const cuuint64_t strides[2] = {strides_in[0], strides_in[1]};
-  const cuuint32_t box[3] = {box_in[0], box_in[1], box_in[2]};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_INVALID_ARG;
+  const MapKey k{base,
+                 {dims_in[0], dims_in[1], dims_in[2]},
+                 {strides_in[0], strides_in[1]},
+                 {box_in[0], box_in[1], box_in[2]},
+                 3};
+  return encode_tiled(map, k);
+}
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("PKV_PDL");
+    return !(v && v[0] == '0' && v[1] == '\0');
+  }();
+  return on;
+}
+
+// Opt-in to more than 48 KB of dynamic shared memory, once per device and kernel.
+int set_smem_once(const void* kernel, int bytes, uint64_t* done_mask) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PKV_ERR_CUDA;
+  const uint64_t bit = uint64_t(1) << dev;
+  if (__atomic_load_n(done_mask, __ATOMIC_ACQUIRE) & bit) return PKV_OK;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  __atomic_fetch_or(done_mask, bit, __ATOMIC_RELEASE);
+  return PKV_OK;
 }
 
 // ------------------------------------------------------------------ tracing
@@ -345,7 +393,8 @@ int attention_impl(const void* q, const void* k_new, const void* v_new, const vo
   plan.num_sms = ctx->num_sms;
   if (write) {
     const int64_t warps_per_cta = 1024 / 32;
-    const int64_t want = (num_tokens + warps_per_cta - 1) / warps_per_cta;
+    const int64_t pieces = (cache->num_kv_heads * (cache->head_dim * (cache->dtype == PKV_F32 ? 4 : 2) / 16) + 63) / 64;
+    const int64_t want = (num_tokens * pieces + warps_per_cta - 1) / warps_per_cta;  // a warp per 64-vector piece
     plan.k_new = static_cast<const uint4*>(k_new);
     plan.v_new = static_cast<const uint4*>(v_new);
     plan.k_cache = static_cast<uint4*>(const_cast<void*>(k_cache));

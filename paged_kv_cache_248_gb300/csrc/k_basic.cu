@@ -16,6 +16,8 @@ __global__ void __launch_bounds__(256) slot_mapping_kernel(const int32_t* __rest
                                                            const int32_t* __restrict__ qsl, int32_t num_seqs,
                                                            int64_t num_tokens, int64_t* __restrict__ slots,
                                                            uint32_t* err) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (t >= num_tokens) return;
   const int i = find_seq(qsl, num_seqs, t);
@@ -37,6 +39,8 @@ __global__ void __launch_bounds__(256) write_kernel(const uint4* __restrict__ k,
                                                     const int64_t* __restrict__ slots, int64_t num_tokens,
                                                     int32_t hkv, int32_t vec_per_row, int64_t num_slots,
                                                     uint4* __restrict__ kc, uint4* __restrict__ vc, uint32_t* err) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int64_t per_tok = static_cast<int64_t>(hkv) * vec_per_row;
   const int64_t total = num_tokens * per_tok;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -66,6 +70,8 @@ __global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(const int32_t
                                                                    int64_t num_blocks, int64_t vec_per_block,
                                                                    int32_t slices, uint4* kc, uint4* vc,
                                                                    uint32_t* err) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int64_t pair = blockIdx.x / slices;
   const int32_t slice = blockIdx.x % slices;
   if (pair >= n) return;
@@ -110,9 +116,8 @@ int launch_slot_mapping(const int32_t* bt, int32_t max_blocks, const int32_t* se
   TraceScope trace(kTraceSlotMap, s);
   const int threads = 256;
   const int64_t blocks = (num_tokens + threads - 1) / threads;
-  slot_mapping_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(bt, max_blocks, seq_lens, qsl, num_seqs,
-                                                                         num_tokens, slots, err);
-  return cuda_status(cudaGetLastError());
+  return cuda_status(launch_k(slot_mapping_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, s, bt,
+                              max_blocks, seq_lens, qsl, num_seqs, num_tokens, slots, err));
 }
 
 int launch_write(const void* k, const void* v, const int64_t* slots, int64_t T, void* kc, void* vc,
@@ -129,10 +134,10 @@ int launch_write(const void* k, const void* v, const int64_t* slots, int64_t T, 
   int64_t blocks = (total + threads - 1) / threads;
   const int64_t cap = static_cast<int64_t>(ctx->num_sms) * 16;
   if (blocks > cap) blocks = cap;
-  write_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(
-      static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots, T, c.num_kv_heads, vec_per_row,
-      c.num_blocks * kBlock, static_cast<uint4*>(kc), static_cast<uint4*>(vc), err);
-  return cuda_status(cudaGetLastError());
+  return cuda_status(launch_k(write_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, s,
+                              static_cast<const uint4*>(k), static_cast<const uint4*>(v), slots, T, c.num_kv_heads,
+                              vec_per_row, c.num_blocks * kBlock, static_cast<uint4*>(kc),
+                              static_cast<uint4*>(vc), err));
 }
 
 int launch_copy_blocks(const int32_t* src, const int32_t* dst, int64_t n, void* kc, void* vc,
@@ -149,9 +154,9 @@ int launch_copy_blocks(const int32_t* src, const int32_t* dst, int64_t n, void* 
   while (n * slices < 4LL * ctx->num_sms && vec_per_block / (slices * 2) >= kCopyThreads) slices *= 2;
   const int64_t blocks = n * slices;
   if (blocks > 0x7fffffffLL) return PKV_ERR_INVALID_ARG;
-  copy_blocks_kernel<<<static_cast<unsigned>(blocks), kCopyThreads, 0, s>>>(
-      src, dst, n, c.num_blocks, vec_per_block, slices, static_cast<uint4*>(kc), static_cast<uint4*>(vc), err);
-  return cuda_status(cudaGetLastError());
+  return cuda_status(launch_k(copy_blocks_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kCopyThreads), 0, s,
+                              src, dst, n, c.num_blocks, vec_per_block, slices, static_cast<uint4*>(kc),
+                              static_cast<uint4*>(vc), err));
 }
 
 }  // namespace pkv

@@ -32,6 +32,8 @@ __global__ void __launch_bounds__(kGenThreads) generic_attention_kernel(
   __shared__ float sm_m[kGenWarps][kHeadChunk];
   __shared__ float sm_l[kGenWarps][kHeadChunk];
   __shared__ float sm_o[kGenWarps][kHeadChunk][D];
+  grid_dep_wait();
+  grid_dep_launch();
 
   const int group = hq / hkv;
   const int nchunks = (group + kHeadChunk - 1) / kHeadChunk;
@@ -148,11 +150,11 @@ int launch_typed(const AttnArgs& a, uint32_t* err, cudaStream_t s, bool prefill_
   const int nchunks = (group + kHeadChunk - 1) / kHeadChunk;
   const int64_t blocks = a.num_tokens * hkv * nchunks;
   if (blocks > 0x7fffffffLL) return PKV_ERR_INVALID_ARG;
-  generic_attention_kernel<T, D><<<static_cast<unsigned>(blocks), kGenThreads, 0, s>>>(
-      static_cast<const T*>(a.q), static_cast<const T*>(a.k_cache), static_cast<const T*>(a.v_cache),
-      a.cache.num_blocks, hkv, a.block_tables, a.max_blocks, a.seq_lens, a.qsl, a.num_seqs, a.num_q_heads,
-      a.scale * kLog2e, static_cast<T*>(a.out), err, prefill_only ? 1 : 0);
-  return cuda_status(cudaGetLastError());
+  return cuda_status(launch_k(generic_attention_kernel<T, D>, dim3(static_cast<unsigned>(blocks)), dim3(kGenThreads),
+                              0, s, static_cast<const T*>(a.q), static_cast<const T*>(a.k_cache),
+                              static_cast<const T*>(a.v_cache), a.cache.num_blocks, hkv, a.block_tables,
+                              a.max_blocks, a.seq_lens, a.qsl, a.num_seqs, a.num_q_heads, a.scale * kLog2e,
+                              static_cast<T*>(a.out), err, prefill_only ? 1 : 0));
 }
 
 }  // namespace

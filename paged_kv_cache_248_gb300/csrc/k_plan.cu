@@ -180,57 +180,98 @@ __device__ void plan_cascade(const PlanArgs& p) {
   __syncthreads();
 }
 
-// The writer CTAs of a fused step: a warp per new token computes its slot (as
-// slot_mapping_kernel does) and copies the token's K and V rows for every kv head
-// into it (as write_kernel does), with the same error flags.  The attention kernels
-// launched after this one see the rows.
+// The writer CTAs of a fused step: a warp per 64-vector piece of a new token's rows
+// computes the token's slot (as slot_mapping_kernel does) and copies the piece of
+// its K and V rows into it (as write_kernel does), with the same error flags.  The
+// attention kernels launched after this one see the rows.
+//
+// Latency, not bandwidth, bounds this part: a step's few new tokens each wait on a
+// chain of dependent loads.  The chain is kept short: the CTA stages query_start_loc
+// in shared memory with one round of coalesced loads (batches up to kWriterQslMax
+// requests; larger ones search global memory), and every lane loads its part of the
+// piece before the slot is known, so those loads overlap the two dependent loads the
+// slot needs (the request's length, then its table entry).
+constexpr int kWriterQslMax = 8192;
+constexpr int kWriterPiece = 64;  // 16-byte vectors of a (token) row a warp moves: two per lane, K and V
 __device__ void write_new_tokens(const PlanArgs& p) {
+  __shared__ int32_t s_qsl[kWriterQslMax + 1];
   const int lane = threadIdx.x & 31;
+  const bool staged = p.num_seqs <= kWriterQslMax;
+  if (staged) {
+    for (int i = threadIdx.x; i <= p.num_seqs; i += blockDim.x) s_qsl[i] = __ldg(p.qsl + i);
+    __syncthreads();
+  }
   const int64_t nwarps = static_cast<int64_t>(gridDim.x - 1) * (blockDim.x >> 5);
-  const int64_t per_tok = static_cast<int64_t>(p.hkv) * p.vec_per_row;
-  for (int64_t t = static_cast<int64_t>(blockIdx.x - 1) * (blockDim.x >> 5) + (threadIdx.x >> 5); t < p.num_tokens;
-       t += nwarps) {
+  const int per_tok = p.hkv * p.vec_per_row;  // 16-byte vectors of a token's K (or V) row
+  const int pieces = (per_tok + kWriterPiece - 1) / kWriterPiece;
+  const int64_t units = p.num_tokens * pieces;
+  for (int64_t u = static_cast<int64_t>(blockIdx.x - 1) * (blockDim.x >> 5) + (threadIdx.x >> 5); u < units;
+       u += nwarps) {
+    const int64_t t = u / pieces;
+    const int r0 = static_cast<int>(u - t * pieces) * kWriterPiece + lane;  // this lane's vectors: r0, r0 + 32
+    const uint4* ks = p.k_new + t * per_tok;
+    const uint4* vs = p.v_new + t * per_tok;
+    uint4 ka = make_uint4(0, 0, 0, 0), kb = ka, va = ka, vb = ka;
+    if (r0 < per_tok) {
+      ka = __ldcs(ks + r0);
+      va = __ldcs(vs + r0);
+    }
+    if (r0 + 32 < per_tok) {
+      kb = __ldcs(ks + r0 + 32);
+      vb = __ldcs(vs + r0 + 32);
+    }
     int64_t slot = -1;
     if (lane == 0) {
-      const int i = find_seq(p.qsl, p.num_seqs, t);
-      const int64_t q0 = __ldg(p.qsl + i), q1 = __ldg(p.qsl + i + 1);
+      int i;
+      int64_t q0, q1;
+      if (staged) {
+        int lo = 0, hi = p.num_seqs - 1;
+        while (lo < hi) {
+          const int mid = lo + (hi - lo + 1) / 2;
+          if (static_cast<int64_t>(s_qsl[mid]) <= t) lo = mid; else hi = mid - 1;
+        }
+        i = lo;
+        q0 = s_qsl[i];
+        q1 = s_qsl[i + 1];
+      } else {
+        i = find_seq(p.qsl, p.num_seqs, t);
+        q0 = __ldg(p.qsl + i);
+        q1 = __ldg(p.qsl + i + 1);
+      }
       const int64_t pos = static_cast<int64_t>(__ldg(p.seq_lens + i)) - (q1 - q0) + (t - q0);
+      const bool first = r0 == 0;  // errors and the slot are reported once per token
       if (t < q0 || t >= q1 || pos < 0 || pos / kBlock >= p.max_blocks) {
-        flag_error(p.err, kErrLength);
+        if (first) flag_error(p.err, kErrLength);
       } else {
         const int32_t b = __ldg(p.bt + static_cast<int64_t>(i) * p.max_blocks + pos / kBlock);
-        if (b < 0) flag_error(p.err, kErrBlockId);
-        else slot = static_cast<int64_t>(b) * kBlock + pos % kBlock;
+        if (b < 0) {
+          if (first) flag_error(p.err, kErrBlockId);
+        } else {
+          slot = static_cast<int64_t>(b) * kBlock + pos % kBlock;
+        }
       }
-      if (p.slots_out) p.slots_out[t] = slot;
+      if (first && p.slots_out) p.slots_out[t] = slot;
       if (slot >= p.num_slots) {
-        flag_error(p.err, kErrSlot);
+        if (first) flag_error(p.err, kErrSlot);
         slot = -1;
       }
     }
     slot = __shfl_sync(0xffffffffu, slot, 0);
     if (slot < 0) continue;
-    const int64_t blk = slot / kBlock, off = slot % kBlock;
-    const uint4* ks = p.k_new + t * per_tok;
-    const uint4* vs = p.v_new + t * per_tok;
-    for (int64_t r0 = lane; r0 < per_tok; r0 += 64) {
-      const int64_t r1 = r0 + 32;
-      const uint4 ka = __ldcs(ks + r0), va = __ldcs(vs + r0);
-      uint4 kb = make_uint4(0, 0, 0, 0), vb = kb;
-      if (r1 < per_tok) {
-        kb = __ldcs(ks + r1);
-        vb = __ldcs(vs + r1);
-      }
-      const int64_t h0 = r0 / p.vec_per_row, c0 = r0 - h0 * p.vec_per_row;
-      const int64_t d0 = ((blk * p.hkv + h0) * kBlock + off) * p.vec_per_row + c0;
-      p.k_cache[d0] = ka;
-      p.v_cache[d0] = va;
-      if (r1 < per_tok) {
-        const int64_t h1 = r1 / p.vec_per_row, c1 = r1 - h1 * p.vec_per_row;
-        const int64_t d1 = ((blk * p.hkv + h1) * kBlock + off) * p.vec_per_row + c1;
-        p.k_cache[d1] = kb;
-        p.v_cache[d1] = vb;
-      }
+    // vector r = (kv head h, column c) goes to ((block * hkv + h) * 16 + off) * vpr + c
+    const int vpr = p.vec_per_row;
+    const int64_t base = ((slot / kBlock) * p.hkv * kBlock + slot % kBlock) * vpr;
+    if (r0 < per_tok) {
+      const int h = r0 / vpr;
+      const int64_t d = base + static_cast<int64_t>(h) * kBlock * vpr + (r0 - h * vpr);
+      p.k_cache[d] = ka;
+      p.v_cache[d] = va;
+    }
+    if (r0 + 32 < per_tok) {
+      const int h = (r0 + 32) / vpr;
+      const int64_t d = base + static_cast<int64_t>(h) * kBlock * vpr + (r0 + 32 - h * vpr);
+      p.k_cache[d] = kb;
+      p.v_cache[d] = vb;
     }
   }
 }
@@ -354,6 +395,10 @@ __device__ void order_decode_requests(const PlanArgs& p, int total) {
 }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs p) {
+  // the previous step's kernels read the workspace this rewrites and the cache the
+  // writers write: wait for them
+  grid_dep_wait();
+  grid_dep_launch();
   if (blockIdx.x > 0) {  // writer CTAs never join the planner's block barriers
     write_new_tokens(p);
     return;
@@ -417,8 +462,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs p) {
 int launch_plan(const PlanArgs& p, cudaStream_t s) {
   TraceScope trace(kTracePlan, s);
   const int writers = p.k_new ? p.write_ctas : 0;
-  plan_kernel<<<1 + writers, kPlanThreads, 0, s>>>(p);
-  return cuda_status(cudaGetLastError());
+  return cuda_status(launch_k(plan_kernel, dim3(1 + writers), dim3(kPlanThreads), 0, s, p));
 }
 
 }  // namespace pkv

@@ -54,6 +54,18 @@ enum TraceKind : int {
   kTraceCascade = 8,
 };
 
+// Programmatic dependent launch.  Every library kernel is launched so that it may
+// start while the kernel before it in the stream is still running (launch_k below).
+// Each kernel therefore does only on-chip set-up (shared memory, barriers, TMEM,
+// tensor-map prefetch) before grid_dep_wait(), which returns once the preceding
+// grid has completed and its memory writes are visible; every CTA calls it before
+// its first global-memory access and before any early exit, so that a kernel's
+// completion always implies its predecessors'.  grid_dep_launch() then lets the
+// next kernel's CTAs be scheduled as SMs free up.  Both are no-ops when the kernel
+// was launched without the attribute.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void flag_error(uint32_t* err, uint32_t bits) {
   if (err != nullptr) atomicOr(err, bits);
 }
@@ -243,6 +255,30 @@ int launch_prefill_tc(const AttnArgs& a, const Workspace& ws, int num_sms, uint3
 int encode_tensor_map_3d(CUtensorMap* map, const void* base, const uint64_t dims[3], const uint64_t strides[2],
                          const uint32_t box[3]);
 
+// Whether kernels are launched as programmatic dependents of their predecessor
+// (environment PKV_PDL=0 turns it off; read once per process).
+bool pdl_enabled();
+
+// Launches `kernel` on `s`, as a programmatic dependent when pdl_enabled().
+template <typename... Params, typename... Args>
+cudaError_t launch_k(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                     Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
+}
+
+// cudaFuncSetAttribute(kernel, MaxDynamicSharedMemorySize, bytes) on the current
+// device the first time only; done_mask holds one bit per device.
+int set_smem_once(const void* kernel, int bytes, uint64_t* done_mask);
 int encode_tensor_map_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
                          uint32_t box_inner, uint32_t box_outer);
 
