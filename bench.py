@@ -39,9 +39,9 @@ import workloads as wl  # noqa: E402
 METRIC = "decode KV-read GB/s (% of HBM peak); mixed-step tokens/sec at 1 GB300"
 
 
-# DRAM traffic of the decode kernel per algorithmic byte, from one ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum = 505.31 MB + 5.19 MB for 503.62 MB of
-# algorithmic bytes, batched-decode workload; profiles/decode_kernel_batched_decode.md).
+# DRAM traffic of the decode kernel per algorithmic byte, from one ncu capture of one
+# decode launch on the batched-decode workload (dram__bytes_read.sum +
+# dram__bytes_write.sum = 505.34 MB + 4.34 MB for 503.62 MB of algorithmic bytes).
 # It scales to other workloads by the bytes processed, and it is reported only while
 # the profiled sources are unchanged.
 NCU_TRAFFIC = {
@@ -365,13 +365,53 @@ def timed(fn, steps, warmup, barrier=None):
 
 # ----------------------------------------------------------------------------- CPU oracle sample
 
+def _to_bits(x):
+    return (x.view(torch.int16) if x.dtype == torch.bfloat16 else x).cpu().numpy().copy()
+
+
+def host_batch(w, t_gpu, seq_ids):
+    """Requests ``seq_ids`` with only their blocks, copied to the host (block ids
+    renumbered), as the oracle reads them: (k_cache, v_cache, q, k_new, v_new,
+    block_tables, seq_lens, query_start_loc, copy-on-write pairs or None)."""
+    seq_ids = np.asarray(seq_ids, np.int64)
+    qsl = w.query_start_loc
+    bt = w.block_tables[seq_ids]
+    ids = [bt[bt >= 0]]
+    if w.cow_src is not None:   # the sources of the requests' copy-on-write pairs too
+        ids.append(w.cow_src[seq_ids])
+    used = np.unique(np.concatenate(ids))
+    remap = np.full(w.num_blocks, -1, np.int32)
+    remap[used] = np.arange(len(used), dtype=np.int32)
+    cow = None if w.cow_src is None else (remap[w.cow_src[seq_ids]], remap[w.cow_dst[seq_ids]])
+    bt2 = np.where(bt >= 0, remap[np.maximum(bt, 0)], -1).astype(np.int32)
+    idx = torch.from_numpy(used.astype(np.int64)).to(t_gpu["k_cache"].device)
+    kc = _to_bits(t_gpu["k_cache"].index_select(0, idx))
+    vc = _to_bits(t_gpu["v_cache"].index_select(0, idx))
+    rows = np.concatenate([np.arange(qsl[i], qsl[i + 1]) for i in seq_ids]).astype(np.int64)
+    ridx = torch.from_numpy(rows).to(t_gpu["q"].device)
+    q, kn, vn = (_to_bits(t_gpu[k].index_select(0, ridx)) for k in ("q", "k_new", "v_new"))
+    qsl2 = np.concatenate([[0], np.cumsum(w.q_lens[seq_ids])]).astype(np.int32)
+    return kc, vc, q, kn, vn, bt2, w.seq_lens[seq_ids].copy(), qsl2, cow
+
+
+def row_macs(w, rows=None) -> int:
+    """Multiply-adds of attention for the given query rows (default all): 2 * head_dim *
+    Hq per (row, visible key) pair."""
+    qsl, L = w.query_start_loc, w.seq_lens.astype(np.int64)
+    req = np.searchsorted(qsl, np.arange(w.num_tokens), side="right") - 1
+    pos = L[req] - (qsl[req + 1] - np.arange(w.num_tokens))   # absolute position of each row
+    vis = pos + 1
+    if rows is not None:
+        vis = vis[np.asarray(rows)]
+    return int(vis.sum()) * 2 * w.head_dim * w.num_q_heads
+
+
 def cpu_sample(w, t_gpu, target_s: float = 12.0, seed: int = 0):
     """Time the oracle (as it stands) on a bounded sample of the workload: a sub-batch
     of requests (all chunks, a subset of decodes) with sampled query rows; returns
     (tokens/s, description, threads)."""
     import oracle
     rng = np.random.default_rng(seed)
-    qsl = w.query_start_loc
     ql = w.q_lens
     dec_ids = np.nonzero(ql == 1)[0]
     pre_ids = np.nonzero(ql > 1)[0]
@@ -379,24 +419,10 @@ def cpu_sample(w, t_gpu, target_s: float = 12.0, seed: int = 0):
     def build(n_dec, rows_per_chunk):
         pick_dec = rng.choice(dec_ids, size=min(n_dec, len(dec_ids)), replace=False) if len(dec_ids) else []
         seq_ids = np.concatenate([pre_ids, np.sort(pick_dec)]).astype(np.int64)
-        bt = w.block_tables[seq_ids]
-        used = np.unique(bt[bt >= 0])
-        remap = np.full(w.num_blocks, -1, np.int32)
-        remap[used] = np.arange(len(used), dtype=np.int32)
-        bt2 = np.where(bt >= 0, remap[np.maximum(bt, 0)], -1).astype(np.int32)
-        idx = torch.from_numpy(used.astype(np.int64)).to(t_gpu["k_cache"].device)
-        to_bits = lambda x: (x.view(torch.int16) if x.dtype == torch.bfloat16 else x).cpu().numpy().copy()  # noqa
-        kc = to_bits(t_gpu["k_cache"].index_select(0, idx))
-        vc = to_bits(t_gpu["v_cache"].index_select(0, idx))
-        rows = np.concatenate([np.arange(qsl[i], qsl[i + 1]) for i in seq_ids]).astype(np.int64)
-        ridx = torch.from_numpy(rows).to(t_gpu["q"].device)
-        q = to_bits(t_gpu["q"].index_select(0, ridx))
-        kn = to_bits(t_gpu["k_new"].index_select(0, ridx))
-        vn = to_bits(t_gpu["v_new"].index_select(0, ridx))
+        kc, vc, q, kn, vn, bt2, L, qsl2, _ = host_batch(w, t_gpu, seq_ids)
         q_lens = ql[seq_ids]
-        qsl2 = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
         sel = []
-        for j, i in enumerate(seq_ids):
+        for j in range(len(seq_ids)):
             n = int(q_lens[j])
             if n == 1:
                 sel.append(qsl2[j])
@@ -404,7 +430,6 @@ def cpu_sample(w, t_gpu, target_s: float = 12.0, seed: int = 0):
                 k = min(n, rows_per_chunk)
                 sel.extend(qsl2[j] + np.sort(rng.choice(n, size=k, replace=False)))
         sel = np.asarray(sel, np.int64)
-        L = w.seq_lens[seq_ids].copy()
         return kc, vc, q, kn, vn, bt2, L, qsl2, sel
 
     def run(args):
@@ -428,6 +453,46 @@ def cpu_sample(w, t_gpu, target_s: float = 12.0, seed: int = 0):
     return n / dt, desc, oracle.max_threads(), dt
 
 
+def cpu_one_core(w, t_gpu, max_rows: int | None = None, seed: int = 0) -> dict:
+    """The oracle on ONE thread.  Small workloads: the whole step (copy-on-write where
+    the workload has it, slot mapping, write, attention of every row).  Large ones
+    (``max_rows`` set): the step over a random subset of rows, timed, then
+    extrapolated to the whole step by multiply-adds, and labelled so."""
+    import oracle
+    seq_ids = np.arange(w.num_seqs)
+    if max_rows is not None and w.num_tokens > max_rows:
+        rng = np.random.default_rng(seed)
+        rows = np.sort(rng.choice(w.num_tokens, size=max_rows, replace=False))
+        req = np.unique(np.searchsorted(w.query_start_loc, rows, side="right") - 1)
+        seq_ids = req
+    kc, vc, q, kn, vn, bt2, L, qsl2, cow = host_batch(w, t_gpu, seq_ids)
+    full_rows = np.concatenate([np.arange(w.query_start_loc[i], w.query_start_loc[i + 1]) for i in seq_ids])
+    if max_rows is not None and w.num_tokens > max_rows:
+        keep = np.isin(full_rows, rows)
+        sel = np.nonzero(keep)[0].astype(np.int64)
+        timed_macs = row_macs(w, full_rows[keep])
+    else:
+        sel = None
+        timed_macs = row_macs(w)
+    t0 = time.perf_counter()
+    if cow is not None:   # the requests' copy-on-write pairs, renumbered into the host batch
+        oracle.copy_blocks(cow[0], cow[1], kc, vc)
+    slots = oracle.slot_mapping(bt2, L, qsl2)
+    oracle.write(kn, vn, slots, kc, vc)
+    oracle.attention(q, kc, vc, bt2, L, qsl2, w.scale, rows=sel, n_threads=1)
+    dt = time.perf_counter() - t0
+    total_macs = row_macs(w)
+    est = dt * total_macs / timed_macs
+    kv = algorithmic_bytes(w)["decode_kv"] + algorithmic_bytes(w)["prefill"]
+    out = {"s_per_step": est, "tokens_per_s": w.num_tokens / est, "kv_gbs": kv / est / 1e9, "threads": 1}
+    if sel is None:
+        out["how"] = "whole step timed"
+    else:
+        out["how"] = (f"extrapolated: {len(sel)} of {w.num_tokens} query rows timed ({dt:.2f} s, "
+                      f"{100.0 * timed_macs / total_macs:.2f} % of the multiply-adds), scaled by multiply-adds")
+    return out
+
+
 # ----------------------------------------------------------------------------- main
 
 def main():
@@ -440,6 +505,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-decode-line", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="leave out the tiny, decode and prefix lines and the one-core oracle times")
     ap.add_argument("--no-cascade", action="store_true",
                     help="attend a shared prefix per request instead of once per group")
     ap.add_argument("--unfused", action="store_true",
@@ -469,17 +536,20 @@ def main():
     work_b = algorithmic_bytes(w)
     work_f = algorithmic_flops(w)
 
-    # ---- timed region: K steps, tracing the library's launches on the same stream
-    pkv.pkv_trace_enable(True)
-    pkv.pkv_trace_read()
+    # ---- timed region: K steps as a caller runs them (no launch events), then the same
+    # K steps again with the library recording CUDA events around each of its launches
+    # on the launching stream: the per-kernel times and the launch count come from that
+    # second region, the step time from the first
     for _ in range(args.warmup):
         step.run()
     torch.cuda.synchronize()
-    pkv.pkv_trace_read()
     with ClockSampler(local) as clk:
         ms = timed(step.run, args.steps, 0, barrier)
-    trace = pkv.pkv_trace_read()
-    pkv.pkv_trace_enable(False)
+        pkv.pkv_trace_enable(True)
+        pkv.pkv_trace_read()
+        ms_traced = timed(step.run, args.steps, 0, barrier)
+        trace = pkv.pkv_trace_read()
+        pkv.pkv_trace_enable(False)
     st = pkv.pkv_get_last_error()
     if st != 0:
         raise RuntimeError(f"device error during bench: {pkv.status_string(st)}")
@@ -502,10 +572,13 @@ def main():
         n_dom, t_dom = kernel_ms["decode"][0], sum(kernel_ms[k][1] for k in parts)
     per_launch_ms = t_dom / n_dom
     if dom == "prefill":
+        # a launch of ~0.1 ms at full clock: the burst GEMM peak is its denominator; the
+        # power-capped sustained peak is reported beside it
         flops = work_f["prefill"]
         ach = flops / (per_launch_ms / 1e3) / 1e12
-        roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops_sustained"],
-                "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops_sustained"], "traffic": None}
+        roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops"], "traffic": None,
+                "frac_of_sustained": ach / pk["bf16_tflops_sustained"]}
     else:
         b = work_b["decode"] if dom.startswith(("decode", "cascade")) else work_b["total"]
         ach = b / (per_launch_ms / 1e3) / 1e9
@@ -524,6 +597,7 @@ def main():
                        work_b["total"] / 1e9),
                    "parallelism": "replicas only" if world > 1 else "single GPU"},
         "clocks": clocks, "roofline": roof, "gpu_launches": launches,
+        "ms_per_step_with_launch_events": max_over_ranks(ms_traced, world, device),
         "kernels": {k: {"launches": n, "ms_total": t, "ms_per_launch": t / n} for k, (n, t) in kernel_ms.items()},
         "work": {"bytes": work_b, "flops": work_f},
     }
@@ -572,9 +646,14 @@ def main():
     if not args.no_decode_line and args.workload == "mixed":
         res["decode_kv_read"] = decode_line(pkv, device, pk, args)
 
+    if not args.no_configs and args.workload == "mixed":
+        res["configs"] = config_lines(pkv, device, pk, args)
+
     if not args.no_cpu and rank == 0 and world == 1:
         v, desc, cores, dt = cpu_sample(w, step.t)
         res["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc}
+        if args.workload == "mixed" and not args.no_configs:
+            res["cpu_baseline"]["one_core"] = one_core_lines(pkv, device, step)
 
     if rank == 0:
         print(json.dumps(res))
@@ -589,9 +668,10 @@ def decode_line(pkv, device, pk, args) -> dict:
     w = wl.make("long")
     s = Step(pkv, w, device)
     s.run()
-    pkv.pkv_trace_enable(True)
-    pkv.pkv_trace_read()
     ms = timed(s.attention_only, max(10, args.steps), args.warmup)
+    pkv.pkv_trace_enable(True)   # per-kernel times from a second, traced pass
+    pkv.pkv_trace_read()
+    timed(s.attention_only, max(10, args.steps), 0)
     trace = pkv.pkv_trace_read()
     pkv.pkv_trace_enable(False)
     if pkv.pkv_get_last_error() != 0:
@@ -608,6 +688,105 @@ def decode_line(pkv, device, pk, args) -> dict:
     del s
     torch.cuda.empty_cache()
     return out
+
+
+def flushed_time(fn, steps: int, warmup: int, flush: torch.Tensor) -> float:
+    """Mean device time of ``fn`` over ``steps`` calls, each bracketed by CUDA events on
+    the launching stream, with a write of ``flush`` (larger than L2) before every
+    call and outside its events, so that no call finds the previous one's data in L2."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    evs = []
+    for _ in range(steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        evs.append((e0, e1))
+    torch.cuda.synchronize()
+    return float(np.mean([a.elapsed_time(b) for a, b in evs]))
+
+
+def config_lines(pkv, device, pk, args) -> dict:
+    """The three smaller named workloads, each one whole step as the default line runs
+    it (copy-on-write where the workload has it, then paged_attention_step; the shared
+    prefix as a group hint), L2 flushed before every timed step:
+      tiny   -- microseconds per step (launch-latency bound);
+      decode -- KV GB/s and the fraction of the HBM peak the step and its decode
+                kernel reach;
+      prefix -- logical KV GB/s (the shared prefix counted once per request, so it
+                may exceed HBM), the fraction of the HBM peak on the unique bytes the
+                step must move, and the copy-on-write kernel's GB/s."""
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)  # 256 MB > 129 MB L2
+    steps = max(10, args.steps)
+    out = {}
+    for name in ("tiny", "decode", "prefix"):
+        w = wl.make(name)
+        s = Step(pkv, w, device)
+        ms = flushed_time(s.run, steps, args.warmup, flush)
+        pkv.pkv_trace_enable(True)   # per-kernel times from a second, traced pass
+        pkv.pkv_trace_read()
+        flushed_time(s.run, steps, 0, flush)
+        trace = pkv.pkv_trace_read()
+        pkv.pkv_trace_enable(False)
+        if pkv.pkv_get_last_error() != 0:
+            raise RuntimeError(f"device error in the {name} line")
+        ker = {k: {"launches": n, "ms_per_launch": t / n} for k, (n, t) in trace.items() if n}
+        b = algorithmic_bytes(w)
+        kv_tok = 2 * w.num_kv_heads * w.head_dim * w.elem_bytes
+        new_tok = w.num_tokens * 2 * kv_tok          # read the new rows, write them into their slots
+        line = {"workload": f"{name}: {describe(w)}", "ms_per_step": ms, "steps": steps,
+                "l2": "flushed (256 MB write) before every step", "kernels": ker}
+        if name == "tiny":
+            line["us_per_step"] = ms * 1e3
+            line["bound"] = "launch latency"
+        elif name == "decode":
+            step_bytes = b["total"] + new_tok
+            line.update({"kv_bytes": b["decode_kv"], "kv_gbs": b["decode_kv"] / (ms / 1e3) / 1e9,
+                         "step_bytes": step_bytes, "step_frac_of_hbm": step_bytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"],
+                         "roofline_ms": step_bytes / (pk["hbm_gbs"] * 1e9) * 1e3})
+            if "decode" in ker:
+                kms = ker["decode"]["ms_per_launch"]
+                line["decode_kernel_frac_of_hbm"] = b["decode"] / (kms / 1e3) / 1e9 / pk["hbm_gbs"]
+        else:
+            logical = int(w.seq_lens.astype(np.int64).sum()) * kv_tok
+            n_cow = int(w.cow_src.shape[0])
+            blk = w.num_kv_heads * 16 * w.head_dim * w.elem_bytes
+            cow_bytes = n_cow * 2 * 2 * blk          # read and write K and V of each pair
+            step_bytes = b["total"] + new_tok + cow_bytes
+            line.update({"logical_kv_bytes": logical, "logical_kv_gbs": logical / (ms / 1e3) / 1e9,
+                         "unique_step_bytes": step_bytes,
+                         "unique_frac_of_hbm": step_bytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"],
+                         "roofline_ms": step_bytes / (pk["hbm_gbs"] * 1e9) * 1e3})
+            if "copy_blocks" in ker:
+                cms = ker["copy_blocks"]["ms_per_launch"]
+                line["cow"] = {"pairs": n_cow, "bytes": cow_bytes, "ms_per_launch": cms,
+                               "gbs": cow_bytes / (cms / 1e3) / 1e9,
+                               "frac_of_hbm": cow_bytes / (cms / 1e3) / 1e9 / pk["hbm_gbs"]}
+        line["peak_gbs"], line["peak_source"] = pk["hbm_gbs"], pk["source"]
+        out[name] = line
+        del s
+        torch.cuda.empty_cache()
+    del flush
+    return out
+
+
+def one_core_lines(pkv, device, mixed_step) -> dict:
+    """The oracle on one thread for every named workload (section "CPU oracle timing"
+    of the measurement plan): whole steps for tiny, decode and prefix; a timed subset
+    extrapolated by multiply-adds for mixed and long."""
+    res = {}
+    for name in ("tiny", "decode", "prefix", "long"):
+        w = wl.make(name)
+        t = w.make_tensors(device)
+        res[name] = cpu_one_core(w, t, max_rows=4 if name == "long" else None)
+        del t
+        torch.cuda.empty_cache()
+    res["mixed"] = cpu_one_core(mixed_step.w, mixed_step.t, max_rows=256)
+    return res
 
 
 def describe(w) -> str:
