@@ -88,8 +88,9 @@ size_t layout_workspace(void* base, int32_t num_seqs, int32_t hkv, int32_t group
   w.pre_order = static_cast<int32_t*>(take(static_cast<size_t>(max_pre_units) * 2 * sizeof(int32_t)));
   w.dec_order = static_cast<int32_t*>(take(static_cast<size_t>(num_seqs) * sizeof(int32_t)));
   w.dec_start = static_cast<int32_t*>(take((static_cast<size_t>(num_seqs) + 1) * sizeof(int32_t)));
+  w.dec_pos = static_cast<int32_t*>(take(static_cast<size_t>(2 * kDecPosMax) * sizeof(int32_t)));
   w.unit_bad = static_cast<int32_t*>(take(static_cast<size_t>(num_seqs) * hkv * sizeof(int32_t)));
-  w.merge_list = static_cast<int32_t*>(take(static_cast<size_t>(num_seqs) * sizeof(int32_t)));
+  w.merge_list = static_cast<int32_t*>(take(static_cast<size_t>(num_seqs) * 8 * sizeof(int32_t)));
   w.part_ml = static_cast<float*>(take(static_cast<size_t>(max_dec_items) * group * 2 * sizeof(float)));
   w.part_o = static_cast<float*>(take(static_cast<size_t>(max_dec_items) * group * head_dim * sizeof(float)));
   if (cas && cas->num_groups > 0 && cas->num_members > 0) {
@@ -390,6 +391,7 @@ int attention_impl(const void* q, const void* k_new, const void* v_new, const vo
   plan.rows_q = kTileKeys / gp;
   plan.dec_order = ws.dec_order;
   plan.dec_start = ws.dec_start;
+  plan.dec_pos = ws.dec_pos;
   plan.num_sms = ctx->num_sms;
   if (write) {
     const int64_t warps_per_cta = 1024 / 32;

@@ -48,6 +48,7 @@ constexpr int kStageBytes = 2 * kKBytes;      // K + V
 constexpr int kQBytes = 4096;                 // Q: [2 halves][16 rows][128 B]
 constexpr int kPBytes = 4096;                 // P^T: 128 keys x 16 heads, MN-major, no swizzle
 constexpr int kRing = 3;                      // ring of items prepared by the scheduler
+constexpr int kAheadTiles = 4;                // key tiles claimed but not yet issued before another claim
 constexpr int kMaxIds = kNoSplitKeys / kBlock;  // block ids of one item (the longest item is unsplit)
 constexpr uint32_t kTmemCols = 64;            // S^T x2 (cols 0, 16), O^T x2 (cols 32, 48)
 constexpr int kBlocksPerTile = kTileKeys / kBlock;
@@ -73,6 +74,7 @@ struct Ctl {
   int bad[kRing];
   int32_t ids[kRing][kMaxIds];  // physical block ids of each ring item, validated
   float red[2][4][16];
+  uint32_t issued_tiles;  // key tiles the producer has issued so far (it alone writes this)
   // a shared-prefix member's prefix partials, copied in at the start of its item and
   // folded at the end: accumulators [split * GP + head][128], max and sum by item parity
   float cas_o[kCasStage][128];
@@ -92,6 +94,7 @@ struct DecodeParams {
   const int32_t* dec_prefix;
   const int32_t* dec_order;   // when *order_flag: queue position order of the requests
   const int32_t* dec_start;   //   and the items' exclusive prefix in that order
+  const int32_t* dec_pos;     //   and per queue position (request, its first position)
   const int32_t* order_flag;
   int32_t* queue;
   int32_t* unit_bad;
@@ -187,19 +190,50 @@ __device__ __forceinline__ int head_of_lane(int lane) {
 __device__ void scheduler_warp(const DecodeParams& P, Ctl& c) {
   const int lane = threadIdx.x & 31;
   volatile int* abort_flag = &c.abort_flag;
+  // the first item's position record is loaded with the item count and the order flag
+  // (one round trip); it is used only if the batch turns out to be ordered
+  const int2* pos_rec = reinterpret_cast<const int2*>(P.dec_pos);
+  const int2 first_rec = blockIdx.x < kDecPosMax ? __ldg(pos_rec + blockIdx.x) : make_int2(0, 0);
   const int total = P.dec_prefix[P.num_seqs];
   // queue positions follow the planner's order of the requests when it made one
   const bool ordered = *P.order_flag != 0;
   const int32_t* starts = ordered ? P.dec_start : P.dec_prefix;
+  uint32_t claimed_tiles = 0;  // key tiles of the valid items taken so far
   for (uint32_t it = 0;; ++it) {
     const int slot = it % kRing;
     if (!mbar_wait(&c.item_empty[slot], ((it / kRing) & 1) ^ 1, abort_flag)) {
       if (!*abort_flag && lane == 0) raise_abort(c, P.err);
       break;
     }
-    int idx = 0;
-    if (lane == 0) idx = atomicAdd(P.queue, 1);
-    idx = __shfl_sync(0xffffffffu, idx, 0);
+    // An item taken off the queue is one no other CTA can take: take the next only when
+    // the producer is within kAheadTiles tiles of needing it, so that long items are
+    // not held here while other CTAs run dry at the end (short items still fill the
+    // ring).  The producer's progress needs nothing from this warp, so the wait ends;
+    // it is bounded like every other wait.
+    if (it > 0) {
+      const volatile uint32_t* issued = &c.issued_tiles;
+      if (static_cast<int32_t>(claimed_tiles - *issued) > kAheadTiles) {
+        const uint64_t t0 = globaltimer_ns();
+        bool waited = true;
+        while (static_cast<int32_t>(claimed_tiles - *issued) > kAheadTiles) {
+          if (*abort_flag || globaltimer_ns() - t0 > kWaitTimeoutNs) {
+            waited = false;
+            break;
+          }
+          __nanosleep(64);
+        }
+        if (!waited) {
+          if (!*abort_flag && lane == 0) raise_abort(c, P.err);
+          break;
+        }
+      }
+    }
+    // every CTA's first item is its own index; later ones come off the queue after those
+    int idx = static_cast<int>(blockIdx.x);
+    if (it > 0) {
+      if (lane == 0) idx = static_cast<int>(gridDim.x) + atomicAdd(P.queue, 1);
+      idx = __shfl_sync(0xffffffffu, idx, 0);
+    }
     ItemInfo r{};
     if (idx >= total) {
       if (lane == 0) {
@@ -209,19 +243,27 @@ __device__ void scheduler_warp(const DecodeParams& P, Ctl& c) {
       }
       break;
     }
-    // the request owning the queue position: last k with starts[k] <= idx, by a 32-way
-    // search (each round the 32 lanes probe evenly spaced candidates)
-    int lo = 0, hi = P.num_seqs - 1;
-    while (hi > lo) {
-      const int step = (hi - lo + 32) / 32;
-      const int pos = lo + lane * step;
-      const bool le = pos <= hi && __ldg(starts + pos) <= idx;
-      const unsigned m = __ballot_sync(0xffffffffu, le);  // lane 0 always: starts[lo] <= idx
-      lo += (31 - __clz(m)) * step;
-      hi = min(hi, lo + step - 1);
+    // the request owning the queue position and its first position: one load in an
+    // ordered batch, else the last k with starts[k] <= idx by a 32-way search (each
+    // round the 32 lanes probe evenly spaced candidates)
+    int i, qbase;
+    if (ordered) {
+      const int2 e = it == 0 ? first_rec : __ldg(pos_rec + idx);
+      i = e.x;
+      qbase = e.y;
+    } else {
+      int lo = 0, hi = P.num_seqs - 1;
+      while (hi > lo) {
+        const int step = (hi - lo + 32) / 32;
+        const int pos = lo + lane * step;
+        const bool le = pos <= hi && __ldg(starts + pos) <= idx;
+        const unsigned m = __ballot_sync(0xffffffffu, le);  // lane 0 always: starts[lo] <= idx
+        lo += (31 - __clz(m)) * step;
+        hi = min(hi, lo + step - 1);
+      }
+      i = lo;
+      qbase = __ldg(starts + lo);
     }
-    const int i = ordered ? __ldg(P.dec_order + lo) : lo;
-    const int qbase = __ldg(starts + lo);
     const int base = __ldg(P.dec_prefix + i);  // the request's items in request order
     const int cnt = __ldg(P.dec_prefix + i + 1) - base;
     const int64_t L = __ldg(P.seq_lens + i);
@@ -268,6 +310,7 @@ __device__ void scheduler_warp(const DecodeParams& P, Ctl& c) {
       }
     }
     bad = __any_sync(0xffffffffu, bad);
+    if (r.valid) claimed_tiles += static_cast<uint32_t>((r.key_end - r.key_start + kTileKeys - 1) / kTileKeys);
     if (lane == 0) {
       if (bad) flag_error(P.err, kErrBlockId);
       c.ring[slot] = r;
@@ -332,6 +375,7 @@ __device__ void producer_warp(const DecodeParams& P, const CUtensorMap* qmap, co
           tma_load_2d(s + kKBytes + kHalfBytes, vmap, &c.full[st], 64, row);
         }
         ++tc;
+        if (lane == 0) *reinterpret_cast<volatile uint32_t*>(&c.issued_tiles) = tc;
       }
       if (!ok) break;
     }
@@ -752,6 +796,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     mbar_init(&c.drain, 1);
     mbar_init(&c.group_bar, 4);
     c.abort_flag = 0;
+    c.issued_tiles = 0;
     fence_mbar_init();
     tma_prefetch_map(&qmap);
     tma_prefetch_map(&kmap);
@@ -818,17 +863,30 @@ __global__ void __launch_bounds__(128 * kMergeGroups, GP <= 8 ? 2 : 0) merge_ker
   grid_dep_wait();
   grid_dep_launch();
   const int d = threadIdx.x % 128, run = threadIdx.x / 128;
+  // the planner's record of the request (loaded with the list length: a record past
+  // the list is never used)
+  const int4* recs = reinterpret_cast<const int4*>(P.merge_list);
+  int64_t e = blockIdx.x;
+  int4 ra = make_int4(0, 0, 0, 0), rb = ra;
+  if (e / P.hkv < P.num_seqs) {
+    ra = __ldg(recs + 2 * (e / P.hkv));
+    rb = __ldg(recs + 2 * (e / P.hkv) + 1);
+  }
   const int64_t n_units = static_cast<int64_t>(P.counters[kMergeCountSlot]) * P.hkv;
-  for (int64_t e = blockIdx.x; e < n_units; e += gridDim.x) {
-    const int i = __ldg(P.merge_list + e / P.hkv), h = static_cast<int>(e % P.hkv);
+  for (; e < n_units; e += gridDim.x) {
+    if (e != blockIdx.x) {
+      ra = __ldg(recs + 2 * (e / P.hkv));
+      rb = __ldg(recs + 2 * (e / P.hkv) + 1);
+    }
+    const int i = ra.x, h = static_cast<int>(e % P.hkv);
     const int64_t u = static_cast<int64_t>(i) * P.hkv + h;
-    const int base_i = __ldg(P.dec_prefix + i);
-    const int ns = (__ldg(P.dec_prefix + i + 1) - base_i) / P.hkv;
-    const int pre = P.seq_prefix ? __ldg(P.seq_prefix + i) : 0;
+    const int base_i = ra.y, ns = ra.z;
+    const int pre = rb.x;
     if (ns <= 1) continue;  // (a member of one split was finished by the decode kernel)
+    const bool bad = __ldg(P.unit_bad + u) != 0;
     const int64_t base = base_i + static_cast<int64_t>(h) * ns;
     const int npre = pre > 0 ? static_cast<int>(cascade_splits(pre)) : 0;
-    const int64_t cbase = pre > 0 ? (static_cast<int64_t>(__ldg(P.seq_entry + i)) * P.hkv + h) * P.cas_np_max : 0;
+    const int64_t cbase = pre > 0 ? (static_cast<int64_t>(rb.y) * P.hkv + h) * P.cas_np_max : 0;
     // this run: entries [e0, e1) of prefix partials then splits
     const int n_all = npre + ns;
     const int per = (n_all + kMergeGroups - 1) / kMergeGroups;
@@ -899,8 +957,7 @@ __global__ void __launch_bounds__(128 * kMergeGroups, GP <= 8 ? 2 : 0) merge_ker
       }
     }
     if (run == 0) {
-      const bool bad = __ldg(P.unit_bad + u) != 0;
-      const int64_t trow = __ldg(P.qsl + i);
+      const int64_t trow = ra.w;
       __nv_bfloat16* orow = P.out + (trow * P.hq + static_cast<int64_t>(h) * P.group) * 128 + d;
 #pragma unroll
       for (int g = 0; g < GP; ++g)
@@ -909,9 +966,119 @@ __global__ void __launch_bounds__(128 * kMergeGroups, GP <= 8 ? 2 : 0) merge_ker
   }
 }
 
+// The split merge when no unit folds more than MergeSmall<GP>::kEntries partials (the
+// host bounds this from the longest context and prefix): one 128-thread CTA per
+// (request, kv head) whose thread d runs all four of merge_kernel's runs for its column
+// one after another -- the same folds in the same order, so the same bits -- with every
+// partial's load issued before the first fold and no block barrier.
+template <int GP>
+struct MergeSmall {
+  static constexpr int kEntries = GP <= 4 ? 8 : GP == 8 ? 4 : 2;
+};
+template <int GP>
+__global__ void __launch_bounds__(128) merge_small_kernel(const MergeParams P) {
+  constexpr int E = MergeSmall<GP>::kEntries;
+  grid_dep_wait();
+  grid_dep_launch();
+  const int d = threadIdx.x;
+  const int4* recs = reinterpret_cast<const int4*>(P.merge_list);
+  int64_t e = blockIdx.x;
+  int4 ra = make_int4(0, 0, 0, 0), rb = ra;
+  if (e / P.hkv < P.num_seqs) {
+    ra = __ldg(recs + 2 * (e / P.hkv));
+    rb = __ldg(recs + 2 * (e / P.hkv) + 1);
+  }
+  const int64_t n_units = static_cast<int64_t>(P.counters[kMergeCountSlot]) * P.hkv;
+  for (; e < n_units; e += gridDim.x) {
+    if (e != blockIdx.x) {
+      ra = __ldg(recs + 2 * (e / P.hkv));
+      rb = __ldg(recs + 2 * (e / P.hkv) + 1);
+    }
+    const int i = ra.x, h = static_cast<int>(e % P.hkv);
+    const int base_i = ra.y, ns = ra.z, pre = rb.x;
+    if (ns <= 1) continue;
+    const int64_t u = static_cast<int64_t>(i) * P.hkv + h;
+    const bool bad = __ldg(P.unit_bad + u) != 0;
+    const int64_t base = base_i + static_cast<int64_t>(h) * ns;
+    const int npre = pre > 0 ? static_cast<int>(cascade_splits(pre)) : 0;
+    const int64_t cbase = pre > 0 ? (static_cast<int64_t>(rb.y) * P.hkv + h) * P.cas_np_max : 0;
+    const int n_all = min(npre + ns, E);
+    float ml[E][2 * GP], ov[E][GP];
+#pragma unroll
+    for (int k = 0; k < E; ++k) {
+      if (k < n_all && k < npre) {
+        const float* ml_p = P.cas_ml + (cbase + k) * GP * 2;
+        const float* o_p = P.cas_o + (cbase + k) * GP * 128 + d;
+#pragma unroll
+        for (int q = 0; q < 2 * GP; ++q) ml[k][q] = __ldg(ml_p + q);
+#pragma unroll
+        for (int g = 0; g < GP; ++g) ov[k][g] = __ldg(o_p + g * 128);
+      } else if (k < n_all) {
+        const int64_t it = base + (k - npre);
+        const float4* ml4 = reinterpret_cast<const float4*>(P.part_ml + it * GP * 2);
+        const float4* o4 = reinterpret_cast<const float4*>(P.part_o + (it * 128 + d) * GP);
+#pragma unroll
+        for (int q = 0; q < GP / 2; ++q) {
+          const float4 t = __ldg(ml4 + q);
+          ml[k][4 * q] = t.x;
+          ml[k][4 * q + 1] = t.y;
+          ml[k][4 * q + 2] = t.z;
+          ml[k][4 * q + 3] = t.w;
+        }
+#pragma unroll
+        for (int q = 0; q < GP / 4; ++q) {
+          const float4 t = __ldg(o4 + q);
+          ov[k][4 * q] = t.x;
+          ov[k][4 * q + 1] = t.y;
+          ov[k][4 * q + 2] = t.z;
+          ov[k][4 * q + 3] = t.w;
+        }
+      }
+    }
+    // merge_kernel's runs: run r folds entries [r * per, (r + 1) * per) from nothing, and
+    // runs 1.. are then folded into run 0 in order
+    const int per = (n_all + kMergeGroups - 1) / kMergeGroups;
+    float M[GP], num[GP], den[GP];
+#pragma unroll
+    for (int r = 0; r < kMergeGroups; ++r) {
+      float Mr[GP], nr[GP], dr[GP];
+#pragma unroll
+      for (int g = 0; g < GP; ++g) {
+        Mr[g] = -INFINITY;
+        nr[g] = 0.f;
+        dr[g] = 0.f;
+      }
+      const int e0 = min(n_all, r * per), e1 = min(n_all, e0 + per);
+#pragma unroll
+      for (int k = 0; k < E; ++k)
+        if (k >= e0 && k < e1) merge_fold<GP>(Mr, nr, dr, ml[k], ov[k]);
+      if (r == 0) {
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
+          M[g] = Mr[g];
+          num[g] = nr[g];
+          den[g] = dr[g];
+        }
+      } else if (r * per < n_all) {
+        float mlr[2 * GP];
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
+          mlr[2 * g] = Mr[g];
+          mlr[2 * g + 1] = dr[g];
+        }
+        merge_fold<GP>(M, num, den, mlr, nr);
+      }
+    }
+    __nv_bfloat16* orow = P.out + (static_cast<int64_t>(ra.w) * P.hq + static_cast<int64_t>(h) * P.group) * 128 + d;
+#pragma unroll
+    for (int g = 0; g < GP; ++g)
+      if (g < P.group) orow[g * 128] = __float2bfloat16_rn(bad ? 0.f : __fdividef(num[g], den[g]));
+  }
+}
+
 template <int GP>
 int launch_gp(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& vm, const DecodeParams& p, int grid,
-              const Workspace& ws, bool may_split, cudaStream_t s) {
+              const Workspace& ws, bool may_split, int max_entries, cudaStream_t s) {
   const int32_t* counters = ws.counters;
   const int32_t* merge_list = ws.merge_list;
   static uint64_t smem_set = 0;
@@ -933,6 +1100,11 @@ int launch_gp(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& v
   const int64_t cap = static_cast<int64_t>(grid) * 4;
   const int mgrid = static_cast<int>(n_units < cap ? n_units : cap);
   TraceScope trace(kTraceMerge, s);
+  if (max_entries <= MergeSmall<GP>::kEntries) {
+    const int64_t scap = static_cast<int64_t>(grid) * 16;
+    return cuda_status(launch_k(merge_small_kernel<GP>, dim3(static_cast<unsigned>(n_units < scap ? n_units : scap)),
+                                dim3(128), 0, s, m));
+  }
   return cuda_status(launch_k(merge_kernel<GP>, dim3(mgrid), dim3(128 * kMergeGroups), 0, s, m));
 }
 
@@ -965,6 +1137,7 @@ int launch_decode_tc(const AttnArgs& a, const Workspace& ws, int num_sms, uint32
   p.dec_prefix = ws.dec_prefix;
   p.dec_order = ws.dec_order;
   p.dec_start = ws.dec_start;
+  p.dec_pos = ws.dec_pos;
   p.order_flag = ws.counters + kDecOrderSlot;
   p.queue = ws.counters + 0;
   p.unit_bad = ws.unit_bad;
@@ -988,9 +1161,12 @@ int launch_decode_tc(const AttnArgs& a, const Workspace& ws, int num_sms, uint32
   p.scale_log2 = a.scale * 1.4426950408889634f;
   // the planner never splits a request longer than the host bound, and none up to kNoSplitKeys
   const bool may_split = a.max_seq_len > kNoSplitKeys;
-  if (gp == 4) return launch_gp<4>(qm, km, vm, p, num_sms, ws, may_split, s);
-  if (gp == 8) return launch_gp<8>(qm, km, vm, p, num_sms, ws, may_split, s);
-  return launch_gp<16>(qm, km, vm, p, num_sms, ws, may_split, s);
+  // the most partials one unit can fold: its own key splits plus its prefix's splits
+  const int max_entries = static_cast<int>(decode_splits(a.max_seq_len)) +
+                          (ws.seq_prefix ? ws.cas_np_max : 0);
+  if (gp == 4) return launch_gp<4>(qm, km, vm, p, num_sms, ws, may_split, max_entries, s);
+  if (gp == 8) return launch_gp<8>(qm, km, vm, p, num_sms, ws, may_split, max_entries, s);
+  return launch_gp<16>(qm, km, vm, p, num_sms, ws, may_split, max_entries, s);
 }
 
 }  // namespace pkv

@@ -116,6 +116,7 @@ extern "C" PKV_API int paged_attention_noalloc(const void* q, const void* k_cach
   plan.rows_q = kTileKeys / gp;
   plan.dec_order = ws.dec_order;
   plan.dec_start = ws.dec_start;
+  plan.dec_pos = ws.dec_pos;
   plan.num_sms = sms;
   st = launch_plan(plan, s);
   if (st) return st;

@@ -28,6 +28,7 @@ namespace pkv {
 namespace {
 
 constexpr int kPlanThreads = 1024;
+constexpr int kPlanSmemMax = 144 * 1024;  // dynamic shared memory the plan launch may ask for
 
 __device__ __forceinline__ int warp_inclusive_scan(int v) {
   const int lane = threadIdx.x & 31;
@@ -180,6 +181,118 @@ __device__ void plan_cascade(const PlanArgs& p) {
   __syncthreads();
 }
 
+// The same membership decisions with every intermediate state in shared memory (`sm`,
+// the launch's dynamic buffer), for batches within the limits below: the planner then
+// waits on three rounds of global loads (the group offsets; each entry's request; that
+// request's lengths, group and table rows) instead of one or more per phase.  Leaves
+// each request's prefix tokens and member entry in shared memory for the rest of the
+// plan, and writes the global copies the other kernels read.  Called by the whole block.
+constexpr int kCasOnchipSeqs = 8192;
+constexpr int kCasOnchipMembers = 8192;
+constexpr int kCasOnchipGroups = 1024;
+constexpr int kCasOnchipBlocks = 512;  // longest prefix whose table one thread compares
+__device__ void plan_cascade_onchip(const PlanArgs& p, int32_t* sm, int32_t*& s_prefix, int32_t*& s_entry) {
+  __shared__ int s_csr_ok;
+  const CascadeArgs& g = p.cas;
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const int n = p.num_seqs, M = g.num_members, G = g.num_groups;
+  s_entry = sm;                    // [n]: claiming entry; -1 none; -2 listed more than once
+  s_prefix = s_entry + n;          // [n]: prefix tokens of a member, else 0
+  int32_t* s_pb = s_prefix + n;    // [M]: the entry's prefix blocks if it passed its checks, else 0
+  int32_t* s_req = s_pb + M;       // [M]: the entry's request
+  int32_t* s_start = s_req + M;    // [G + 1]
+  int32_t* s_blocks = s_start + G + 1;  // [G]
+  for (int i = tid; i < n; i += nthr) s_entry[i] = -1;
+  for (int k = tid; k <= G; k += nthr) s_start[k] = __ldg(g.start + k);
+  for (int k = tid; k < G; k += nthr) s_blocks[k] = __ldg(g.blocks + k);
+  if (tid == 0) s_csr_ok = 1;
+  __syncthreads();
+  if (tid == 0 && !(s_start[0] == 0 && s_start[G] == M)) s_csr_ok = 0;
+  for (int k = tid; k < G; k += nthr)
+    if (s_start[k] > s_start[k + 1]) s_csr_ok = 0;  // CSR offsets must not decrease
+  __syncthreads();
+  const bool csr_ok = s_csr_ok != 0;
+  // per entry: claim the request (a second claim marks it listed twice), check its
+  // lengths, and compare the start of its table with the prefix's ids
+  for (int k = tid; k < M; k += nthr) {
+    int pb_ok = 0;
+    const int i = csr_ok ? __ldg(g.members + k) : -1;
+    s_req[k] = i;
+    if (i >= 0 && i < n) {
+      if (atomicCAS(&s_entry[i], -1, k) != -1) atomicExch(&s_entry[i], -2);
+      int lo = 0, hi = G - 1;  // the entry's group: last gi with start[gi] <= k
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_start[mid] <= k) lo = mid; else hi = mid - 1;
+      }
+      const int pb = s_blocks[lo];
+      const int64_t q0 = __ldg(p.qsl + i), q1 = __ldg(p.qsl + i + 1), L = __ldg(p.seq_lens + i);
+      if (pb >= 1 && pb <= g.max_blocks && q0 >= 0 && q1 == q0 + 1 && q1 <= p.num_tokens && L <= p.max_seq_len &&
+          (L + kBlock - 1) / kBlock <= p.max_blocks && L > static_cast<int64_t>(pb) * kBlock) {
+        const int32_t* own = p.bt + static_cast<int64_t>(i) * p.max_blocks;
+        const int32_t* pre = g.tables + static_cast<int64_t>(lo) * g.max_blocks;
+        int diff = 0;
+        if (((reinterpret_cast<uintptr_t>(own) | reinterpret_cast<uintptr_t>(pre)) & 15) == 0) {
+          const int n4 = pb / 4;
+          // four 16-byte loads of each row in flight at a time
+          for (int q0v = 0; q0v < n4; q0v += 4) {
+            int4 a[4], b[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              if (q0v + u < n4) {
+                a[u] = __ldg(reinterpret_cast<const int4*>(own) + q0v + u);
+                b[u] = __ldg(reinterpret_cast<const int4*>(pre) + q0v + u);
+              }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              if (q0v + u < n4) diff |= (a[u].x != b[u].x) | (a[u].y != b[u].y) | (a[u].z != b[u].z) | (a[u].w != b[u].w);
+          }
+          for (int j = 4 * n4; j < pb; ++j) diff |= __ldg(own + j) != __ldg(pre + j);
+        } else {
+          for (int j = 0; j < pb; ++j) diff |= __ldg(own + j) != __ldg(pre + j);
+        }
+        pb_ok = diff ? 0 : pb;
+      }
+    }
+    s_pb[k] = pb_ok;
+  }
+  __syncthreads();
+  // a request is a member iff exactly one entry claimed it and that entry passed
+  for (int i = tid; i < n; i += nthr) {
+    const int k = s_entry[i];
+    const int pb = k >= 0 ? s_pb[k] : 0;
+    s_prefix[i] = pb * kBlock;
+    s_entry[i] = pb > 0 ? k : -1;
+    p.seq_prefix[i] = pb * kBlock;
+    p.seq_entry[i] = pb > 0 ? k : -1;
+  }
+  __syncthreads();
+  for (int k = tid; k < M; k += nthr) {
+    const int i = s_req[k];
+    p.member_ok[k] = (i >= 0 && i < n && s_entry[i] == k) ? 1 : 0;
+  }
+  // cascade items per group: member tiles x kv heads x prefix key splits
+  int carry = 0;
+  for (int base = 0; base < G; base += nthr) {
+    const int gi = base + tid;
+    int nu = 0;
+    if (gi < G && csr_ok) {
+      const int pb = s_blocks[gi];
+      const int cnt = s_start[gi + 1] - s_start[gi];
+      if (pb >= 1 && pb <= g.max_blocks && cnt > 0)
+        nu = ((cnt + p.cas_rows - 1) / p.cas_rows) * p.hkv * static_cast<int>(cascade_splits(int64_t(pb) * kBlock));
+    }
+    const int v[3] = {nu, 0, 0};
+    int ex[3], tot[3];
+    block_scan3(v, ex, tot);
+    if (gi < G) p.cas_prefix[gi] = carry + ex[0];
+    carry += tot[0];
+  }
+  if (tid == 0) p.cas_prefix[G] = carry;
+  __syncthreads();
+}
+
 // The writer CTAs of a fused step: a warp per 64-vector piece of a new token's rows
 // computes the token's slot (as slot_mapping_kernel does) and copies the piece of
 // its K and V rows into it (as write_kernel does), with the same error flags.  The
@@ -193,10 +306,9 @@ __device__ void plan_cascade(const PlanArgs& p) {
 // slot needs (the request's length, then its table entry).
 constexpr int kWriterQslMax = 8192;
 constexpr int kWriterPiece = 64;  // 16-byte vectors of a (token) row a warp moves: two per lane, K and V
-__device__ void write_new_tokens(const PlanArgs& p) {
-  __shared__ int32_t s_qsl[kWriterQslMax + 1];
+__device__ void write_new_tokens(const PlanArgs& p, int32_t* s_qsl) {
   const int lane = threadIdx.x & 31;
-  const bool staged = p.num_seqs <= kWriterQslMax;
+  const bool staged = p.num_seqs <= kWriterQslMax;  // (the launch then gives s_qsl num_seqs + 1 ints)
   if (staged) {
     for (int i = threadIdx.x; i <= p.num_seqs; i += blockDim.x) s_qsl[i] = __ldg(p.qsl + i);
     __syncthreads();
@@ -335,12 +447,12 @@ __device__ void order_prefill_pairs(const PlanArgs& p) {
 // A small decode batch -- at most kDecOrderMaxItemsPerSm items per SM, where the last
 // items decide when the kernel ends -- is handed out largest item first: the decode
 // requests sorted by the key tiles of their largest item (an unsplit request's whole
-// context, else one split), with the items' prefix in that order.  The decode kernel
-// maps a queue position through it and keeps storing partials by the request-order
-// item index.  Larger batches keep request order.
-constexpr int kDecOrderMaxItemsPerSm = 16;
+// context, else one split), with the items' prefix in that order, and for every queue
+// position the request and its first position, so that the decode kernel finds an
+// item's request with one load.  The decode kernel keeps storing partials by the
+// request-order item index.  Larger batches keep request order.
 constexpr int kDecOrderBuckets = 32;
-__device__ void order_decode_requests(const PlanArgs& p, int total) {
+__device__ void order_decode_requests(const PlanArgs& p, int total, const int32_t* seq_prefix) {
   __shared__ int bucket[kDecOrderBuckets];
   const int tid = threadIdx.x;
   if (tid < kDecOrderBuckets) bucket[tid] = 0;
@@ -351,7 +463,7 @@ __device__ void order_decode_requests(const PlanArgs& p, int total) {
       if (nd <= 0) continue;
       const int ns = nd / p.hkv;
       const bool cascade = p.cas.num_groups > 0 && p.cas.num_members > 0;
-      const int64_t keys = static_cast<int64_t>(p.seq_lens[i]) - (cascade ? p.seq_prefix[i] : 0);
+      const int64_t keys = static_cast<int64_t>(p.seq_lens[i]) - (cascade ? seq_prefix[i] : 0);
       const int64_t tiles = ns > 1 ? p.split_keys / kTileKeys : (keys + kTileKeys - 1) / kTileKeys;
       const int key = static_cast<int>(tiles < kDecOrderBuckets - 1 ? (tiles > 0 ? tiles : 0) : kDecOrderBuckets - 1);
       fn(kDecOrderBuckets - 1 - key, i);  // larger items in lower buckets
@@ -379,13 +491,16 @@ __device__ void order_decode_requests(const PlanArgs& p, int total) {
   for (int base = 0; base < p.num_seqs; base += blockDim.x) {
     const int k = base + tid;
     int v3[3] = {0, 0, 0};
+    int i = -1;
     if (k < nreq) {
-      const int i = p.dec_order[k];
+      i = p.dec_order[k];
       v3[0] = p.dec_prefix[i + 1] - p.dec_prefix[i];
     }
     int ex[3], tot[3];
     block_scan3(v3, ex, tot);
-    if (k < p.num_seqs) p.dec_start[k] = carry + ex[0];
+    const int start = carry + ex[0];
+    if (k < p.num_seqs) p.dec_start[k] = start;
+    for (int m = 0; m < v3[0]; ++m) reinterpret_cast<int2*>(p.dec_pos)[start + m] = make_int2(i, start);
     carry += tot[0];
   }
   if (tid == 0) {
@@ -395,12 +510,13 @@ __device__ void order_decode_requests(const PlanArgs& p, int total) {
 }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs p) {
+  extern __shared__ int32_t plan_smem[];  // writers: query_start_loc; planner: on-chip membership
   // the previous step's kernels read the workspace this rewrites and the cache the
   // writers write: wait for them
   grid_dep_wait();
   grid_dep_launch();
   if (blockIdx.x > 0) {  // writer CTAs never join the planner's block barriers
-    write_new_tokens(p);
+    write_new_tokens(p, plan_smem);
     return;
   }
   const int64_t n_units = static_cast<int64_t>(p.num_seqs) * p.hkv;
@@ -409,7 +525,18 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs p) {
   }
   if (threadIdx.x < kNumQueueCounters) p.counters[threadIdx.x] = 0;
   const bool cascade = p.cas.num_groups > 0 && p.cas.num_members > 0;
-  if (cascade) plan_cascade(p);
+  const int32_t* seq_pre = p.seq_prefix;  // each request's prefix tokens and member entry
+  const int32_t* seq_ent = p.seq_entry;
+  if (cascade) {
+    if (p.cas_onchip) {
+      int32_t *sp = nullptr, *se = nullptr;
+      plan_cascade_onchip(p, plan_smem, sp, se);
+      seq_pre = sp;
+      seq_ent = se;
+    } else {
+      plan_cascade(p);
+    }
+  }
   __syncthreads();
   int carry_d = 0, carry_p = 0, carry_m = 0;
   for (int base = 0; base < p.num_seqs; base += blockDim.x) {
@@ -424,7 +551,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs p) {
         flag_error(p.err, kErrLength);  // rows cannot be addressed: no item
       } else if (q_len == 1) {
         const bool ok = L >= 1 && L <= p.max_seq_len && (L + kBlock - 1) / kBlock <= p.max_blocks;
-        const int P = cascade ? p.seq_prefix[i] : 0;  // keys the cascade kernel attends
+        const int P = cascade ? seq_pre[i] : 0;  // keys the cascade kernel attends
         const int ns = ok ? static_cast<int>(decode_splits(L - P)) : 1;
         nd = p.hkv * ns;
         nm = ns > 1 ? 1 : 0;  // its partials need the split merge (a member of one split
@@ -439,7 +566,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs p) {
     if (i < p.num_seqs) {
       p.dec_prefix[i] = carry_d + ex[0];
       p.pre_prefix[i] = carry_p + ex[1];
-      if (nm) p.merge_list[carry_m + ex[2]] = i;
+      if (nm) {  // everything the split merge needs about the request, in one 32-byte record
+        int4* m = reinterpret_cast<int4*>(p.merge_list) + 2 * static_cast<int64_t>(carry_m + ex[2]);
+        m[0] = make_int4(i, carry_d + ex[0], nd / p.hkv, static_cast<int>(p.qsl[i]));
+        m[1] = make_int4(cascade ? seq_pre[i] : 0, cascade ? seq_ent[i] : -1, 0, 0);
+      }
     }
     carry_d += tot[0];
     carry_p += tot[1];
@@ -451,7 +582,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs p) {
   }
   // (carry_p and carry_d are the same in every thread)
   if (carry_p > 0 && p.pre_order) order_prefill_pairs(p);
-  if (carry_d > 0 && p.dec_order && carry_d <= kDecOrderMaxItemsPerSm * p.num_sms) order_decode_requests(p, carry_d);
+  if (carry_d > 0 && p.dec_order && carry_d <= kDecOrderMaxItemsPerSm * p.num_sms && carry_d <= kDecPosMax)
+    order_decode_requests(p, carry_d, seq_pre);
   if (threadIdx.x == 0) {
     p.counters[kMergeCountSlot] = carry_m;
   }
@@ -460,9 +592,25 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs p) {
 }  // namespace
 
 int launch_plan(const PlanArgs& p, cudaStream_t s) {
-  TraceScope trace(kTracePlan, s);
   const int writers = p.k_new ? p.write_ctas : 0;
-  return cuda_status(launch_k(plan_kernel, dim3(1 + writers), dim3(kPlanThreads), 0, s, p));
+  // dynamic shared memory: query_start_loc for the writers, the membership state for
+  // the planner (on chip when the batch is within the limits), whichever is larger
+  PlanArgs q = p;
+  size_t smem = 0;
+  if (writers > 0 && p.num_seqs <= kWriterQslMax) smem = (static_cast<size_t>(p.num_seqs) + 1) * sizeof(int32_t);
+  const bool cascade = p.cas.num_groups > 0 && p.cas.num_members > 0;
+  q.cas_onchip = cascade && p.num_seqs <= kCasOnchipSeqs && p.cas.num_members <= kCasOnchipMembers &&
+                 p.cas.num_groups <= kCasOnchipGroups && p.cas.max_blocks <= kCasOnchipBlocks;
+  if (q.cas_onchip) {
+    const size_t need = (2 * static_cast<size_t>(p.num_seqs) + 2 * static_cast<size_t>(p.cas.num_members) +
+                         2 * static_cast<size_t>(p.cas.num_groups) + 1) * sizeof(int32_t);
+    smem = need > smem ? need : smem;
+  }
+  static uint64_t smem_set = 0;
+  const int st = set_smem_once(reinterpret_cast<const void*>(plan_kernel), kPlanSmemMax, &smem_set);
+  if (st) return st;
+  TraceScope trace(kTracePlan, s);
+  return cuda_status(launch_k(plan_kernel, dim3(1 + writers), dim3(kPlanThreads), smem, s, q));
 }
 
 }  // namespace pkv

@@ -344,7 +344,8 @@ __device__ void producer_warp(const PrefillParams& P, const CUtensorMap* qmap, c
       break;
     }
     if (lane == 0) {
-      const int idx = atomicAdd(P.queue, 1);
+      // every CTA's first item is its own index; later ones come off the queue after those
+      const int idx = it == 0 ? static_cast<int>(blockIdx.x) : static_cast<int>(gridDim.x) + atomicAdd(P.queue, 1);
       c.ring[slot] = kCas ? make_cas_item(P, idx, total) : make_item(P, idx, total);
       c.bad[slot] = 0;
       mbar_arrive(&c.item_full[slot]);

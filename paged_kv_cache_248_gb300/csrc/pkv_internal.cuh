@@ -33,6 +33,11 @@ constexpr int kNumQueueCounters = 8; // work-queue counters in the workspace
 constexpr int kMergeCountSlot = 2;   // counters[2]: number of requests in the merge list
 constexpr int kCascadeQueueSlot = 3; // counters[3]: the shared-prefix kernel's work queue
 constexpr int kDecOrderSlot = 4;     // counters[4]: 1 when the decode items follow dec_order
+// A decode batch the planner orders (at most 16 items per SM) also gets a direct map
+// from queue position to (request, the request's first position); sized for GPUs of
+// up to 256 SMs.
+constexpr int kDecOrderMaxItemsPerSm = 16;
+constexpr int kDecPosMax = kDecOrderMaxItemsPerSm * 256;
 
 // Shared-prefix (cascade) key splits: a prefix of P tokens is attended in pieces of
 // kCascadeSplitKeys keys, a function of P alone.
@@ -158,8 +163,10 @@ struct Workspace {
   int32_t* pre_order;    // [2 * max_pre_units] prefill pairs, heaviest first: (pair id in request order, its request)
   int32_t* dec_order;    // [num_seqs] decode requests, largest item first (small batches)
   int32_t* dec_start;    // [num_seqs + 1] exclusive prefix of decode items in that order
+  int32_t* dec_pos;      // [2 * kDecPosMax] per queue position of an ordered batch: (request, first position)
   int32_t* unit_bad;     // [num_seqs * hkv] a split saw a bad block id
-  int32_t* merge_list;   // [num_seqs] decode requests cut into several splits
+  int32_t* merge_list;   // [num_seqs][8] decode requests cut into several splits: (request, its first
+                         // item, splits, query row, prefix keys, member entry, 0, 0)
   float* part_ml;        // [max_dec_items * GP * 2] split running max and sum
   float* part_o;         // [max_dec_items * head_dim * GP] split accumulators
   // shared-prefix (cascade) state; all null without prefix groups
@@ -219,6 +226,7 @@ struct PlanArgs {
   int32_t* pre_order = nullptr;  // heaviest-first order of the prefill pairs, two ints per position
   int32_t* dec_order = nullptr;  // largest-item-first order of the decode requests
   int32_t* dec_start = nullptr;
+  int32_t* dec_pos = nullptr;
   int32_t num_sms = 0;
   int64_t max_pre_units = 0;
   int32_t rows_q = 0;            // query tokens per prefill tile
@@ -235,6 +243,7 @@ struct PlanArgs {
   int64_t num_slots = 0;         // num_blocks * 16
   int32_t vec_per_row = 0;       // 16-byte vectors per (token, kv head) row
   int32_t write_ctas = 0;        // CTAs after the planning CTA that do the writes
+  int32_t cas_onchip = 0;        // set by launch_plan: the membership checks run in shared memory
 };
 // One launch: CTA 0 plans; CTAs 1..write_ctas (if any) map and scatter the new tokens.
 int launch_plan(const PlanArgs& p, cudaStream_t s);

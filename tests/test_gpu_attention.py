@@ -375,3 +375,26 @@ def test_seq_len_shorter_than_query_is_flagged(pkv):
                               m["query_start_loc"], w.scale, 1, 64)
     assert pkv.pkv_get_last_error() == pkv.PKV_ERR_INDEX
     assert torch.count_nonzero(out[1]) == 0 and torch.count_nonzero(out[0]) > 0
+
+
+def test_both_merge_launches_give_the_same_bits(pkv):
+    # Requests of 3 to 8 key splits are merged by one thread per column when no request
+    # of the batch folds more partials than that, and by four 128-thread runs otherwise;
+    # both fold in the same order.  The same requests in a batch with a 9-split request
+    # (the general merge) and without it (the per-thread merge) give identical rows,
+    # and both match the oracle.
+    lens = [2049, 3000, 4096, 5121, 8000, 300]
+    w_small = wl.sized_case(45, lens, [1] * len(lens), 32, 8, 128, "bf16")
+    w_big = wl.sized_case(45, lens + [9000], [1] * (len(lens) + 1), 32, 8, 128, "bf16")
+    t_cpu = w_big.make_tensors("cpu")
+    t = {k: v.cuda() for k, v in t_cpu.items()}
+    # the small batch's tables are the big batch's first rows, so both read the same keys
+    w_small = dataclasses.replace(w_small, num_blocks=w_big.num_blocks,
+                                  block_tables=w_big.block_tables[:len(lens), :w_big.block_tables.shape[1]].copy())
+    t_small = dict(t, q=t["q"][:len(lens)].contiguous())
+    small = _attention_only(pkv, w_small, t_small)
+    big = _attention_only(pkv, w_big, t)
+    assert torch.equal(small, big[:len(lens)])
+    ref = oracle.attention(bits(t_cpu["q"]), bits(t_cpu["k_cache"]), bits(t_cpu["v_cache"]), w_big.block_tables,
+                           w_big.seq_lens, w_big.query_start_loc, w_big.scale)
+    compare(big, ref, "bf16", w_big.name)

@@ -212,3 +212,20 @@ def test_cascade_step_replays_from_a_cuda_graph(pkv):
     torch.cuda.synchronize()
     assert pkv.pkv_get_last_error() == 0
     assert torch.equal(out_g, out_e)
+
+
+@pytest.mark.parametrize("prefix_blocks", [(520, 7), (513, 513)])
+def test_long_prefixes_take_the_global_membership_checks(pkv, prefix_blocks):
+    # a prefix table longer than 512 blocks makes the planner check membership in
+    # global memory instead of shared memory; with the bad hints of
+    # shared_prefix_case (a chunk, a context inside the prefix, a request listed
+    # twice, a table of its own) the result is the same as without groups
+    w, hints = wl.shared_prefix_case(13, prefix_blocks=prefix_blocks, members=(4, 3), max_suffix=200, bystanders=3)
+    t_cpu = w.make_tensors("cpu")
+    t = {k: v.cuda() for k, v in t_cpu.items()}
+    plain, cas, st = run_both(pkv, w, hints, t)
+    assert st == 0
+    ref = oracle.attention(bits(t_cpu["q"]), bits(t_cpu["k_cache"]), bits(t_cpu["v_cache"]), w.block_tables,
+                           w.seq_lens, w.query_start_loc, w.scale)
+    compare(cas, ref, "bf16", w.name)
+    compare(plain, ref, "bf16", w.name + " (no groups)")
