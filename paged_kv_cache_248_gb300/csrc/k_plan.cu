@@ -28,7 +28,7 @@ namespace pkv {
 namespace {
 
 constexpr int kPlanThreads = 1024;
-constexpr int kPlanSmemMax = 144 * 1024;  // dynamic shared memory the plan launch may ask for
+constexpr int kPlanSmemMax = 196 * 1024;  // dynamic shared memory the plan launch may ask for
 
 __device__ __forceinline__ int warp_inclusive_scan(int v) {
   const int lane = threadIdx.x & 31;
@@ -182,27 +182,34 @@ __device__ void plan_cascade(const PlanArgs& p) {
 }
 
 // The same membership decisions with every intermediate state in shared memory (`sm`,
-// the launch's dynamic buffer), for batches within the limits below: the planner then
-// waits on three rounds of global loads (the group offsets; each entry's request; that
-// request's lengths, group and table rows) instead of one or more per phase.  Leaves
-// each request's prefix tokens and member entry in shared memory for the rest of the
-// plan, and writes the global copies the other kernels read.  Called by the whole block.
+// the launch's dynamic buffer), for batches within the limits below.  One pass over
+// (entry, 16-id chunk) pairs makes every check at once -- the chunk-0 thread of an
+// entry claims the request and checks its lengths, every thread compares its chunk of
+// the request's table with the prefix's -- so the planner waits on three rounds of
+// global loads (the group offsets; each entry's request; that request's lengths and
+// table rows) instead of one or more per phase.  Leaves each request's prefix tokens
+// and member entry in shared memory for the rest of the plan and writes the global
+// copies the other kernels read.  Called by the whole block.
 constexpr int kCasOnchipSeqs = 8192;
 constexpr int kCasOnchipMembers = 8192;
 constexpr int kCasOnchipGroups = 1024;
-constexpr int kCasOnchipBlocks = 512;  // longest prefix whose table one thread compares
+constexpr int kCasOnchipBlocks = 512;  // longest prefix table compared in this pass
+__host__ __device__ constexpr int64_t cas_onchip_ints(int64_t n, int64_t m, int64_t g) { return 2 * n + 3 * m + 2 * g + 1; }
 __device__ void plan_cascade_onchip(const PlanArgs& p, int32_t* sm, int32_t*& s_prefix, int32_t*& s_entry) {
   __shared__ int s_csr_ok;
+  constexpr int kChunk = 16;
   const CascadeArgs& g = p.cas;
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int n = p.num_seqs, M = g.num_members, G = g.num_groups;
   s_entry = sm;                    // [n]: claiming entry; -1 none; -2 listed more than once
   s_prefix = s_entry + n;          // [n]: prefix tokens of a member, else 0
-  int32_t* s_pb = s_prefix + n;    // [M]: the entry's prefix blocks if it passed its checks, else 0
+  int32_t* s_pb = s_prefix + n;    // [M]: the entry's prefix blocks if its lengths pass, else 0
   int32_t* s_req = s_pb + M;       // [M]: the entry's request
-  int32_t* s_start = s_req + M;    // [G + 1]
+  int32_t* s_diff = s_req + M;     // [M]: some chunk of the table differs from the prefix
+  int32_t* s_start = s_diff + M;   // [G + 1]
   int32_t* s_blocks = s_start + G + 1;  // [G]
   for (int i = tid; i < n; i += nthr) s_entry[i] = -1;
+  for (int k = tid; k < M; k += nthr) s_diff[k] = 0;
   for (int k = tid; k <= G; k += nthr) s_start[k] = __ldg(g.start + k);
   for (int k = tid; k < G; k += nthr) s_blocks[k] = __ldg(g.blocks + k);
   if (tid == 0) s_csr_ok = 1;
@@ -212,56 +219,54 @@ __device__ void plan_cascade_onchip(const PlanArgs& p, int32_t* sm, int32_t*& s_
     if (s_start[k] > s_start[k + 1]) s_csr_ok = 0;  // CSR offsets must not decrease
   __syncthreads();
   const bool csr_ok = s_csr_ok != 0;
-  // per entry: claim the request (a second claim marks it listed twice), check its
-  // lengths, and compare the start of its table with the prefix's ids
-  for (int k = tid; k < M; k += nthr) {
-    int pb_ok = 0;
-    const int i = csr_ok ? __ldg(g.members + k) : -1;
-    s_req[k] = i;
-    if (i >= 0 && i < n) {
-      if (atomicCAS(&s_entry[i], -1, k) != -1) atomicExch(&s_entry[i], -2);
-      int lo = 0, hi = G - 1;  // the entry's group: last gi with start[gi] <= k
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (s_start[mid] <= k) lo = mid; else hi = mid - 1;
-      }
-      const int pb = s_blocks[lo];
-      const int64_t q0 = __ldg(p.qsl + i), q1 = __ldg(p.qsl + i + 1), L = __ldg(p.seq_lens + i);
-      if (pb >= 1 && pb <= g.max_blocks && q0 >= 0 && q1 == q0 + 1 && q1 <= p.num_tokens && L <= p.max_seq_len &&
-          (L + kBlock - 1) / kBlock <= p.max_blocks && L > static_cast<int64_t>(pb) * kBlock) {
-        const int32_t* own = p.bt + static_cast<int64_t>(i) * p.max_blocks;
-        const int32_t* pre = g.tables + static_cast<int64_t>(lo) * g.max_blocks;
-        int diff = 0;
-        if (((reinterpret_cast<uintptr_t>(own) | reinterpret_cast<uintptr_t>(pre)) & 15) == 0) {
-          const int n4 = pb / 4;
-          // four 16-byte loads of each row in flight at a time
-          for (int q0v = 0; q0v < n4; q0v += 4) {
-            int4 a[4], b[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              if (q0v + u < n4) {
-                a[u] = __ldg(reinterpret_cast<const int4*>(own) + q0v + u);
-                b[u] = __ldg(reinterpret_cast<const int4*>(pre) + q0v + u);
-              }
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-              if (q0v + u < n4) diff |= (a[u].x != b[u].x) | (a[u].y != b[u].y) | (a[u].z != b[u].z) | (a[u].w != b[u].w);
-          }
-          for (int j = 4 * n4; j < pb; ++j) diff |= __ldg(own + j) != __ldg(pre + j);
-        } else {
-          for (int j = 0; j < pb; ++j) diff |= __ldg(own + j) != __ldg(pre + j);
-        }
-        pb_ok = diff ? 0 : pb;
-      }
+  const int chunks = (g.max_blocks + kChunk - 1) / kChunk;
+  const int64_t work = csr_ok ? static_cast<int64_t>(M) * chunks : 0;
+  for (int64_t wi = tid; wi < work; wi += nthr) {
+    const int k = static_cast<int>(wi / chunks), j0 = static_cast<int>(wi % chunks) * kChunk;
+    const int i = __ldg(g.members + k);
+    const bool i_ok = i >= 0 && i < n;
+    int lo = 0, hi = G - 1;  // the entry's group: last gi with start[gi] <= k
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_start[mid] <= k) lo = mid; else hi = mid - 1;
     }
-    s_pb[k] = pb_ok;
+    const int pb = s_blocks[lo];
+    const bool pb_ok = pb >= 1 && pb <= g.max_blocks && pb <= p.max_blocks;  // (also keeps the reads in the rows)
+    if (j0 == 0) {  // the entry's own checks, once
+      int keep = 0;
+      if (i_ok) {
+        if (atomicCAS(&s_entry[i], -1, k) != -1) atomicExch(&s_entry[i], -2);  // a second claim: listed twice
+        const int64_t q0 = __ldg(p.qsl + i), q1 = __ldg(p.qsl + i + 1), L = __ldg(p.seq_lens + i);
+        if (pb_ok && q0 >= 0 && q1 == q0 + 1 && q1 <= p.num_tokens && L <= p.max_seq_len &&
+            (L + kBlock - 1) / kBlock <= p.max_blocks && L > static_cast<int64_t>(pb) * kBlock)
+          keep = pb;
+      }
+      s_req[k] = i_ok ? i : -1;
+      s_pb[k] = keep;
+    }
+    if (i_ok && pb_ok && j0 < pb) {  // this chunk of the request's table against the prefix's
+      const int32_t* own = p.bt + static_cast<int64_t>(i) * p.max_blocks;
+      const int32_t* pre = g.tables + static_cast<int64_t>(lo) * g.max_blocks;
+      const int j1 = min(pb, j0 + kChunk);
+      int diff = 0;
+      if (j1 - j0 == kChunk && ((reinterpret_cast<uintptr_t>(own + j0) | reinterpret_cast<uintptr_t>(pre + j0)) & 15) == 0) {
+#pragma unroll
+        for (int q = 0; q < kChunk / 4; ++q) {
+          const int4 a = __ldg(reinterpret_cast<const int4*>(own + j0) + q);
+          const int4 b = __ldg(reinterpret_cast<const int4*>(pre + j0) + q);
+          diff |= (a.x != b.x) | (a.y != b.y) | (a.z != b.z) | (a.w != b.w);
+        }
+      } else {
+        for (int j = j0; j < j1; ++j) diff |= __ldg(own + j) != __ldg(pre + j);
+      }
+      if (diff) s_diff[k] = 1;
+    }
   }
   __syncthreads();
   // a request is a member iff exactly one entry claimed it and that entry passed
   for (int i = tid; i < n; i += nthr) {
     const int k = s_entry[i];
-    const int pb = k >= 0 ? s_pb[k] : 0;
+    const int pb = (k >= 0 && !s_diff[k]) ? s_pb[k] : 0;
     s_prefix[i] = pb * kBlock;
     s_entry[i] = pb > 0 ? k : -1;
     p.seq_prefix[i] = pb * kBlock;
@@ -269,8 +274,8 @@ __device__ void plan_cascade_onchip(const PlanArgs& p, int32_t* sm, int32_t*& s_
   }
   __syncthreads();
   for (int k = tid; k < M; k += nthr) {
-    const int i = s_req[k];
-    p.member_ok[k] = (i >= 0 && i < n && s_entry[i] == k) ? 1 : 0;
+    const int i = csr_ok ? s_req[k] : -1;
+    p.member_ok[k] = (i >= 0 && s_entry[i] == k) ? 1 : 0;
   }
   // cascade items per group: member tiles x kv heads x prefix key splits
   int carry = 0;
@@ -509,6 +514,48 @@ __device__ void order_decode_requests(const PlanArgs& p, int total, const int32_
   }
 }
 
+// The same order built entirely in shared memory, for batches of at most kOrdOnchipSeqs
+// requests: the main loop leaves each request's decode item count and bucket in
+// s_nd / s_key, and only the position table goes to global memory (the decode
+// kernel reads nothing else of an ordered batch).
+constexpr int kOrdOnchipSeqs = 4096;
+__device__ void order_decode_onchip(const PlanArgs& p, const int32_t* s_nd, const int32_t* s_key, int32_t* s_order) {
+  __shared__ int bucket[kDecOrderBuckets];
+  const int tid = threadIdx.x;
+  if (tid < kDecOrderBuckets) bucket[tid] = 0;
+  __syncthreads();
+  for (int i = tid; i < p.num_seqs; i += blockDim.x)
+    if (s_nd[i] > 0) atomicAdd(&bucket[s_key[i]], 1);
+  __syncthreads();
+  if (tid < 32) {  // exclusive prefix over the buckets, one warp
+    const int v = bucket[tid];
+    int inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, inc, o);
+      if (tid >= o) inc += n;
+    }
+    bucket[tid] = inc - v;
+  }
+  __syncthreads();
+  for (int i = tid; i < p.num_seqs; i += blockDim.x)
+    if (s_nd[i] > 0) s_order[atomicAdd(&bucket[s_key[i]], 1)] = i;
+  __syncthreads();
+  const int nreq = bucket[kDecOrderBuckets - 1];  // every decode request has a place
+  int carry = 0;
+  for (int base = 0; base < nreq; base += blockDim.x) {
+    const int k = base + tid;
+    const int i = k < nreq ? s_order[k] : -1;
+    int v3[3] = {k < nreq ? s_nd[i] : 0, 0, 0};
+    int ex[3], tot[3];
+    block_scan3(v3, ex, tot);
+    const int start = carry + ex[0];
+    for (int m = 0; m < v3[0]; ++m) reinterpret_cast<int2*>(p.dec_pos)[start + m] = make_int2(i, start);
+    carry += tot[0];
+  }
+  if (tid == 0) p.counters[kDecOrderSlot] = 1;
+}
+
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs p) {
   extern __shared__ int32_t plan_smem[];  // writers: query_start_loc; planner: on-chip membership
   // the previous step's kernels read the workspace this rewrites and the cache the
@@ -538,10 +585,17 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs p) {
     }
   }
   __syncthreads();
+  // on-chip ordering state after the membership region: items and bucket per request
+  int32_t* s_nd = nullptr;
+  int32_t* s_key = nullptr;
+  if (p.ord_onchip) {
+    s_nd = plan_smem + p.ord_offset;
+    s_key = s_nd + p.num_seqs;
+  }
   int carry_d = 0, carry_p = 0, carry_m = 0;
   for (int base = 0; base < p.num_seqs; base += blockDim.x) {
     const int i = base + threadIdx.x;
-    int nd = 0, np = 0, nm = 0;
+    int nd = 0, np = 0, nm = 0, key = 0;
     if (i < p.num_seqs) {
       const int64_t q0 = p.qsl[i], q1 = p.qsl[i + 1];
       const int64_t L = p.seq_lens[i];
@@ -554,6 +608,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs p) {
         const int P = cascade ? seq_pre[i] : 0;  // keys the cascade kernel attends
         const int ns = ok ? static_cast<int>(decode_splits(L - P)) : 1;
         nd = p.hkv * ns;
+        // the request's bucket for a largest-first order: key tiles of its largest item
+        const int64_t tiles = ns > 1 ? p.split_keys / kTileKeys : (L - P + kTileKeys - 1) / kTileKeys;
+        key = kDecOrderBuckets - 1 - static_cast<int>(tiles < kDecOrderBuckets - 1 ? (tiles > 0 ? tiles : 0)
+                                                                                   : kDecOrderBuckets - 1);
         nm = ns > 1 ? 1 : 0;  // its partials need the split merge (a member of one split
                               // folds its prefix partials in the decode kernel)
       } else if (q_len > 1) {
@@ -563,6 +621,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs p) {
     const int v[3] = {nd, np, nm};
     int ex[3], tot[3];
     block_scan3(v, ex, tot);
+    if (i < p.num_seqs && s_nd) {
+      s_nd[i] = nd;
+      s_key[i] = key;
+    }
     if (i < p.num_seqs) {
       p.dec_prefix[i] = carry_d + ex[0];
       p.pre_prefix[i] = carry_p + ex[1];
@@ -582,8 +644,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs p) {
   }
   // (carry_p and carry_d are the same in every thread)
   if (carry_p > 0 && p.pre_order) order_prefill_pairs(p);
-  if (carry_d > 0 && p.dec_order && carry_d <= kDecOrderMaxItemsPerSm * p.num_sms && carry_d <= kDecPosMax)
-    order_decode_requests(p, carry_d, seq_pre);
+  if (carry_d > 0 && p.dec_order && carry_d <= kDecOrderMaxItemsPerSm * p.num_sms && carry_d <= kDecPosMax) {
+    if (p.ord_onchip) order_decode_onchip(p, s_nd, s_key, s_key + p.num_seqs);
+    else order_decode_requests(p, carry_d, seq_pre);
+  }
   if (threadIdx.x == 0) {
     p.counters[kMergeCountSlot] = carry_m;
   }
@@ -601,11 +665,18 @@ int launch_plan(const PlanArgs& p, cudaStream_t s) {
   const bool cascade = p.cas.num_groups > 0 && p.cas.num_members > 0;
   q.cas_onchip = cascade && p.num_seqs <= kCasOnchipSeqs && p.cas.num_members <= kCasOnchipMembers &&
                  p.cas.num_groups <= kCasOnchipGroups && p.cas.max_blocks <= kCasOnchipBlocks;
-  if (q.cas_onchip) {
-    const size_t need = (2 * static_cast<size_t>(p.num_seqs) + 2 * static_cast<size_t>(p.cas.num_members) +
-                         2 * static_cast<size_t>(p.cas.num_groups) + 1) * sizeof(int32_t);
-    smem = need > smem ? need : smem;
-  }
+  q.ord_onchip = p.dec_order != nullptr && p.num_seqs <= kOrdOnchipSeqs;
+  // the planner's layout: membership region, then ordering region (each dropped to its
+  // global-memory form if the two would not fit)
+  auto planner_ints = [&]() {
+    int64_t ints = q.cas_onchip ? cas_onchip_ints(p.num_seqs, p.cas.num_members, p.cas.num_groups) : 0;
+    q.ord_offset = static_cast<int32_t>(ints);
+    return ints + (q.ord_onchip ? 3 * static_cast<int64_t>(p.num_seqs) : 0);  // items, bucket, order
+  };
+  if (planner_ints() * 4 > kPlanSmemMax) q.ord_onchip = 0;
+  if (planner_ints() * 4 > kPlanSmemMax) q.cas_onchip = 0;
+  const size_t need = static_cast<size_t>(planner_ints()) * sizeof(int32_t);
+  smem = need > smem ? need : smem;
   static uint64_t smem_set = 0;
   const int st = set_smem_once(reinterpret_cast<const void*>(plan_kernel), kPlanSmemMax, &smem_set);
   if (st) return st;

@@ -191,10 +191,11 @@ __device__ __forceinline__ float row_extremum(uint32_t taddr, int nvis) {
 // The exponents 2^(scale * s - m_ref) of one S row (masked keys: 0, with kMask),
 // written back as bf16 P over the row's first 64 columns; returns the row sum.  Each
 // 32-column piece is loaded while the previous one is converted, and the 16 P columns
-// a piece gives land on columns this thread has already read.
+// a piece gives land on columns this thread has already read.  A masked key's scaled
+// score is set to -inf before its exponent (an infinite raw score would give NaN at
+// scale 0).
 template <bool kMask>
 __device__ __forceinline__ float row_exp_to_p(uint32_t taddr, int nvis, float scale, float m_ref) {
-  const float hidden = scale >= 0.f ? -INFINITY : INFINITY;  // raw score that scales to -inf
   float ls[4] = {0.f, 0.f, 0.f, 0.f};  // the row sum in four independent parts (two packed pairs)
   uint32_t a[32], b[32];
   tmem_ld32_issue(taddr, a);
@@ -208,12 +209,10 @@ __device__ __forceinline__ float row_exp_to_p(uint32_t taddr, int nvis, float sc
 #pragma unroll
     for (int q = 0; q < 16; ++q) {
       const int k = 32 * h + 2 * q;
-      const float xa = (!kMask || k < nvis) ? __uint_as_float(cur[2 * q]) : hidden;
-      const float xb = (!kMask || k + 1 < nvis) ? __uint_as_float(cur[2 * q + 1]) : hidden;
       float ya, yb;
-      ffma2(ya, yb, xa, xb, scale, -m_ref);
-      const float pa = ex2_approx(ya);
-      const float pb = ex2_approx(yb);
+      ffma2(ya, yb, __uint_as_float(cur[2 * q]), __uint_as_float(cur[2 * q + 1]), scale, -m_ref);
+      const float pa = ex2_approx((!kMask || k < nvis) ? ya : -INFINITY);
+      const float pb = ex2_approx((!kMask || k + 1 < nvis) ? yb : -INFINITY);
       if (q & 1) fadd2(ls[2], ls[3], pa, pb);
       else fadd2(ls[0], ls[1], pa, pb);
       __nv_bfloat162 h2 = __floats2bfloat162_rn(pa, pb);
@@ -676,8 +675,9 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uin
       // keys k0 .. k0 + nvis - 1 are visible to this row (cascade: the whole split).
       // The scores stay unscaled: the tile maximum of scale * s is scale times the
       // maximum of s (the minimum, for a negative scale), and each exponent takes
-      // scale * s - m in one fused multiply-add.  Masked keys get the raw value that
-      // scales to -inf.  Tiles every row of the warp sees whole skip the masking.
+      // scale * s - m in one fused multiply-add.  Masked keys count for no extremum and
+      // their scaled scores become -inf before the exponent.  Tiles every row of the
+      // warp sees whole skip the masking.
       const int nvis = kCas ? tkend - k0 : pos - k0 + 1;
       const bool whole = __all_sync(0xffffffffu, nvis >= kTileKeys);
       const uint32_t srow = tmem + lane_off + s_col;

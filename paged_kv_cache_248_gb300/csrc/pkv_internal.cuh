@@ -244,6 +244,8 @@ struct PlanArgs {
   int32_t vec_per_row = 0;       // 16-byte vectors per (token, kv head) row
   int32_t write_ctas = 0;        // CTAs after the planning CTA that do the writes
   int32_t cas_onchip = 0;        // set by launch_plan: the membership checks run in shared memory
+  int32_t ord_onchip = 0;        // set by launch_plan: the decode order is built in shared memory
+  int32_t ord_offset = 0;        //   at this int offset of the planner's dynamic shared memory
 };
 // One launch: CTA 0 plans; CTAs 1..write_ctas (if any) map and scatter the new tokens.
 int launch_plan(const PlanArgs& p, cudaStream_t s);

@@ -398,3 +398,12 @@ def test_both_merge_launches_give_the_same_bits(pkv):
     ref = oracle.attention(bits(t_cpu["q"]), bits(t_cpu["k_cache"]), bits(t_cpu["v_cache"]), w_big.block_tables,
                            w_big.seq_lens, w_big.query_start_loc, w_big.scale)
     compare(big, ref, "bf16", w_big.name)
+
+
+def test_zero_scale_averages_the_visible_values(pkv):
+    # scale 0: every visible key weighs the same, so each row is the mean of its
+    # visible V rows (the oracle computes that exactly); masked keys of diagonal and
+    # partial tiles must weigh nothing rather than turn into NaN
+    w = dataclasses.replace(wl.random_case(46, num_seqs=10, max_ctx=900, max_q=300, group=4, num_kv_heads=2,
+                                           head_dim=128, dtype="bf16"), scale=0.0)
+    run_pair(pkv, w)
