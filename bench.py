@@ -39,28 +39,29 @@ import workloads as wl  # noqa: E402
 METRIC = "decode KV-read GB/s (% of HBM peak); mixed-step tokens/sec at 1 GB300"
 
 
-# DRAM traffic of the decode kernel per algorithmic byte, from one ncu capture of one
-# decode launch on the batched-decode workload (dram__bytes_read.sum +
-# dram__bytes_write.sum = 505.15 MB + 4.63 MB for 503.62 MB of algorithmic bytes).
-# It scales to other workloads by the bytes processed, and it is reported only while
-# the profiled sources are unchanged.
+# DRAM traffic of the decode kernel per algorithmic byte, from one-pass ncu captures of one
+# decode launch of each workload (dram__bytes_read.sum + dram__bytes_write.sum):
+#   mixed step:      19.4999 GB + 36.4 MB for 19.409 GB of algorithmic bytes;
+#   batched decode:  505.07 MB + 3.86 MB for 503.62 MB (decode-only: K/V loaded evict-first).
+# A ratio is reported only for the workload it was measured on, and only while the
+# profiled sources are unchanged.
 NCU_TRAFFIC = {
-    "decode": {"ratio": 509.78 / 503.62,
-               "sources": ("k_decode.cu", "ptx.cuh", "pkv_internal.cuh"),
-               "sha256": "7c2605292215a862dfa08b2a2b9394b382cac3cfa45ccca34769b95350426b1a"},
+    "sources": ("k_decode.cu", "ptx.cuh", "pkv_internal.cuh"),
+    "sha256": "d1b62eb2871e6c2929772248bc4bf42ea2461bc1ab9c1393d176c679785d7c3c",
+    "decode": {"mixed": (19.4999e9 + 36.4e6) / 19409039536, "decode": (505.07e6 + 3.86e6) / 503617604},
 }
 
 
-def traffic_ratio(kernel: str):
+def traffic_ratio(kernel: str, workload: str):
     import hashlib
-    t = NCU_TRAFFIC.get(kernel)
-    if t is None:
+    t = NCU_TRAFFIC.get(kernel, {})
+    if workload not in t:
         return None
     h = hashlib.sha256()
-    for f in t["sources"]:
+    for f in NCU_TRAFFIC["sources"]:
         with open(os.path.join(ROOT, "paged_kv_cache_248_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
-    return t["ratio"] if h.hexdigest() == t["sha256"] else None
+    return t[workload] if h.hexdigest() == NCU_TRAFFIC["sha256"] else None
 
 
 def peaks():
@@ -582,7 +583,7 @@ def main():
     else:
         b = work_b["decode"] if dom.startswith(("decode", "cascade")) else work_b["total"]
         ach = b / (per_launch_ms / 1e3) / 1e9
-        ratio = traffic_ratio(dom)
+        ratio = traffic_ratio(dom, w.name)
         roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": ach / pk["hbm_gbs"], "traffic": ratio * b if ratio else None,
                 "algorithmic_bytes_per_launch": b}
