@@ -148,7 +148,7 @@ __device__ void plan_cascade(const PlanArgs& p) {
     const int pb = p.member_ok[k];
     if (pb > 0) {
       p.seq_prefix[i] = pb * kBlock;
-      p.member_ok[k] = 1;
+      p.member_ok[k] = static_cast<int32_t>(p.qsl[i]) + 1;  // the member's query row + 1
     } else if (csr_ok && i >= 0 && i < p.num_seqs && p.seq_entry[i] == k && p.seq_prefix[i] == 0) {
       p.seq_entry[i] = -1;  // claimed but not a member
     }
@@ -194,7 +194,7 @@ constexpr int kCasOnchipSeqs = 8192;
 constexpr int kCasOnchipMembers = 8192;
 constexpr int kCasOnchipGroups = 1024;
 constexpr int kCasOnchipBlocks = 512;  // longest prefix table compared in this pass
-__host__ __device__ constexpr int64_t cas_onchip_ints(int64_t n, int64_t m, int64_t g) { return 2 * n + 3 * m + 2 * g + 1; }
+__host__ __device__ constexpr int64_t cas_onchip_ints(int64_t n, int64_t m, int64_t g) { return 2 * n + 4 * m + 2 * g + 1; }
 __device__ void plan_cascade_onchip(const PlanArgs& p, int32_t* sm, int32_t*& s_prefix, int32_t*& s_entry) {
   __shared__ int s_csr_ok;
   constexpr int kChunk = 16;
@@ -206,7 +206,8 @@ __device__ void plan_cascade_onchip(const PlanArgs& p, int32_t* sm, int32_t*& s_
   int32_t* s_pb = s_prefix + n;    // [M]: the entry's prefix blocks if its lengths pass, else 0
   int32_t* s_req = s_pb + M;       // [M]: the entry's request
   int32_t* s_diff = s_req + M;     // [M]: some chunk of the table differs from the prefix
-  int32_t* s_start = s_diff + M;   // [G + 1]
+  int32_t* s_row = s_diff + M;     // [M]: the request's query row
+  int32_t* s_start = s_row + M;    // [G + 1]
   int32_t* s_blocks = s_start + G + 1;  // [G]
   for (int i = tid; i < n; i += nthr) s_entry[i] = -1;
   for (int k = tid; k < M; k += nthr) s_diff[k] = 0;
@@ -237,6 +238,7 @@ __device__ void plan_cascade_onchip(const PlanArgs& p, int32_t* sm, int32_t*& s_
       if (i_ok) {
         if (atomicCAS(&s_entry[i], -1, k) != -1) atomicExch(&s_entry[i], -2);  // a second claim: listed twice
         const int64_t q0 = __ldg(p.qsl + i), q1 = __ldg(p.qsl + i + 1), L = __ldg(p.seq_lens + i);
+        s_row[k] = static_cast<int32_t>(q0);
         if (pb_ok && q0 >= 0 && q1 == q0 + 1 && q1 <= p.num_tokens && L <= p.max_seq_len &&
             (L + kBlock - 1) / kBlock <= p.max_blocks && L > static_cast<int64_t>(pb) * kBlock)
           keep = pb;
@@ -275,7 +277,7 @@ __device__ void plan_cascade_onchip(const PlanArgs& p, int32_t* sm, int32_t*& s_
   __syncthreads();
   for (int k = tid; k < M; k += nthr) {
     const int i = csr_ok ? s_req[k] : -1;
-    p.member_ok[k] = (i >= 0 && s_entry[i] == k) ? 1 : 0;
+    p.member_ok[k] = (i >= 0 && s_entry[i] == k) ? s_row[k] + 1 : 0;  // the member's query row + 1
   }
   // cascade items per group: member tiles x kv heads x prefix key splits
   int carry = 0;

@@ -617,9 +617,11 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uin
     const bool row_out = rj < tnq && rg < P.group;  // a real (token, head) row
     __nv_bfloat16* orow = P.out + ((static_cast<int64_t>(info.t0) + j_row) * P.hq +
                                    static_cast<int64_t>(info.head) * P.group + rg) * 128;
-    // this row's member entry (cascade) and whether it is stored
+    // this row's member entry (cascade), the entry's query row + 1 (0: not a member) and
+    // whether the row is stored
     const int entry = tj0 + rj;
-    const bool cas_live = kCas && rj < tnq && P.member_ok[entry] != 0;
+    const int32_t mrow = (kCas && rj < tnq) ? P.member_ok[entry] : 0;
+    const bool cas_live = kCas && mrow != 0;
     if (kCas) {
       // gather the query row of (member, head) into the swizzled K-major Q tile once
       // the previous item's last S = Q K^T of this tile slot has read it
@@ -629,7 +631,7 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uin
       }
       uint4 qv[16];
       if (cas_live && rg < P.group) {
-        const int64_t t = P.qsl[P.cas_members[entry]];
+        const int64_t t = mrow - 1;
         const uint4* src = reinterpret_cast<const uint4*>(
             P.q + (t * P.hq + static_cast<int64_t>(info.head) * P.group + rg) * 128);
 #pragma unroll

@@ -172,7 +172,7 @@ struct Workspace {
   // shared-prefix (cascade) state; all null without prefix groups
   int32_t* seq_prefix;   // [num_seqs] prefix tokens attended by the cascade kernel (0: none)
   int32_t* seq_entry;    // [num_seqs] the request's member-list entry (-1: none)
-  int32_t* member_ok;    // [num_members] the entry passed the planner's checks
+  int32_t* member_ok;    // [num_members] the entry's query row + 1 if it passed the planner's checks, else 0
   int32_t* cas_prefix;   // [num_groups + 1] exclusive prefix of cascade work items
   float* cas_ml;         // [num_members * hkv * cas_np_max * GP * 2] prefix partial max and sum
   float* cas_o;          // [num_members * hkv * cas_np_max * GP * head_dim] prefix accumulators
