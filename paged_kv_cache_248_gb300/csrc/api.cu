@@ -101,6 +101,8 @@ size_t layout_workspace(void* base, int32_t num_seqs, int32_t hkv, int32_t group
     w.seq_entry = static_cast<int32_t*>(take(static_cast<size_t>(num_seqs) * sizeof(int32_t)));
     w.member_ok = static_cast<int32_t*>(take(nm * sizeof(int32_t)));
     w.cas_prefix = static_cast<int32_t*>(take((static_cast<size_t>(cas->num_groups) + 1) * sizeof(int32_t)));
+    w.grp_ok = static_cast<int32_t*>(take(static_cast<size_t>(cas->num_groups) * sizeof(int32_t)));
+    w.blk_mark = static_cast<int32_t*>(take(static_cast<size_t>(cas->pool_blocks) * sizeof(int32_t)));
     w.cas_ml = static_cast<float*>(take(slots * group * 2 * sizeof(float)));
     w.cas_o = static_cast<float*>(take(slots * group * head_dim * sizeof(float)));
   }
@@ -374,6 +376,7 @@ int attention_impl(const void* q, const void* k_new, const void* v_new, const vo
                           cascade_splits(static_cast<int64_t>(cas.max_blocks) * kBlock);
     if (slots * gp >= (int64_t(1) << 31)) return PKV_ERR_UNSUPPORTED;
   }
+  cas.pool_blocks = cache->num_blocks;
   const CascadeArgs* casp = cas.num_groups > 0 ? &cas : nullptr;
   const int64_t max_pre_units = max_prefill_units(num_tokens, num_seqs, gp);
   const size_t need =
@@ -407,6 +410,8 @@ int attention_impl(const void* q, const void* k_new, const void* v_new, const vo
     plan.write_ctas = static_cast<int32_t>(want < 2 * ctx->num_sms ? want : 2 * ctx->num_sms);
   }
   const int cas_tpi = casp ? cascade_tiles_per_item(cas.num_members, hkv, gp, cas.max_blocks, ctx->num_sms) : 1;
+  // with few groups the cascade kernel finds its own items and runs beside the planner
+  const int cas_concurrent = casp && cas.num_groups <= kCasConcurrentGroups ? 1 : 0;
   if (casp) {
     plan.cas = cas;
     plan.cas_rows = cas_tpi * (kTileKeys / gp);
@@ -414,11 +419,17 @@ int attention_impl(const void* q, const void* k_new, const void* v_new, const vo
     plan.seq_entry = ws.seq_entry;
     plan.member_ok = ws.member_ok;
     plan.cas_prefix = ws.cas_prefix;
+    plan.grp_ok = ws.grp_ok;
+    plan.blk_mark = ws.blk_mark;
+    plan.num_blocks = cache->num_blocks;
+    plan.cas_concurrent = cas_concurrent;
+    // a fresh mark value per call (bit 30 set; the multiplier spreads consecutive calls)
+    plan.epoch = static_cast<int32_t>(0x40000000u | ((++ctx->calls * 2654435761u) & 0x3FFFFFFFu));
   }
   st = launch_plan(plan, s);
   if (st) return st;
   if (casp) {
-    st = launch_cascade_tc(a, cas, ws, ctx->num_sms, cas_tpi, ctx->err, s);
+    st = launch_cascade_tc(a, cas, ws, ctx->num_sms, cas_tpi, cas_concurrent, ctx->err, s);
     if (st) return st;
   }
   st = launch_decode_tc(a, ws, ctx->num_sms, ctx->err, s);

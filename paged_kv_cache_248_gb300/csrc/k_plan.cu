@@ -106,7 +106,8 @@ __device__ void plan_cascade(const PlanArgs& p) {
     const int i = g.members[k];
     int pb_ok = 0;
     if (csr_ok && i >= 0 && i < p.num_seqs && p.seq_entry[i] == k && p.seq_prefix[i] == 0) {
-      const int pb = g.blocks[group_of(k)];
+      const int gk = group_of(k);
+      const int pb = p.grp_ok[gk] ? g.blocks[gk] : 0;
       const int64_t q0 = p.qsl[i], q1 = p.qsl[i + 1], L = p.seq_lens[i];
       if (pb >= 1 && pb <= g.max_blocks && q0 >= 0 && q1 == q0 + 1 && q1 <= p.num_tokens && L <= p.max_seq_len &&
           (L + kBlock - 1) / kBlock <= p.max_blocks && L > static_cast<int64_t>(pb) * kBlock)
@@ -181,6 +182,63 @@ __device__ void plan_cascade(const PlanArgs& p) {
   __syncthreads();
 }
 
+// Which groups may admit members (grp_ok).  A group whose prefix names a block outside
+// the pool admits nobody: its members attend their whole context in the decode kernel,
+// which reports the bad id for them.  When the cascade kernel runs beside this launch
+// (cas_concurrent) it reads the prefix blocks while the writer CTAs may still be
+// writing this call's new tokens, so then a new token that lands in any group's prefix
+// block -- or a query_start_loc that decreases, which the writers would map
+// differently -- admits nobody anywhere (a correct, slower fallback for inputs a
+// serving loop does not produce: shared prefix blocks are full and never written).
+// Every group's prefix blocks are marked with the call's epoch in the workspace, then
+// each request's warp checks the blocks its new tokens go to, as the writers compute
+// them.  Called by the whole block; returns synchronised.
+__device__ void prefix_block_checks(const PlanArgs& p) {
+  __shared__ int s_conflict;
+  const CascadeArgs& g = p.cas;
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const bool marks = p.cas_concurrent && p.k_new != nullptr;
+  if (tid == 0) s_conflict = 0;
+  for (int gi = tid; gi < g.num_groups; gi += nthr) p.grp_ok[gi] = 1;
+  __syncthreads();
+  const int64_t n_ids = static_cast<int64_t>(g.num_groups) * g.max_blocks;
+  for (int64_t x = tid; x < n_ids; x += nthr) {
+    const int gi = static_cast<int>(x / g.max_blocks), j = static_cast<int>(x % g.max_blocks);
+    if (j >= __ldg(g.blocks + gi)) continue;  // (a length outside [1, max_blocks] admits nobody anyway)
+    const int32_t b = __ldg(g.tables + x);
+    if (b < 0 || b >= p.num_blocks) p.grp_ok[gi] = 0;
+    else if (marks) p.blk_mark[b] = p.epoch;
+  }
+  __syncthreads();
+  if (marks) {
+    // a thread per request: its loads overlap those of the other requests
+    for (int i = tid; i < p.num_seqs; i += nthr) {
+      const int64_t q0 = __ldg(p.qsl + i), q1 = __ldg(p.qsl + i + 1), L = __ldg(p.seq_lens + i);
+      if (q1 < q0) {
+        s_conflict = 1;
+        continue;
+      }
+      // new tokens at positions L - (q1 - q0) .. L - 1, those the writers store: pos >= 0
+      // and pos / 16 < max_blocks
+      const int64_t first = L - (q1 - q0) > 0 ? L - (q1 - q0) : 0, last = L - 1;
+      if (q1 == q0 || last < first) continue;
+      const int64_t lb1 = last / kBlock < p.max_blocks - 1 ? last / kBlock : p.max_blocks - 1;
+      const int32_t* row = p.bt + static_cast<int64_t>(i) * p.max_blocks;
+      bool hit = false;
+#pragma unroll 4
+      for (int64_t lb = first / kBlock; lb <= lb1; ++lb) {
+        const int32_t b = __ldg(row + lb);
+        hit |= b >= 0 && b < p.num_blocks && p.blk_mark[b] == p.epoch;
+      }
+      if (hit) s_conflict = 1;
+    }
+    __syncthreads();
+    if (s_conflict)
+      for (int gi = tid; gi < g.num_groups; gi += nthr) p.grp_ok[gi] = 0;
+  }
+  __syncthreads();
+}
+
 // The same membership decisions with every intermediate state in shared memory (`sm`,
 // the launch's dynamic buffer), for batches within the limits below.  One pass over
 // (entry, 16-id chunk) pairs makes every check at once -- the chunk-0 thread of an
@@ -212,7 +270,7 @@ __device__ void plan_cascade_onchip(const PlanArgs& p, int32_t* sm, int32_t*& s_
   for (int i = tid; i < n; i += nthr) s_entry[i] = -1;
   for (int k = tid; k < M; k += nthr) s_diff[k] = 0;
   for (int k = tid; k <= G; k += nthr) s_start[k] = __ldg(g.start + k);
-  for (int k = tid; k < G; k += nthr) s_blocks[k] = __ldg(g.blocks + k);
+  for (int k = tid; k < G; k += nthr) s_blocks[k] = p.grp_ok[k] ? __ldg(g.blocks + k) : 0;  // 0: admits nobody
   if (tid == 0) s_csr_ok = 1;
   __syncthreads();
   if (tid == 0 && !(s_start[0] == 0 && s_start[G] == M)) s_csr_ok = 0;
@@ -577,6 +635,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs p) {
   const int32_t* seq_pre = p.seq_prefix;  // each request's prefix tokens and member entry
   const int32_t* seq_ent = p.seq_entry;
   if (cascade) {
+    prefix_block_checks(p);
     if (p.cas_onchip) {
       int32_t *sp = nullptr, *se = nullptr;
       plan_cascade_onchip(p, plan_smem, sp, se);

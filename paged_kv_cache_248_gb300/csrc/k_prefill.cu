@@ -115,13 +115,12 @@ struct PrefillParams {
   const int32_t* cas_blocks;
   const int32_t* cas_start;
   const int32_t* cas_members;
-  const int32_t* cas_prefix;
-  const int32_t* member_ok;
+  const int32_t* cas_prefix;  // the planner's item prefix (used without cas_concurrent)
   float* cas_o;
   float* cas_ml;
-  int32_t* unit_bad;
   int32_t cas_max_blocks, cas_groups, cas_np_max;
-  int32_t cas_tiles;  // query tiles per cascade item: 2, or 1 (tile 1 of every item absent)
+  int32_t cas_tiles;       // query tiles per cascade item: 2, or 1 (tile 1 of every item absent)
+  int32_t cas_concurrent;  // items from the hint alone, beside the planning launch (groups <= 32)
 };
 
 // Three-input maximum / minimum (one instruction on sm_100 and later).
@@ -284,26 +283,27 @@ __device__ PItem make_item(const PrefillParams& P, int idx, int total) {
   return r;
 }
 
-// A cascade item: group g by its item prefix, then (member tile pair, kv head, key split).
-__device__ PItem make_cas_item(const PrefillParams& P, int idx, int total) {
+// Cascade items of one group: its member entries in tiles of cas_tiles * rows_q (the
+// planner counts them the same way) x kv heads x key splits of the prefix.
+__device__ __forceinline__ int cas_group_items(const PrefillParams& P, int e0, int e1, int pb) {
+  if (pb < 1 || pb > P.cas_max_blocks || e1 <= e0) return 0;
+  const int rows = P.cas_tiles * P.rows_q;
+  return (e1 - e0 + rows - 1) / rows * P.hkv * static_cast<int>(cascade_splits(int64_t(pb) * kBlock));
+}
+
+// A cascade item: item `local` of group g (entries e0 .. e1 - 1, pb prefix blocks), as
+// (member tile pair, kv head, key split).
+__device__ PItem make_cas_item(const PrefillParams& P, int idx, int g, int local, int e0, int e1, int pb) {
   PItem r{};
   r.qt[0] = r.qt[1] = -1;
-  if (idx >= total) {
+  if (g < 0) {
     r.idx = -1;
     return r;
   }
-  int lo = 0, hi = P.cas_groups - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (P.cas_prefix[mid] <= idx) lo = mid; else hi = mid - 1;
-  }
   r.idx = idx;
-  r.seq = lo;
-  const int pb = P.cas_blocks[lo];
-  const int e0 = P.cas_start[lo], e1 = P.cas_start[lo + 1];
-  if (pb < 1 || pb > P.cas_max_blocks || e1 <= e0) return r;  // inconsistent plan: invalid item
+  r.seq = g;
+  if (pb < 1 || pb > P.cas_max_blocks || e1 <= e0 || local < 0) return r;  // inconsistent: invalid item
   const int np = static_cast<int>(cascade_splits(int64_t(pb) * kBlock));
-  const int local = idx - P.cas_prefix[lo];
   r.split = local % np;
   r.head = (local / np) % P.hkv;
   const int pq = local / np / P.hkv;  // the item's tile group of member entries
@@ -331,7 +331,28 @@ template <bool kCas>
 __device__ void producer_warp(const PrefillParams& P, const CUtensorMap* qmap, const CUtensorMap* kmap,
                               const CUtensorMap* vmap, Ctl& c, uint8_t* qbuf, uint8_t* kbuf, uint8_t* vbuf) {
   const int lane = threadIdx.x & 31;
-  const int total = kCas ? P.cas_prefix[P.cas_groups] : P.pre_prefix[P.num_seqs];
+  // cascade items beside the planner: lane g holds group g's entries, prefix length,
+  // item count and the exclusive prefix of the counts
+  int ce0 = 0, ce1 = 0, cpb = 0, ccnt = 0, cpfx = 0;
+  int total;
+  if (kCas && P.cas_concurrent) {
+    if (lane < P.cas_groups) {
+      ce0 = __ldg(P.cas_start + lane);
+      ce1 = __ldg(P.cas_start + lane + 1);
+      cpb = __ldg(P.cas_blocks + lane);
+      ccnt = cas_group_items(P, ce0, ce1, cpb);
+    }
+    int incl = ccnt;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += y;
+    }
+    cpfx = incl - ccnt;
+    total = __shfl_sync(0xffffffffu, incl, 31);
+  } else {
+    total = kCas ? P.cas_prefix[P.cas_groups] : P.pre_prefix[P.num_seqs];
+  }
   volatile int* abort_flag = &c.abort_flag;
   uint32_t it = 0, tk = 0, tv = 0;  // items; K and V tiles issued
   uint32_t qc[2] = {0, 0};          // Q tiles loaded per tile slot
@@ -342,10 +363,42 @@ __device__ void producer_warp(const PrefillParams& P, const CUtensorMap* qmap, c
       ok = false;
       break;
     }
-    if (lane == 0) {
+    if (kCas) {
+      // cascade items are alike, so CTA b takes items b, b + grid, b + 2 grid, ...; the
+      // item's group is the last one whose first item is not past it
+      const int idx = static_cast<int>(blockIdx.x + it * gridDim.x);
+      int g = -1, local = 0, e0 = 0, e1 = 0, pb = 0;
+      if (idx < total) {
+        if (P.cas_concurrent) {
+          const unsigned m = __ballot_sync(0xffffffffu, ccnt > 0 && cpfx <= idx);
+          g = m ? 31 - __clz(m) : 0;
+          local = idx - __shfl_sync(0xffffffffu, cpfx, g);
+          e0 = __shfl_sync(0xffffffffu, ce0, g);
+          e1 = __shfl_sync(0xffffffffu, ce1, g);
+          pb = __shfl_sync(0xffffffffu, cpb, g);
+          if (!m) local = -1;
+        } else if (lane == 0) {
+          int lo = 0, hi = P.cas_groups - 1;
+          while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (P.cas_prefix[mid] <= idx) lo = mid; else hi = mid - 1;
+          }
+          g = lo;
+          local = idx - P.cas_prefix[lo];
+          e0 = P.cas_start[lo];
+          e1 = P.cas_start[lo + 1];
+          pb = P.cas_blocks[lo];
+        }
+      }
+      if (lane == 0) {
+        c.ring[slot] = make_cas_item(P, idx, g, local, e0, e1, pb);
+        c.bad[slot] = 0;
+        mbar_arrive(&c.item_full[slot]);
+      }
+    } else if (lane == 0) {
       // every CTA's first item is its own index; later ones come off the queue after those
       const int idx = it == 0 ? static_cast<int>(blockIdx.x) : static_cast<int>(gridDim.x) + atomicAdd(P.queue, 1);
-      c.ring[slot] = kCas ? make_cas_item(P, idx, total) : make_item(P, idx, total);
+      c.ring[slot] = make_item(P, idx, total);
       c.bad[slot] = 0;
       mbar_arrive(&c.item_full[slot]);
     }
@@ -617,11 +670,18 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uin
     const bool row_out = rj < tnq && rg < P.group;  // a real (token, head) row
     __nv_bfloat16* orow = P.out + ((static_cast<int64_t>(info.t0) + j_row) * P.hq +
                                    static_cast<int64_t>(info.head) * P.group + rg) * 128;
-    // this row's member entry (cascade), the entry's query row + 1 (0: not a member) and
-    // whether the row is stored
+    // this row's member entry (cascade) and its query row: a listed request with one new
+    // token (the planner decides later which entries the decode kernel folds in)
     const int entry = tj0 + rj;
-    const int32_t mrow = (kCas && rj < tnq) ? P.member_ok[entry] : 0;
-    const bool cas_live = kCas && mrow != 0;
+    int64_t crow = -1;
+    if (kCas && rj < tnq) {
+      const int i = __ldg(P.cas_members + entry);
+      if (i >= 0 && i < P.num_seqs) {
+        const int64_t q0 = __ldg(P.qsl + i), q1 = __ldg(P.qsl + i + 1);
+        if (q0 >= 0 && q1 == q0 + 1 && q1 <= P.num_tokens) crow = q0;
+      }
+    }
+    const bool cas_live = kCas && crow >= 0;
     if (kCas) {
       // gather the query row of (member, head) into the swizzled K-major Q tile once
       // the previous item's last S = Q K^T of this tile slot has read it
@@ -631,7 +691,7 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uin
       }
       uint4 qv[16];
       if (cas_live && rg < P.group) {
-        const int64_t t = mrow - 1;
+        const int64_t t = crow;
         const uint4* src = reinterpret_cast<const uint4*>(
             P.q + (t * P.hq + static_cast<int64_t>(info.head) * P.group + rg) * 128);
 #pragma unroll
@@ -772,10 +832,10 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uin
             st_global_v8(dst + 32 * h + 8 * q, w8);
           }
       }
+      // (a prefix with a bad block id admits nobody: the planner checks the ids itself)
       if (cas_live) {
         P.cas_ml[(cslot * P.gp + rg) * 2] = m_ref;
         P.cas_ml[(cslot * P.gp + rg) * 2 + 1] = l_sum;
-        if (bad && rg == 0) P.unit_bad[static_cast<int64_t>(P.cas_members[entry]) * P.hkv + info.head] = 1;
       }
       continue;
     }
@@ -875,7 +935,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = c.tmem_base;
-  grid_dep_wait();  // the plan, the new tokens and the earlier kernels of this call
+  // the plan, the new tokens and the earlier kernels of this call; a cascade beside the
+  // planner reads nothing those write (the planner admits no member of a group whose
+  // prefix a new token lands in) and waits for them only before it exits
+  const bool beside = kCas && P.cas_concurrent;
+  if (!beside) grid_dep_wait();
   grid_dep_launch();
   if (warp == 0) producer_warp<kCas>(P, &qmap, &kmap, &vmap, c, qbuf, kbuf, vbuf);
   else if (warp == 1) mma_warp(P, c, qbuf, kbuf, vbuf, tmem);
@@ -887,6 +951,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     tmem_dealloc(tmem, kTmemCols);
     tmem_relinquish();
   }
+  // the grid ends after the planning launch: the kernels after it wait on this one only
+  if (beside && threadIdx.x == 0) grid_dep_wait();
 }
 
 }  // namespace
@@ -936,8 +1002,7 @@ int launch_prefill_tc(const AttnArgs& a, const Workspace& ws, int num_sms, uint3
 }
 
 int launch_cascade_tc(const AttnArgs& a, const CascadeArgs& cas, const Workspace& ws, int num_sms, int tiles_per_item,
-                      uint32_t* err,
-                      cudaStream_t s) {
+                      int concurrent, uint32_t* err, cudaStream_t s) {
   const int hkv = a.cache.num_kv_heads;
   const int group = a.num_q_heads / hkv;
   if (group > 16 || a.cache.head_dim != 128 || a.cache.dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
@@ -972,10 +1037,9 @@ int launch_cascade_tc(const AttnArgs& a, const CascadeArgs& cas, const Workspace
   p.cas_start = cas.start;
   p.cas_members = cas.members;
   p.cas_prefix = ws.cas_prefix;
-  p.member_ok = ws.member_ok;
   p.cas_o = ws.cas_o;
   p.cas_ml = ws.cas_ml;
-  p.unit_bad = ws.unit_bad;
+  p.cas_concurrent = concurrent != 0 && cas.num_groups <= kCasConcurrentGroups ? 1 : 0;
   p.cas_max_blocks = cas.max_blocks;
   p.cas_groups = cas.num_groups;
   p.cas_np_max = ws.cas_np_max;
@@ -984,8 +1048,14 @@ int launch_cascade_tc(const AttnArgs& a, const CascadeArgs& cas, const Workspace
   st = set_smem_once(reinterpret_cast<const void*>(prefill_kernel<true>), kSmemBytes, &smem_set);
   if (st) return st;
   TraceScope trace(kTraceCascade, s);
+  // at most ceil(members / rows) + groups member tiles: CTAs past the items would only
+  // hold an SM until the planner ends
+  const int64_t tile_rows = static_cast<int64_t>(tiles_per_item) * p.rows_q;
+  const int64_t items = ((cas.num_members + tile_rows - 1) / tile_rows + cas.num_groups) * hkv *
+                        cascade_splits(static_cast<int64_t>(cas.max_blocks) * kBlock);
+  const int grid = static_cast<int>(items < num_sms ? items : num_sms);
   // the Q tensor map is unused in this mode (Q rows are gathered); K's stands in
-  return cuda_status(launch_k(prefill_kernel<true>, dim3(num_sms), dim3(kThreads), kSmemBytes, s, km, km, vm, p));
+  return cuda_status(launch_k(prefill_kernel<true>, dim3(grid), dim3(kThreads), kSmemBytes, s, km, km, vm, p));
 }
 
 }  // namespace pkv

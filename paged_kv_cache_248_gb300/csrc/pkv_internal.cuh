@@ -109,6 +109,7 @@ struct DeviceCtx {
   uint32_t* err = nullptr;     // device error word
   void* ws = nullptr;          // workspace
   size_t ws_bytes = 0;
+  uint32_t calls = 0;          // calls with prefix groups so far: seeds each call's block-mark epoch
 };
 
 // Per-device context (created on first use on the current device).
@@ -172,8 +173,11 @@ struct Workspace {
   // shared-prefix (cascade) state; all null without prefix groups
   int32_t* seq_prefix;   // [num_seqs] prefix tokens attended by the cascade kernel (0: none)
   int32_t* seq_entry;    // [num_seqs] the request's member-list entry (-1: none)
-  int32_t* member_ok;    // [num_members] the entry's query row + 1 if it passed the planner's checks, else 0
+  int32_t* member_ok;    // [num_members] planner scratch (the global membership checks)
   int32_t* cas_prefix;   // [num_groups + 1] exclusive prefix of cascade work items
+  int32_t* grp_ok;       // [num_groups] the group may admit members: its prefix ids are valid blocks
+                         // that no new token of the call is written into
+  int32_t* blk_mark;     // [pool blocks] a block is in some group's prefix iff it holds the call's epoch
   float* cas_ml;         // [num_members * hkv * cas_np_max * GP * 2] prefix partial max and sum
   float* cas_o;          // [num_members * hkv * cas_np_max * GP * head_dim] prefix accumulators
   int32_t cas_np_max;    // key splits of the longest prefix
@@ -188,6 +192,7 @@ struct CascadeArgs {
   const int32_t* members;  // [num_members] request indices
   int32_t num_groups;
   int32_t num_members;
+  int64_t pool_blocks = 0;  // blocks of the K/V pool (sizes the workspace's block marks)
 };
 
 // Computes the layout at `base` (nullptr: only the size) and returns the bytes needed;
@@ -234,6 +239,12 @@ struct PlanArgs {
   int32_t* seq_entry = nullptr;
   int32_t* member_ok = nullptr;
   int32_t* cas_prefix = nullptr;
+  int32_t* grp_ok = nullptr;
+  int32_t* blk_mark = nullptr;
+  int64_t num_blocks = 0;
+  int32_t epoch = 0;              // this call's block-mark value (bit 30 set, so stale small integers never match)
+  int32_t cas_concurrent = 0;     // the cascade kernel runs beside this launch and reads prefix blocks while the
+                                  //   writers write: a group is admitted only if no new token lands in its prefix
   // new tokens written by the same launch (k_new null: none): slot mapping and K/V scatter
   const uint4* k_new = nullptr;
   const uint4* v_new = nullptr;
@@ -260,8 +271,12 @@ inline int cascade_tiles_per_item(int64_t num_members, int hkv, int gp, int64_t 
   const int64_t pairs = (num_members + 2 * rows - 1) / (2 * rows) * hkv * cascade_splits(max_prefix_blocks * kBlock);
   return pairs >= num_sms ? 2 : 1;
 }
-int launch_cascade_tc(const AttnArgs& a, const CascadeArgs& cas, const Workspace& ws, int num_sms, int tiles_per_item, uint32_t* err,
-                      cudaStream_t s);
+// With `concurrent` (at most kCasConcurrentGroups groups) the kernel derives its items
+// from the hint alone and waits for the planning launch only before it exits, so the
+// two run side by side; otherwise it starts once the planner's item prefix is written.
+constexpr int kCasConcurrentGroups = 32;
+int launch_cascade_tc(const AttnArgs& a, const CascadeArgs& cas, const Workspace& ws, int num_sms, int tiles_per_item,
+                      int concurrent, uint32_t* err, cudaStream_t s);
 int launch_prefill_tc(const AttnArgs& a, const Workspace& ws, int num_sms, uint32_t* err, cudaStream_t s);
 int encode_tensor_map_3d(CUtensorMap* map, const void* base, const uint64_t dims[3], const uint64_t strides[2],
                          const uint32_t box[3]);

@@ -73,17 +73,61 @@ def test_step_equals_the_separate_calls_and_the_oracle(pkv, seed, group, hkv, dt
     compare(fus[0], ref, dtype, w.name)
 
 
+def hint_tensors(hints):
+    return tuple(dev(hints[k]) for k in ("prefix_block_tables", "prefix_num_blocks", "member_start", "member_seqs"))
+
+
 def test_step_with_prefix_groups(pkv):
-    w, hints = wl.shared_prefix_case(26, prefix_blocks=(24, 40), members=(20, 9), bystanders=6)
+    # no new token lands in a prefix block: the fused step admits the same members as
+    # the separate calls and gives the same bits
+    w, hints = wl.shared_prefix_case(26, prefix_blocks=(24, 40), members=(20, 9), bystanders=6, bad_hints=False)
     t_cpu = w.make_tensors("cpu")
     t = {k: v.cuda() for k, v in t_cpu.items()}
-    groups = tuple(dev(hints[k]) for k in ("prefix_block_tables", "prefix_num_blocks", "member_start",
-                                            "member_seqs"))
-    sep, fus = both_ways(pkv, w, t, groups)
+    sep, fus = both_ways(pkv, w, t, hint_tensors(hints))
     assert sep[4] == 0
     assert_same(sep, fus)
     ref, _, _, _ = oracle_step(w, t_cpu)
     compare(fus[0], ref, "bf16", w.name)
+
+
+def caches_same_outputs_match(sep, fus, ref, name):
+    assert sep[4] == 0 and fus[4] == 0
+    for x, y, what in zip(sep[1:4], fus[1:4], ("slots", "k_cache", "v_cache")):
+        assert torch.equal(x, y), what
+    compare(sep[0], ref, "bf16", name + " (separate calls)")
+    compare(fus[0], ref, "bf16", name + " (fused step)")
+
+
+def test_step_with_a_new_token_in_a_prefix_block(pkv):
+    # the bad hints list a decode whose context ends inside prefix 0, so its new token
+    # is written into one of the shared prefix blocks.  The fused step's cascade reads
+    # the prefix while the tokens are being written, so the step then lets every member
+    # attend its whole context in the decode kernel: the caches and slots are the
+    # separate calls' bit for bit, and both outputs match the oracle
+    w, hints = wl.shared_prefix_case(26, prefix_blocks=(24, 40), members=(20, 9), bystanders=6)
+    t_cpu = w.make_tensors("cpu")
+    t = {k: v.cuda() for k, v in t_cpu.items()}
+    inside = [i for i in range(w.num_seqs) if w.q_lens[i] == 1 and w.seq_lens[i] < 24 * 16
+              and w.block_tables[i, 0] == hints["prefix_block_tables"][0, 0]]
+    assert inside, "the case has a decode that writes into prefix 0"
+    sep, fus = both_ways(pkv, w, t, hint_tensors(hints))
+    ref, _, _, _ = oracle_step(w, t_cpu)
+    caches_same_outputs_match(sep, fus, ref, w.name)
+
+
+def test_step_with_a_bystander_writing_into_a_prefix(pkv):
+    # a decode that is no member has its newest block pointed at a block of the
+    # shared prefix: its new token overwrites a row every member attends
+    w, hints = wl.shared_prefix_case(29, prefix_blocks=(30,), members=(25,), bystanders=6, bad_hints=False)
+    members = set(hints["member_seqs"].tolist())
+    i = next(i for i in range(w.num_seqs) if i not in members and w.q_lens[i] == 1)
+    last = (int(w.seq_lens[i]) - 1) // 16
+    w.block_tables[i, last] = hints["prefix_block_tables"][0, 7]
+    t_cpu = w.make_tensors("cpu")
+    t = {k: v.cuda() for k, v in t_cpu.items()}
+    sep, fus = both_ways(pkv, w, t, hint_tensors(hints))
+    ref, _, _, _ = oracle_step(w, t_cpu)
+    caches_same_outputs_match(sep, fus, ref, w.name)
 
 
 def test_step_errors_match_the_separate_calls(pkv):
