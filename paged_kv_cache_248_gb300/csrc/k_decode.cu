@@ -15,14 +15,18 @@
 // after on the same stream, combines the partials in split order (log-sum-exp
 // merge), so results never depend on scheduling.
 //
-// Per CTA (224 threads):
+// Per CTA (256 threads):
 //   warp 6     scheduler: takes items off the queue ahead of use and resolves the
 //              request, its lengths, its query row and the item's block ids (checked
 //              against the pool) into a ring in shared memory.
-//   warp 0     producer: only TMA -- the G query rows (one 3-D box per half) and,
-//              per tile, 4 boxes per block (K and V, two 64-column halves each,
-//              128-byte swizzle) straight from the block's physical location -- the
+//   warp 0     K producer: only TMA -- the G query rows (one 3-D box per half) and,
+//              per tile, 2 boxes per block (two 64-column halves of K, 128-byte
+//              swizzle) straight from the block's physical location -- the
 //              block-table gather.  kStages tiles in flight.
+//   warp 7     V producer: the same for V, into the V half of each stage.  A stage's
+//              K is free once its S^T is done and its V once its P V is, so the K
+//              of the next tiles (and of the next item) is requested a softmax
+//              earlier than if the two waited for each other.
 //   warp 1     MMA issuer (one lane): S^T = K Q^T with the 128 keys on M and the
 //              query-head group on N = 16, then O^T = V^T P^T with head_dim on M,
 //              both accumulating fp32 in TMEM.  V^T is read MN-major from the same
@@ -40,7 +44,7 @@
 namespace pkv {
 namespace {
 
-constexpr int kThreads = 224;                 // 7 warps, see the role list above
+constexpr int kThreads = 256;                 // 8 warps, see the role list above
 constexpr int kStages = 3;
 constexpr int kHalfBytes = 16384;             // one 64-column half of a 128-key tile
 constexpr int kKBytes = 2 * kHalfBytes;       // K tile: [2 halves][128 keys][128 B]
@@ -64,7 +68,7 @@ struct alignas(16) ItemInfo {
 };
 
 struct Ctl {
-  uint64_t full[kStages], empty[kStages];
+  uint64_t kfull[kStages], kempty[kStages], vfull[kStages], vempty[kStages];
   uint64_t s_full[2], s_free[2], p_full[2], p_free[2], o_full[2], o_free[2];
   uint64_t q_full[2], q_free[2];
   uint64_t item_full[kRing], item_empty[kRing];
@@ -323,9 +327,11 @@ __device__ void scheduler_warp(const DecodeParams& P, Ctl& c) {
 }
 
 // ------------------------------------------------------------------ producer warp
-// Only mbarrier waits and TMA issues: the G query rows of the item (one 3-D box per
-// 64-column half) and, per 128-key tile, four 16 x 64 boxes per block taken straight
-// from the block's physical location (the block-table gather).
+// Only mbarrier waits and TMA issues.  The K producer (kV false): the G query rows of
+// the item (one 3-D box per 64-column half) and, per 128-key tile, two 16 x 64 boxes of
+// K per block taken straight from the block's physical location (the block-table
+// gather).  The V producer: the same boxes of V.  Each walks the item ring on its own.
+template <bool kV>
 __device__ void producer_warp(const DecodeParams& P, const CUtensorMap* qmap, const CUtensorMap* kmap,
                               const CUtensorMap* vmap, Ctl& c, uint8_t* stages, uint8_t* qbuf) {
   const int lane = threadIdx.x & 31;
@@ -345,47 +351,47 @@ __device__ void producer_warp(const DecodeParams& P, const CUtensorMap* qmap, co
     ++it;
     if (info.idx < 0) break;
     if (info.valid) {
-      const int qb = qc & 1;
-      if (!mbar_wait(&c.q_free[qb], ((qc >> 1) & 1) ^ 1, abort_flag)) {
-        ok = false;
-        break;
+      if (!kV) {
+        const int qb = qc & 1;
+        if (!mbar_wait(&c.q_free[qb], ((qc >> 1) & 1) ^ 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&c.q_full[qb], 2u * static_cast<uint32_t>(P.gp) * 128u);
+          const int32_t y = info.head * P.group;
+          tma_load_3d(qbuf + qb * kQBytes, qmap, &c.q_full[qb], 0, y, info.trow, pol_q);
+          tma_load_3d(qbuf + qb * kQBytes + 2048, qmap, &c.q_full[qb], 64, y, info.trow, pol_q);
+        }
+        ++qc;
       }
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&c.q_full[qb], 2u * static_cast<uint32_t>(P.gp) * 128u);
-        const int32_t y = info.head * P.group;
-        tma_load_3d(qbuf + qb * kQBytes, qmap, &c.q_full[qb], 0, y, info.trow, pol_q);
-        tma_load_3d(qbuf + qb * kQBytes + 2048, qmap, &c.q_full[qb], 64, y, info.trow, pol_q);
-      }
-      ++qc;
       const int nt = (info.key_end - info.key_start + kTileKeys - 1) / kTileKeys;
       for (int j = 0; j < nt; ++j) {
         const int st = tc % kStages;
-        if (!mbar_wait(&c.empty[st], ((tc / kStages) & 1) ^ 1, abort_flag)) {
+        if (!mbar_wait(kV ? &c.vempty[st] : &c.kempty[st], ((tc / kStages) & 1) ^ 1, abort_flag)) {
           ok = false;
           break;
         }
         const int t0 = info.key_start + j * kTileKeys;
         const int nblk = min(kBlocksPerTile, (info.key_end - t0 + kBlock - 1) / kBlock);
         const int id = lane < nblk ? c.ids[slot][j * kBlocksPerTile + lane] : 0;
-        if (lane == 0) mbar_arrive_expect_tx(&c.full[st], static_cast<uint32_t>(nblk) * 8192u);
+        uint64_t* bar = kV ? &c.vfull[st] : &c.kfull[st];
+        const CUtensorMap* map = kV ? vmap : kmap;
+        if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nblk) * 4096u);
         __syncwarp();
         if (lane < nblk) {
-          uint8_t* s = stages + st * kStageBytes + lane * 2048;
+          uint8_t* s = stages + st * kStageBytes + (kV ? kKBytes : 0) + lane * 2048;
           const int32_t row = (id * P.hkv + info.head) * kBlock;
           if (kv_ef) {  // each tile is read once: let the stream give way to code and tables in L2
-            tma_load_2d(s, kmap, &c.full[st], 0, row, pol_kv);
-            tma_load_2d(s + kHalfBytes, kmap, &c.full[st], 64, row, pol_kv);
-            tma_load_2d(s + kKBytes, vmap, &c.full[st], 0, row, pol_kv);
-            tma_load_2d(s + kKBytes + kHalfBytes, vmap, &c.full[st], 64, row, pol_kv);
+            tma_load_2d(s, map, bar, 0, row, pol_kv);
+            tma_load_2d(s + kHalfBytes, map, bar, 64, row, pol_kv);
           } else {
-            tma_load_2d(s, kmap, &c.full[st], 0, row);
-            tma_load_2d(s + kHalfBytes, kmap, &c.full[st], 64, row);
-            tma_load_2d(s + kKBytes, vmap, &c.full[st], 0, row);
-            tma_load_2d(s + kKBytes + kHalfBytes, vmap, &c.full[st], 64, row);
+            tma_load_2d(s, map, bar, 0, row);
+            tma_load_2d(s + kHalfBytes, map, bar, 64, row);
           }
         }
         ++tc;
-        if (lane == 0) *reinterpret_cast<volatile uint32_t*>(&c.issued_tiles) = tc;
+        if (!kV && lane == 0) *reinterpret_cast<volatile uint32_t*>(&c.issued_tiles) = tc;
       }
       if (!ok) break;
     }
@@ -396,7 +402,8 @@ __device__ void producer_warp(const DecodeParams& P, const CUtensorMap* qmap, co
   if (*abort_flag) {
     // let copies already issued land before the CTA's shared memory goes away
     const uint32_t first = tc > static_cast<uint32_t>(kStages) ? tc - kStages : 0;
-    for (uint32_t cnt = first; cnt < tc; ++cnt) mbar_wait(&c.full[cnt % kStages], (cnt / kStages) & 1, nullptr);
+    for (uint32_t cnt = first; cnt < tc; ++cnt)
+      mbar_wait(kV ? &c.vfull[cnt % kStages] : &c.kfull[cnt % kStages], (cnt / kStages) & 1, nullptr);
     if (qc > 0) mbar_wait(&c.q_full[(qc - 1) & 1], ((qc - 1) >> 1) & 1, nullptr);
   }
 }
@@ -443,7 +450,7 @@ __device__ void mma_warp(const DecodeParams& P, Ctl& c, uint8_t* stages, uint8_t
           if (ns < nt) {
             const uint32_t cnt = tc + ns;
             const int st = cnt % kStages, sb = cnt & 1;
-            if (mbar_test(&c.full[st], (cnt / kStages) & 1) && mbar_test(&c.s_free[sb], ((cnt >> 1) & 1) ^ 1)) {
+            if (mbar_test(&c.kfull[st], (cnt / kStages) & 1) && mbar_test(&c.s_free[sb], ((cnt >> 1) & 1) ^ 1)) {
               tc_fence_after();
               const uint64_t a = umma_smem_desc(smem_u32(stages + st * kStageBytes), 16, 1024, kLayout128B);
 #pragma unroll
@@ -451,6 +458,7 @@ __device__ void mma_warp(const DecodeParams& P, Ctl& c, uint8_t* stages, uint8_t
                 umma_f16_ss(tmem + 16 * sb, umma_desc_advance(a, (kk >> 2) * kHalfBytes + (kk & 3) * 32),
                             umma_desc_advance(qdesc, (kk >> 2) * 2048 + (kk & 3) * 32), idesc_s, kk > 0);
               umma_commit(&c.s_full[sb]);
+              umma_commit(&c.kempty[st]);  // this K is read by no other MMA
               if (ns == nt - 1) umma_commit(&c.q_free[qb]);
               issued = true;
               ++ns;
@@ -472,7 +480,7 @@ __device__ void mma_warp(const DecodeParams& P, Ctl& c, uint8_t* stages, uint8_t
                             idesc_o, kk > 0);
               umma_commit(&c.o_full[b]);
               umma_commit(&c.p_free[b]);
-              umma_commit(&c.empty[st]);
+              umma_commit(&c.vempty[st]);
               ++npv;
               progress = true;
             }
@@ -618,9 +626,9 @@ __device__ void softmax_warps(const DecodeParams& P, Ctl& c, uint8_t* stages, ui
         l_run[g] = fmaf(l_run[g], alpha[g], p[g]);
         m_run[g] = m_new;
       }
-      // the stage's K/V have landed (needed to zero V rows of masked keys, and to
-      // order the producer's bad-block flag before it is read)
-      if (!mbar_wait(&c.full[st], (tc / kStages) & 1, abort_flag)) {
+      // the tile's V has landed (needed to zero V rows of masked keys; P V is issued
+      // only after P, so this wait also orders it after the load)
+      if (!mbar_wait(&c.vfull[st], (tc / kStages) & 1, abort_flag)) {
         ok = false;
         break;
       }
@@ -743,11 +751,11 @@ __device__ void softmax_warps(const DecodeParams& P, Ctl& c, uint8_t* stages, ui
         ml[2 * g + 1] = lt[g];
       }
       merge_fold<GP>(M, num, den, ml, acc);
-      // a bad block id in the prefix was flagged by the cascade kernel
-      const bool any_bad = bad || __ldg(P.unit_bad + unit) != 0;
+      // (a member's prefix has only valid block ids: the planner admits no member of a
+      // group whose prefix names a bad one, so only this item's own tiles can be bad)
 #pragma unroll
       for (int g = 0; g < GP; ++g)
-        if (g < G) orow[g * 128] = __float2bfloat16_rn(any_bad ? 0.f : __fdividef(num[g], den[g]));
+        if (g < G) orow[g * 128] = __float2bfloat16_rn(bad ? 0.f : __fdividef(num[g], den[g]));
     } else {
       // partials: accumulators [item][d][GP] (one float4 run per thread), max and sum
       // [item][GP][2]; the merge kernel that runs after this one combines them
@@ -786,8 +794,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&c.full[s], 1);
-      mbar_init(&c.empty[s], 1);
+      mbar_init(&c.kfull[s], 1);
+      mbar_init(&c.kempty[s], 1);
+      mbar_init(&c.vfull[s], 1);
+      mbar_init(&c.vempty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&c.s_full[b], 1);
@@ -801,7 +811,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     }
     for (int s = 0; s < kRing; ++s) {
       mbar_init(&c.item_full[s], 1);
-      mbar_init(&c.item_empty[s], 6);  // producer, MMA warp, four softmax warps
+      mbar_init(&c.item_empty[s], 7);  // two producers, MMA warp, four softmax warps
     }
     mbar_init(&c.drain, 1);
     mbar_init(&c.group_bar, 4);
@@ -824,10 +834,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   grid_dep_wait();  // the plan (and new tokens) of this call, from the kernels before
   grid_dep_launch();
 
-  if (warp == 0) producer_warp(P, &qmap, &kmap, &vmap, c, stages, qbuf);
+  if (warp == 0) producer_warp<false>(P, &qmap, &kmap, &vmap, c, stages, qbuf);
   else if (warp == 1) mma_warp(P, c, stages, qbuf, pbuf, tmem);
   else if (warp < 6) softmax_warps<GP>(P, c, stages, pbuf, tmem);
-  else scheduler_warp(P, c);
+  else if (warp == 6) scheduler_warp(P, c);
+  else producer_warp<true>(P, &qmap, &kmap, &vmap, c, stages, qbuf);
 
   tc_fence_before();
   __syncthreads();
