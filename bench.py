@@ -41,14 +41,14 @@ METRIC = "decode KV-read GB/s (% of HBM peak); mixed-step tokens/sec at 1 GB300"
 
 # DRAM traffic of the decode kernel per algorithmic byte, from one-pass ncu captures of one
 # decode launch of each workload (dram__bytes_read.sum + dram__bytes_write.sum):
-#   mixed step:      19.4999 GB + 36.4 MB for 19.409 GB of algorithmic bytes;
+#   mixed step:      19.4999 GB + 36.1 MB for 19.409 GB of algorithmic bytes;
 #   batched decode:  505.07 MB + 3.86 MB for 503.62 MB (decode-only: K/V loaded evict-first).
 # A ratio is reported only for the workload it was measured on, and only while the
 # profiled sources are unchanged.
 NCU_TRAFFIC = {
     "sources": ("k_decode.cu", "ptx.cuh", "pkv_internal.cuh"),
-    "sha256": "d1b62eb2871e6c2929772248bc4bf42ea2461bc1ab9c1393d176c679785d7c3c",
-    "decode": {"mixed": (19.4999e9 + 36.4e6) / 19409039536, "decode": (505.07e6 + 3.86e6) / 503617604},
+    "sha256": "dba3579f47b75b883b61585f59222874d1fe4858cc0dd7b9a44901b63befb782",
+    "decode": {"mixed": (19.499862e9 + 36.092416e6) / 19409039536, "decode": (505.069568e6 + 3.862784e6) / 503617604},
 }
 
 
