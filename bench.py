@@ -197,21 +197,24 @@ class Step:
             p.paged_attention(q, t["k_cache"], t["v_cache"], self.bt, self.sl, self.qsl, w.scale,
                               w.max_query_len, w.max_seq_len, out=out)
 
-    def write_and_attend(self, q, k_new, v_new, out):
+    def write_and_attend(self, q, k_new, v_new, out, cow=None):
+        """The step's calls after its inputs are on the device: the copy-on-write pairs
+        ``cow`` (src, dst) if any, slot mapping, scatter and attention -- all in one call
+        when fused."""
         p, w, t = self.pkv, self.w, self.t
-        if self.fused:  # slot mapping, scatter and attention in one call
+        if self.fused:
             p.paged_attention_step(q, k_new, v_new, t["k_cache"], t["v_cache"], self.bt, self.sl, self.qsl, w.scale,
-                                   w.max_query_len, w.max_seq_len, prefix_groups=self.groups, out=out)
+                                   w.max_query_len, w.max_seq_len, prefix_groups=self.groups, out=out, cow=cow)
         else:
+            if cow:
+                p.pkv_copy_blocks(cow[0], cow[1], t["k_cache"], t["v_cache"])
             p.pkv_slot_mapping(self.bt, self.sl, self.qsl, w.num_tokens, out=self.slots)
             p.pkv_write(k_new, v_new, self.slots, t["k_cache"], t["v_cache"])
             self.attend(q, out)
 
     def run(self):
-        p, t = self.pkv, self.t
-        if self.cow is not None:
-            p.pkv_copy_blocks(self.cow[0], self.cow[1], t["k_cache"], t["v_cache"])
-        self.write_and_attend(t["q"], t["k_new"], t["v_new"], self.out)
+        t = self.t
+        self.write_and_attend(t["q"], t["k_new"], t["v_new"], self.out, cow=self.cow)
 
     def attention_only(self):
         self.attend(self.t["q"], self.out)
@@ -246,8 +249,7 @@ class E2EStep:
         if s.cow is not None:
             for dst, src in zip(s.cow, self.h_cow):
                 dst.copy_(src, non_blocking=True)
-            p.pkv_copy_blocks(s.cow[0], s.cow[1], t["k_cache"], t["v_cache"])
-        s.write_and_attend(self.d["q"], self.d["k_new"], self.d["v_new"], s.out)
+        s.write_and_attend(self.d["q"], self.d["k_new"], self.d["v_new"], s.out, cow=s.cow)
         self.h_out.copy_(s.out, non_blocking=True)
 
 
@@ -286,13 +288,14 @@ class E2EPipelined:
 
     def _compute(self, d):
         s, p, w, t = self.s, self.s.pkv, self.s.w, self.s.t
-        if d["cow"]:
-            p.pkv_copy_blocks(d["cow"][0], d["cow"][1], t["k_cache"], t["v_cache"])
+        cow = d["cow"] if d["cow"] else None
         if s.fused:
             p.paged_attention_step(d["q"], d["k_new"], d["v_new"], t["k_cache"], t["v_cache"], d["bt"], d["sl"],
                                    d["qsl"], w.scale, w.max_query_len, w.max_seq_len, prefix_groups=s.groups,
-                                   out=d["out"])
+                                   out=d["out"], cow=cow)
         else:
+            if cow:
+                p.pkv_copy_blocks(cow[0], cow[1], t["k_cache"], t["v_cache"])
             p.pkv_slot_mapping(d["bt"], d["sl"], d["qsl"], w.num_tokens, out=s.slots)
             p.pkv_write(d["k_new"], d["v_new"], s.slots, t["k_cache"], t["v_cache"])
             p.paged_attention(d["q"], t["k_cache"], t["v_cache"], d["bt"], d["sl"], d["qsl"], w.scale,

@@ -17,6 +17,7 @@
  *                     causal chunked prefill, gathering K/V through block tables
  *   paged_attention_cascade  the same, reading each shared prompt prefix once
  *   paged_attention_step     slot mapping + K/V scatter + attention in one call
+ *   paged_attention_step_cow the same, after the step's copy-on-write block copies
  *
  * Conventions for every call
  *  - Pointers named as device pointers must point to device memory of the current
@@ -218,6 +219,27 @@ PKV_API int paged_attention_step(const void* q, const void* k_new, const void* v
                                  const int32_t* query_start_loc, int32_t num_seqs, int32_t num_q_heads,
                                  int64_t num_tokens, int32_t max_query_len, int32_t max_seq_len, float scale,
                                  const pkv_prefix_groups* groups, int64_t* slot_mapping, void* out, void* stream);
+
+/*
+ * paged_attention_step_cow -- pkv_copy_blocks(cow_src, cow_dst, num_cow) followed by
+ * paged_attention_step, in one call, with the same results bit for bit.  The copies
+ * are the copy-on-write of the "vLLM's PagedAttention" teardown, section
+ * "PagedAttention": a request about to write into a block another request still
+ * shares gets a fresh copy first.  Taking them in the same call lets the step plan
+ * its work while the copies run, instead of after them; only the new tokens' writes,
+ * which may land in a copied block, wait for the copies.
+ * cow_src, cow_dst  device int32 [num_cow] block ids (as pkv_copy_blocks)
+ * num_cow          0: no copies (exactly paged_attention_step)
+ * Everything else and the errors: as paged_attention_step() and pkv_copy_blocks().
+ */
+PKV_API int paged_attention_step_cow(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                                     void* v_cache, const pkv_cache_desc* cache, const int32_t* block_tables,
+                                     int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                     const int32_t* query_start_loc, int32_t num_seqs, int32_t num_q_heads,
+                                     int64_t num_tokens, int32_t max_query_len, int32_t max_seq_len, float scale,
+                                     const pkv_prefix_groups* groups, const int32_t* cow_src,
+                                     const int32_t* cow_dst, int64_t num_cow, int64_t* slot_mapping, void* out,
+                                     void* stream);
 
 /*
  * paged_attention_noalloc -- paged_attention() for callers that cannot let a library

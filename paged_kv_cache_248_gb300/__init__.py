@@ -71,6 +71,8 @@ def lib():
                                             ctypes.POINTER(_PrefixGroups), P, P],
                 "paged_attention_step": [P, P, P, P, P, D, P, i32, P, P, i32, i32, i64, i32, i32, f32,
                                          ctypes.POINTER(_PrefixGroups), P, P, P],
+                "paged_attention_step_cow": [P, P, P, P, P, D, P, i32, P, P, i32, i32, i64, i32, i32, f32,
+                                             ctypes.POINTER(_PrefixGroups), P, P, i64, P, P, P],
                 "pkv_get_last_error": [P],
                 "pkv_peek_error_bits": [P, ctypes.POINTER(ctypes.c_uint32)],
                 "pkv_num_workers": [ctypes.POINTER(ctypes.c_int32)],
@@ -226,11 +228,13 @@ def paged_attention_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tens
                          v_cache: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor,
                          query_start_loc: torch.Tensor, scale: float, max_query_len: int, max_seq_len: int,
                          prefix_groups=None, slot_mapping: torch.Tensor | None = None,
-                         out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+                         out: torch.Tensor | None = None, stream=None, cow=None) -> torch.Tensor:
     """Slot mapping, K/V scatter and attention of one step in one call (same results as
     pkv_slot_mapping + pkv_write + paged_attention[_cascade]).  ``prefix_groups`` is
     None or (prefix_block_tables, prefix_num_blocks, member_start, member_seqs);
-    ``slot_mapping``, if given, receives the int64 slots."""
+    ``slot_mapping``, if given, receives the int64 slots.  ``cow`` is None or
+    (src, dst) int32 block ids: copied first, as pkv_copy_blocks (C call
+    paged_attention_step_cow)."""
     desc = _cache_desc(k_cache, v_cache)
     if out is None:
         out = torch.empty_like(q)
@@ -238,17 +242,23 @@ def paged_attention_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tens
     if k_new.shape != (T, k_cache.shape[1], d) or v_new.shape != k_new.shape:
         raise ValueError("k_new and v_new must be [num_tokens, num_kv_heads, head_dim]")
     g = _groups(prefix_groups)
-    _check(lib().paged_attention_step(_dev(q, "q", k_cache.dtype), _dev(k_new, "k_new", k_cache.dtype),
-                                      _dev(v_new, "v_new", k_cache.dtype), _dev(k_cache, "k_cache"),
-                                      _dev(v_cache, "v_cache"), ctypes.byref(desc),
-                                      _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
-                                      _dev(seq_lens, "seq_lens", torch.int32),
-                                      _dev(query_start_loc, "query_start_loc", torch.int32), seq_lens.shape[0],
-                                      hq, T, int(max_query_len), int(max_seq_len), float(scale),
-                                      ctypes.byref(g) if g is not None else None,
-                                      _dev(slot_mapping, "slot_mapping", torch.int64) if slot_mapping is not None
-                                      else None, _dev(out, "out", k_cache.dtype), _stream(stream)),
-           "paged_attention_step")
+    head = (_dev(q, "q", k_cache.dtype), _dev(k_new, "k_new", k_cache.dtype), _dev(v_new, "v_new", k_cache.dtype),
+            _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), ctypes.byref(desc),
+            _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+            _dev(seq_lens, "seq_lens", torch.int32), _dev(query_start_loc, "query_start_loc", torch.int32),
+            seq_lens.shape[0], hq, T, int(max_query_len), int(max_seq_len), float(scale),
+            ctypes.byref(g) if g is not None else None)
+    tail = (_dev(slot_mapping, "slot_mapping", torch.int64) if slot_mapping is not None else None,
+            _dev(out, "out", k_cache.dtype), _stream(stream))
+    if cow is None:
+        _check(lib().paged_attention_step(*head, *tail), "paged_attention_step")
+    else:
+        src, dst = cow
+        if src.shape != dst.shape or src.dim() != 1:
+            raise ValueError("cow src and dst must be int32 vectors of one length")
+        _check(lib().paged_attention_step_cow(*head, _dev(src, "cow src", torch.int32),
+                                              _dev(dst, "cow dst", torch.int32), src.shape[0], *tail),
+               "paged_attention_step_cow")
     return out
 
 

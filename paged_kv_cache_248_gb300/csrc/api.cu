@@ -303,15 +303,19 @@ int pkv_copy_blocks(const int32_t* src, const int32_t* dst, int64_t n, void* k_c
 
 namespace {
 
-// paged_attention, paged_attention_cascade and paged_attention_step: `groups` null =
-// no shared prefixes; `k_new` null = no new tokens to write first.
+// paged_attention, paged_attention_cascade, paged_attention_step and
+// paged_attention_step_cow: `groups` null = no shared prefixes; `k_new` null = no new
+// tokens to write first; num_cow > 0 = copy those blocks (as pkv_copy_blocks) before
+// anything else.
 int attention_impl(const void* q, const void* k_new, const void* v_new, const void* k_cache, const void* v_cache,
                    const pkv_cache_desc* cache, const int32_t* block_tables, int32_t max_blocks_per_seq,
                    const int32_t* seq_lens, const int32_t* query_start_loc, int32_t num_seqs, int32_t num_q_heads,
                    int64_t num_tokens, int32_t max_query_len, int32_t max_seq_len, float scale,
-                   const pkv_prefix_groups* groups, int64_t* slots_out, void* out, void* stream) {
+                   const pkv_prefix_groups* groups, int64_t* slots_out, void* out, void* stream,
+                   const int32_t* cow_src = nullptr, const int32_t* cow_dst = nullptr, int64_t num_cow = 0) {
   int st = check_cache(cache);
   if (st) return st;
+  if (num_cow < 0 || (num_cow > 0 && (!cow_src || !cow_dst))) return PKV_ERR_INVALID_ARG;
   const bool write = k_new != nullptr;
   if (write && (!v_new || !aligned16(k_new) || !aligned16(v_new))) return PKV_ERR_INVALID_ARG;
   if (num_tokens < 0 || num_seqs < 0 || num_q_heads <= 0 || num_q_heads % cache->num_kv_heads != 0)
@@ -329,7 +333,14 @@ int attention_impl(const void* q, const void* k_new, const void* v_new, const vo
                         groups->num_members};
     }
   }
-  if (num_tokens == 0) return PKV_OK;
+  if (num_tokens == 0) {  // nothing to attend; the copies (if any) still happen
+    if (num_cow == 0) return PKV_OK;
+    if (!k_cache || !v_cache || !aligned16(k_cache) || !aligned16(v_cache)) return PKV_ERR_INVALID_ARG;
+    DeviceCtx* ctx = device_ctx(&st);
+    if (!ctx) return st;
+    return launch_copy_blocks(cow_src, cow_dst, num_cow, const_cast<void*>(k_cache), const_cast<void*>(v_cache),
+                              *cache, ctx->err, as_stream(stream));
+  }
   if (num_seqs == 0 || max_blocks_per_seq <= 0 || max_query_len <= 0 || max_seq_len <= 0) return PKV_ERR_INVALID_ARG;
   if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !query_start_loc || !out)
     return PKV_ERR_INVALID_ARG;
@@ -346,6 +357,11 @@ int attention_impl(const void* q, const void* k_new, const void* v_new, const vo
   AttnArgs a{q,        k_cache,    v_cache,       *cache,      block_tables, max_blocks_per_seq, seq_lens,
              query_start_loc, num_seqs, num_q_heads, num_tokens, max_query_len, max_seq_len, scale, out};
   cudaStream_t s = as_stream(stream);
+  if (num_cow > 0) {
+    st = launch_copy_blocks(cow_src, cow_dst, num_cow, const_cast<void*>(k_cache), const_cast<void*>(v_cache), *cache,
+                            ctx->err, s);
+    if (st) return st;
+  }
   if (cache->dtype == PKV_F32) {  // groups do not change results
     if (write) {
       int64_t* slots = slots_out;
@@ -408,6 +424,8 @@ int attention_impl(const void* q, const void* k_new, const void* v_new, const vo
     plan.num_slots = cache->num_blocks * kBlock;
     plan.vec_per_row = cache->head_dim * 2 / 16;
     plan.write_ctas = static_cast<int32_t>(want < 2 * ctx->num_sms ? want : 2 * ctx->num_sms);
+    plan.cow_dst = cow_dst;
+    plan.num_cow = num_cow;
   }
   const int cas_tpi = casp ? cascade_tiles_per_item(cas.num_members, hkv, gp, cas.max_blocks, ctx->num_sms) : 1;
   // with few groups the cascade kernel finds its own items and runs beside the planner
@@ -471,6 +489,19 @@ int paged_attention_step(const void* q, const void* k_new, const void* v_new, vo
   return attention_impl(q, k_new, v_new, k_cache, v_cache, cache, block_tables, max_blocks_per_seq, seq_lens,
                         query_start_loc, num_seqs, num_q_heads, num_tokens, max_query_len, max_seq_len, scale,
                         groups, slot_mapping, out, stream);
+}
+
+int paged_attention_step_cow(const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                             const pkv_cache_desc* cache, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                             const int32_t* seq_lens, const int32_t* query_start_loc, int32_t num_seqs,
+                             int32_t num_q_heads, int64_t num_tokens, int32_t max_query_len, int32_t max_seq_len,
+                             float scale, const pkv_prefix_groups* groups, const int32_t* cow_src,
+                             const int32_t* cow_dst, int64_t num_cow, int64_t* slot_mapping, void* out,
+                             void* stream) {
+  if (!k_new || !v_new) return PKV_ERR_INVALID_ARG;
+  return attention_impl(q, k_new, v_new, k_cache, v_cache, cache, block_tables, max_blocks_per_seq, seq_lens,
+                        query_start_loc, num_seqs, num_q_heads, num_tokens, max_query_len, max_seq_len, scale,
+                        groups, slot_mapping, out, stream, cow_src, cow_dst, num_cow);
 }
 
 int pkv_peek_error_bits(void* stream, uint32_t* bits) {

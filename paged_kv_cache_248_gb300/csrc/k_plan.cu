@@ -187,17 +187,19 @@ __device__ void plan_cascade(const PlanArgs& p) {
 // which reports the bad id for them.  When the cascade kernel runs beside this launch
 // (cas_concurrent) it reads the prefix blocks while the writer CTAs may still be
 // writing this call's new tokens, so then a new token that lands in any group's prefix
-// block -- or a query_start_loc that decreases, which the writers would map
-// differently -- admits nobody anywhere (a correct, slower fallback for inputs a
-// serving loop does not produce: shared prefix blocks are full and never written).
-// Every group's prefix blocks are marked with the call's epoch in the workspace, then
-// each request's warp checks the blocks its new tokens go to, as the writers compute
-// them.  Called by the whole block; returns synchronised.
+// block, a copy-on-write copy of the same call that lands in one, or a
+// query_start_loc that decreases (which the writers would map differently) admits
+// nobody anywhere: a correct, slower fallback for inputs a serving loop does not
+// produce, since shared prefix blocks are full and never written.  Every group's
+// prefix blocks are marked with the call's epoch in the workspace, then a thread per
+// request checks the blocks its new tokens go to, as the writers compute them, and the
+// copies' destinations are checked the same way.  Called by the whole block; returns
+// synchronised.
 __device__ void prefix_block_checks(const PlanArgs& p) {
   __shared__ int s_conflict;
   const CascadeArgs& g = p.cas;
   const int tid = threadIdx.x, nthr = blockDim.x;
-  const bool marks = p.cas_concurrent && p.k_new != nullptr;
+  const bool marks = p.cas_concurrent && (p.k_new != nullptr || p.num_cow > 0);
   if (tid == 0) s_conflict = 0;
   for (int gi = tid; gi < g.num_groups; gi += nthr) p.grp_ok[gi] = 1;
   __syncthreads();
@@ -212,7 +214,7 @@ __device__ void prefix_block_checks(const PlanArgs& p) {
   __syncthreads();
   if (marks) {
     // a thread per request: its loads overlap those of the other requests
-    for (int i = tid; i < p.num_seqs; i += nthr) {
+    for (int i = tid; p.k_new != nullptr && i < p.num_seqs; i += nthr) {
       const int64_t q0 = __ldg(p.qsl + i), q1 = __ldg(p.qsl + i + 1), L = __ldg(p.seq_lens + i);
       if (q1 < q0) {
         s_conflict = 1;
@@ -231,6 +233,11 @@ __device__ void prefix_block_checks(const PlanArgs& p) {
         hit |= b >= 0 && b < p.num_blocks && p.blk_mark[b] == p.epoch;
       }
       if (hit) s_conflict = 1;
+    }
+    // a copy-on-write destination in a prefix (the copies may still be running)
+    for (int64_t x = tid; x < p.num_cow; x += nthr) {
+      const int32_t b = __ldg(p.cow_dst + x);
+      if (b >= 0 && b < p.num_blocks && p.blk_mark[b] == p.epoch) s_conflict = 1;
     }
     __syncthreads();
     if (s_conflict)
@@ -619,9 +626,16 @@ __device__ void order_decode_onchip(const PlanArgs& p, const int32_t* s_nd, cons
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs p) {
   extern __shared__ int32_t plan_smem[];  // writers: query_start_loc; planner: on-chip membership
   // the previous step's kernels read the workspace this rewrites and the cache the
-  // writers write: wait for them
-  grid_dep_wait();
-  grid_dep_launch();
+  // writers write: wait for them.  After this call's own copy-on-write launch, which
+  // waited for them before it let this one start, only the writers wait (for the
+  // copies); the kernels after this one may then start before the copies end
+  if (p.num_cow > 0) {
+    grid_dep_launch();
+    if (blockIdx.x > 0) grid_dep_wait();
+  } else {
+    grid_dep_wait();
+    grid_dep_launch();
+  }
   if (blockIdx.x > 0) {  // writer CTAs never join the planner's block barriers
     write_new_tokens(p, plan_smem);
     return;

@@ -254,6 +254,11 @@ struct PlanArgs {
   int64_t num_slots = 0;         // num_blocks * 16
   int32_t vec_per_row = 0;       // 16-byte vectors per (token, kv head) row
   int32_t write_ctas = 0;        // CTAs after the planning CTA that do the writes
+  // copy-on-write copies launched by the same call just before this launch (num_cow 0:
+  // none).  Their kernel waited for everything before it, so the planner need not;
+  // the writers wait for the copies and let the kernels after this one launch first
+  const int32_t* cow_dst = nullptr;
+  int64_t num_cow = 0;
   int32_t cas_onchip = 0;        // set by launch_plan: the membership checks run in shared memory
   int32_t ord_onchip = 0;        // set by launch_plan: the decode order is built in shared memory
   int32_t ord_offset = 0;        //   at this int offset of the planner's dynamic shared memory

@@ -107,6 +107,20 @@ def test_cascade_host_checks_fail_without_launching(lib):
     assert lib.paged_attention_cascade(*bad_scale, None, fake, None) == pkv.PKV_ERR_INVALID_ARG
 
 
+def test_step_with_copies_host_checks_fail_without_launching(lib):
+    import paged_kv_cache_248_gb300 as pkv
+    P = ctypes.c_void_p
+    fake = P(0x1000)  # never dereferenced: each call below fails its host checks first
+    desc = _desc(pkv, d=128, dt=1)
+    head = (fake, fake, fake, fake, fake, ctypes.byref(desc), fake, 4, fake, fake, 2, 8, 2, 1, 64,
+            ctypes.c_float(0.1), None)
+    assert lib.paged_attention_step_cow(*head, fake, fake, -1, None, fake, None) == pkv.PKV_ERR_INVALID_ARG
+    assert lib.paged_attention_step_cow(*head, None, fake, 3, None, fake, None) == pkv.PKV_ERR_INVALID_ARG
+    assert lib.paged_attention_step_cow(*head, fake, None, 3, None, fake, None) == pkv.PKV_ERR_INVALID_ARG
+    no_new = (fake, None) + head[2:]
+    assert lib.paged_attention_step_cow(*no_new, fake, fake, 3, None, fake, None) == pkv.PKV_ERR_INVALID_ARG
+
+
 def test_noalloc_refuses_too_many_split_items_like_paged_attention(lib):
     # 2^20 requests x 8 kv heads x ceil(2^18 / 1024) splits = 2^31 items: both calls
     # refuse the batch as unsupported on the host, before any CUDA call

@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import workloads as wl
-from helpers import compare, oracle_step, sub_batch
+from helpers import bits, compare, oracle_step, sub_batch
 
 pytestmark = pytest.mark.gpu
 
@@ -184,3 +184,79 @@ def test_step_replays_from_a_cuda_graph(pkv):
     assert pkv.pkv_get_last_error() == 0
     assert torch.equal(out_g, out_e)
     assert torch.equal(t["k_cache"], k_after) and torch.equal(t["v_cache"], v_after)
+
+
+def both_ways_cow(pkv, w, t, src, dst, groups=None):
+    """pkv_copy_blocks then paged_attention_step, and paged_attention_step with the
+    copies in the same call, on two copies of the caches: (out, slots, k, v, status) each."""
+    bt, sl, qsl = dev(w.block_tables), dev(w.seq_lens), dev(w.query_start_loc)
+    s, d = dev(np.asarray(src, np.int32)), dev(np.asarray(dst, np.int32))
+    mq, ms = max(1, w.max_query_len), max(1, w.max_seq_len)
+    res = []
+    for fused in (False, True):
+        kc, vc = t["k_cache"].clone(), t["v_cache"].clone()
+        slots = torch.full((w.num_tokens,), -7, dtype=torch.int64, device="cuda")
+        if not fused:
+            pkv.pkv_copy_blocks(s, d, kc, vc)
+        out = pkv.paged_attention_step(t["q"], t["k_new"], t["v_new"], kc, vc, bt, sl, qsl, w.scale, mq, ms,
+                                       prefix_groups=groups, slot_mapping=slots, cow=(s, d) if fused else None)
+        res.append((out, slots, kc, vc, pkv.pkv_get_last_error()))
+    return res
+
+
+def test_step_with_copies_on_the_prefix_workload(pkv):
+    """The prefix-shared workload with its copy-on-write pairs handed to the step:
+    bit-equal to pkv_copy_blocks followed by the step, and every row matches the oracle."""
+    w = wl.make("prefix")
+    t_cpu = w.make_tensors("cpu")
+    t = {k: v.cuda() for k, v in t_cpu.items()}
+    pid = w.notes["shared_prefix_ids"]
+    groups = (dev(pid[None, :]), dev(np.array([pid.size], np.int32)), dev(np.array([0, w.num_seqs], np.int32)),
+              dev(np.arange(w.num_seqs, dtype=np.int32)))
+    sep, fus = both_ways_cow(pkv, w, t, w.cow_src, w.cow_dst, groups)
+    assert sep[4] == 0
+    assert_same(sep, fus)
+    ref, ref_slots, _, _ = oracle_step(w, t_cpu, cow=True)
+    assert np.array_equal(fus[1].cpu().numpy(), ref_slots)
+    compare(fus[0], ref, "bf16", "prefix with copies in the step")
+
+
+def test_step_with_a_copy_into_a_prefix_block(pkv):
+    # a copy whose destination is one of the shared prefix blocks (the copy rewrites a
+    # block every member attends): the step's cascade could read it mid-copy, so the
+    # step lets every member attend its whole context itself; caches equal the separate
+    # calls' bit for bit and both outputs match the oracle
+    w, hints = wl.shared_prefix_case(31, prefix_blocks=(20,), members=(30,), bystanders=6, bad_hints=False)
+    members = set(hints["member_seqs"].tolist())
+    i = next(i for i in range(w.num_seqs) if i not in members)
+    src = np.array([w.block_tables[i, 0]], np.int32)
+    dst = np.array([hints["prefix_block_tables"][0, 4]], np.int32)
+    w.cow_src, w.cow_dst = src, dst
+    t_cpu = w.make_tensors("cpu")
+    t = {k: v.cuda() for k, v in t_cpu.items()}
+    sep, fus = both_ways_cow(pkv, w, t, src, dst, hint_tensors(hints))
+    ref, _, _, _ = oracle_step(w, t_cpu, cow=True)
+    caches_same_outputs_match(sep, fus, ref, w.name)
+
+
+@pytest.mark.parametrize("seed,dtype", [(32, "bf16"), (33, "f32")])
+def test_step_with_copies_equals_the_separate_calls(pkv, seed, dtype):
+    # copies into blocks no table names yet: the caches show them, the outputs do not
+    d = 128 if dtype == "bf16" else 64
+    w = wl.random_case(seed, num_seqs=12, max_ctx=900, max_q=200, group=4, num_kv_heads=2, head_dim=d, dtype=dtype,
+                       pool_slack=9)
+    used = np.unique(w.block_tables[w.block_tables >= 0])
+    free = np.setdiff1d(np.arange(w.num_blocks), used)
+    assert free.size >= 4
+    src, dst = used[:4].astype(np.int32), free[:4].astype(np.int32)
+    w.cow_src, w.cow_dst = src, dst
+    t_cpu = w.make_tensors("cpu")
+    t = {k: v.cuda() for k, v in t_cpu.items()}
+    sep, fus = both_ways_cow(pkv, w, t, src, dst)
+    assert sep[4] == 0
+    assert_same(sep, fus)
+    ref, _, ref_k, ref_v = oracle_step(w, t_cpu, cow=True)
+    compare(fus[0], ref, dtype, w.name)
+    # the pools after the copies and the writes (the writes may land in a copy's source)
+    for got, want, name in ((fus[2], ref_k, "k_cache"), (fus[3], ref_v, "v_cache")):
+        assert np.array_equal(bits(got), want), name
