@@ -303,6 +303,24 @@ int pkv_copy_blocks(const int32_t* src, const int32_t* dst, int64_t n, void* k_c
 
 namespace {
 
+// The writer CTAs of a planning launch: new tokens' K/V rows into their slots (a warp per
+// 64-vector piece of a token's rows, at most two CTAs per SM).
+void set_writers(PlanArgs& p, const void* k_new, const void* v_new, const void* k_cache, const void* v_cache,
+                 const pkv_cache_desc& cache, int64_t* slots_out, int64_t num_tokens, int num_sms) {
+  const int64_t warps_per_cta = 1024 / 32;
+  const int elem = cache.dtype == PKV_F32 ? 4 : 2;
+  const int64_t pieces = (cache.num_kv_heads * (cache.head_dim * elem / 16) + 63) / 64;
+  const int64_t want = (num_tokens * pieces + warps_per_cta - 1) / warps_per_cta;
+  p.k_new = static_cast<const uint4*>(k_new);
+  p.v_new = static_cast<const uint4*>(v_new);
+  p.k_cache = static_cast<uint4*>(const_cast<void*>(k_cache));
+  p.v_cache = static_cast<uint4*>(const_cast<void*>(v_cache));
+  p.slots_out = slots_out;
+  p.num_slots = cache.num_blocks * kBlock;
+  p.vec_per_row = cache.head_dim * elem / 16;
+  p.write_ctas = static_cast<int32_t>(want < 2 * num_sms ? want : 2 * num_sms);
+}
+
 // paged_attention, paged_attention_cascade, paged_attention_step and
 // paged_attention_step_cow: `groups` null = no shared prefixes; `k_new` null = no new
 // tokens to write first; num_cow > 0 = copy those blocks (as pkv_copy_blocks) before
@@ -363,18 +381,15 @@ int attention_impl(const void* q, const void* k_new, const void* v_new, const vo
     if (st) return st;
   }
   if (cache->dtype == PKV_F32) {  // groups do not change results
-    if (write) {
-      int64_t* slots = slots_out;
-      if (!slots) {  // scratch for the slots between the two kernels
-        st = ensure_workspace(ctx, static_cast<size_t>(num_tokens) * sizeof(int64_t), s);
-        if (st) return st;
-        slots = static_cast<int64_t*>(ctx->ws);
-      }
-      st = launch_slot_mapping(block_tables, max_blocks_per_seq, seq_lens, query_start_loc, num_seqs, num_tokens,
-                               slots, ctx->err, s);
-      if (st) return st;
-      st = launch_write(k_new, v_new, slots, num_tokens, const_cast<void*>(k_cache), const_cast<void*>(v_cache),
-                        *cache, ctx->err, s);
+    if (write) {  // slot mapping and scatter in the writer CTAs of a launch that plans nothing
+      PlanArgs w{seq_lens, query_start_loc, num_seqs, num_tokens, cache->num_kv_heads, max_blocks_per_seq,
+                 max_seq_len, kSplitKeys, 0, nullptr, nullptr, nullptr, nullptr, nullptr, ctx->err};
+      w.bt = block_tables;
+      w.writers_only = 1;
+      set_writers(w, k_new, v_new, k_cache, v_cache, *cache, slots_out, num_tokens, ctx->num_sms);
+      w.cow_dst = cow_dst;
+      w.num_cow = num_cow;
+      st = launch_plan(w, s);
       if (st) return st;
     }
     return launch_generic_attention(a, ctx->err, s);
@@ -413,17 +428,7 @@ int attention_impl(const void* q, const void* k_new, const void* v_new, const vo
   plan.dec_pos = ws.dec_pos;
   plan.num_sms = ctx->num_sms;
   if (write) {
-    const int64_t warps_per_cta = 1024 / 32;
-    const int64_t pieces = (cache->num_kv_heads * (cache->head_dim * (cache->dtype == PKV_F32 ? 4 : 2) / 16) + 63) / 64;
-    const int64_t want = (num_tokens * pieces + warps_per_cta - 1) / warps_per_cta;  // a warp per 64-vector piece
-    plan.k_new = static_cast<const uint4*>(k_new);
-    plan.v_new = static_cast<const uint4*>(v_new);
-    plan.k_cache = static_cast<uint4*>(const_cast<void*>(k_cache));
-    plan.v_cache = static_cast<uint4*>(const_cast<void*>(v_cache));
-    plan.slots_out = slots_out;
-    plan.num_slots = cache->num_blocks * kBlock;
-    plan.vec_per_row = cache->head_dim * 2 / 16;
-    plan.write_ctas = static_cast<int32_t>(want < 2 * ctx->num_sms ? want : 2 * ctx->num_sms);
+    set_writers(plan, k_new, v_new, k_cache, v_cache, *cache, slots_out, num_tokens, ctx->num_sms);
     plan.cow_dst = cow_dst;
     plan.num_cow = num_cow;
   }

@@ -640,6 +640,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs p) {
     write_new_tokens(p, plan_smem);
     return;
   }
+  if (p.writers_only) return;
   const int64_t n_units = static_cast<int64_t>(p.num_seqs) * p.hkv;
   for (int64_t u = threadIdx.x; u < n_units; u += blockDim.x) {
     p.unit_bad[u] = 0;

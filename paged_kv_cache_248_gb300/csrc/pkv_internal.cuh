@@ -259,6 +259,7 @@ struct PlanArgs {
   // the writers wait for the copies and let the kernels after this one launch first
   const int32_t* cow_dst = nullptr;
   int64_t num_cow = 0;
+  int32_t writers_only = 0;      // CTA 0 plans nothing (the fp32 path: only the writes)
   int32_t cas_onchip = 0;        // set by launch_plan: the membership checks run in shared memory
   int32_t ord_onchip = 0;        // set by launch_plan: the decode order is built in shared memory
   int32_t ord_offset = 0;        //   at this int offset of the planner's dynamic shared memory
