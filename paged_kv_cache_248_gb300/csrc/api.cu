@@ -455,10 +455,13 @@ int attention_impl(const void* q, const void* k_new, const void* v_new, const vo
     st = launch_cascade_tc(a, cas, ws, ctx->num_sms, cas_tpi, cas_concurrent, ctx->err, s);
     if (st) return st;
   }
-  st = launch_decode_tc(a, ws, ctx->num_sms, ctx->err, s);
+  if (max_query_len <= 1) return launch_decode_tc(a, ws, ctx->num_sms, ctx->err, s);
+  // decode, then the prefill filling the decode's tail, then the split merge
+  st = launch_decode_tc(a, ws, ctx->num_sms, ctx->err, s, kDecodeLaunch);
   if (st) return st;
-  if (max_query_len > 1) st = launch_prefill_tc(a, ws, ctx->num_sms, ctx->err, s);
-  return st;
+  st = launch_prefill_tc(a, ws, ctx->num_sms, ctx->err, s, 1);
+  if (st) return st;
+  return launch_decode_tc(a, ws, ctx->num_sms, ctx->err, s, kMergeLaunch);
 }
 
 }  // namespace

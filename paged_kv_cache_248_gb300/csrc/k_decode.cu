@@ -1099,19 +1099,19 @@ __global__ void __launch_bounds__(128) merge_small_kernel(const MergeParams P) {
 
 template <int GP>
 int launch_gp(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& vm, const DecodeParams& p, int grid,
-              const Workspace& ws, bool may_split, int max_entries, cudaStream_t s) {
+              const Workspace& ws, bool may_split, int max_entries, int what, cudaStream_t s) {
   const int32_t* counters = ws.counters;
   const int32_t* merge_list = ws.merge_list;
   static uint64_t smem_set = 0;
   const int st = set_smem_once(reinterpret_cast<const void*>(decode_kernel<GP>), kSmemBytes, &smem_set);
   if (st) return st;
   cudaError_t e;
-  {
+  if (what & kDecodeLaunch) {
     TraceScope trace(kTraceDecode, s);
     e = launch_k(decode_kernel<GP>, dim3(grid), dim3(kThreads), kSmemBytes, s, qm, km, vm, p);
     if (e != cudaSuccess) return cuda_status(e);
   }
-  if (!may_split) return PKV_OK;  // no context is long enough to be split: nothing to merge
+  if (!may_split || !(what & kMergeLaunch)) return PKV_OK;  // (no context long enough to be split: nothing to merge)
   MergeParams m{p.out,          counters,  merge_list, p.dec_prefix,  p.qsl,     p.unit_bad,    p.part_o,
                 p.part_ml,      p.seq_prefix, ws.seq_entry, ws.cas_o, ws.cas_ml, ws.cas_np_max, p.num_seqs,
                 p.hkv,          p.group,   p.hq};
@@ -1131,7 +1131,7 @@ int launch_gp(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& v
 
 }  // namespace
 
-int launch_decode_tc(const AttnArgs& a, const Workspace& ws, int num_sms, uint32_t* err, cudaStream_t s) {
+int launch_decode_tc(const AttnArgs& a, const Workspace& ws, int num_sms, uint32_t* err, cudaStream_t s, int what) {
   const int hkv = a.cache.num_kv_heads;
   const int group = a.num_q_heads / hkv;
   if (group > 16 || a.cache.head_dim != 128 || a.cache.dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
@@ -1191,9 +1191,9 @@ int launch_decode_tc(const AttnArgs& a, const Workspace& ws, int num_sms, uint32
   // the most partials one unit can fold: its own key splits plus its prefix's splits
   const int max_entries = static_cast<int>(decode_splits(a.max_seq_len)) +
                           (ws.seq_prefix ? ws.cas_np_max : 0);
-  if (gp == 4) return launch_gp<4>(qm, km, vm, p, num_sms, ws, may_split, max_entries, s);
-  if (gp == 8) return launch_gp<8>(qm, km, vm, p, num_sms, ws, may_split, max_entries, s);
-  return launch_gp<16>(qm, km, vm, p, num_sms, ws, may_split, max_entries, s);
+  if (gp == 4) return launch_gp<4>(qm, km, vm, p, num_sms, ws, may_split, max_entries, what, s);
+  if (gp == 8) return launch_gp<8>(qm, km, vm, p, num_sms, ws, may_split, max_entries, what, s);
+  return launch_gp<16>(qm, km, vm, p, num_sms, ws, may_split, max_entries, what, s);
 }
 
 }  // namespace pkv

@@ -121,6 +121,7 @@ struct PrefillParams {
   int32_t cas_max_blocks, cas_groups, cas_np_max;
   int32_t cas_tiles;       // query tiles per cascade item: 2, or 1 (tile 1 of every item absent)
   int32_t cas_concurrent;  // items from the hint alone, beside the planning launch (groups <= 32)
+  int32_t after_decode;    // right after this call's decode kernel, which it need not wait for
 };
 
 // Three-input maximum / minimum (one instruction on sm_100 and later).
@@ -938,7 +939,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   // the plan, the new tokens and the earlier kernels of this call; a cascade beside the
   // planner reads nothing those write (the planner admits no member of a group whose
   // prefix a new token lands in) and waits for them only before it exits
-  const bool beside = kCas && P.cas_concurrent;
+  // (likewise a prefill launched right after the decode kernel: it reads only the
+  // planner's lists, the cache and q, and writes rows of out the decode does not)
+  const bool beside = kCas ? P.cas_concurrent != 0 : P.after_decode != 0;
   if (!beside) grid_dep_wait();
   grid_dep_launch();
   if (warp == 0) producer_warp<kCas>(P, &qmap, &kmap, &vmap, c, qbuf, kbuf, vbuf);
@@ -951,13 +954,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     tmem_dealloc(tmem, kTmemCols);
     tmem_relinquish();
   }
-  // the grid ends after the planning launch: the kernels after it wait on this one only
+  // the grid ends after its predecessor (the planning launch, or the decode kernel): the
+  // kernels after it wait on this one only
   if (beside && threadIdx.x == 0) grid_dep_wait();
 }
 
 }  // namespace
 
-int launch_prefill_tc(const AttnArgs& a, const Workspace& ws, int num_sms, uint32_t* err, cudaStream_t s) {
+int launch_prefill_tc(const AttnArgs& a, const Workspace& ws, int num_sms, uint32_t* err, cudaStream_t s,
+                      int after_decode) {
   const int hkv = a.cache.num_kv_heads;
   const int group = a.num_q_heads / hkv;
   if (group > 16 || a.cache.head_dim != 128 || a.cache.dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
@@ -974,7 +979,8 @@ int launch_prefill_tc(const AttnArgs& a, const Workspace& ws, int num_sms, uint3
   const uint32_t qbox[3] = {64, static_cast<uint32_t>(gp), static_cast<uint32_t>(kTileKeys / gp)};
   st = encode_tensor_map_3d(&qm, a.q, qdims, qstrides, qbox);
   if (st) return st;
-  PrefillParams p;
+  PrefillParams p{};
+  p.after_decode = after_decode != 0 ? 1 : 0;
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.out_v8 = (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0 ? 1 : 0;
   p.bt = a.block_tables;

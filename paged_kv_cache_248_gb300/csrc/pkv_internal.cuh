@@ -266,7 +266,11 @@ struct PlanArgs {
 };
 // One launch: CTA 0 plans; CTAs 1..write_ctas (if any) map and scatter the new tokens.
 int launch_plan(const PlanArgs& p, cudaStream_t s);
-int launch_decode_tc(const AttnArgs& a, const Workspace& ws, int num_sms, uint32_t* err, cudaStream_t s);
+// `what`: kDecodeLaunch, kMergeLaunch or both (the split merge, when a context may be
+// split, right after the decode kernel unless the caller puts another launch between).
+enum : int { kDecodeLaunch = 1, kMergeLaunch = 2 };
+int launch_decode_tc(const AttnArgs& a, const Workspace& ws, int num_sms, uint32_t* err, cudaStream_t s,
+                     int what = kDecodeLaunch | kMergeLaunch);
 // Attends the member decodes of every prefix group to the group's shared prefix,
 // writing per-split partials for the merge (after launch_plan, before launch_decode_tc).
 // Query tiles per cascade item: pairs (sharing each K/V tile) when they still give
@@ -283,7 +287,12 @@ inline int cascade_tiles_per_item(int64_t num_members, int hkv, int gp, int64_t 
 constexpr int kCasConcurrentGroups = 32;
 int launch_cascade_tc(const AttnArgs& a, const CascadeArgs& cas, const Workspace& ws, int num_sms, int tiles_per_item,
                       int concurrent, uint32_t* err, cudaStream_t s);
-int launch_prefill_tc(const AttnArgs& a, const Workspace& ws, int num_sms, uint32_t* err, cudaStream_t s);
+// `after_decode`: launched right after this call's decode kernel (with the merge after
+// it).  It reads nothing the decode writes, so its CTAs start on the SMs the decode's
+// CTAs leave, and wait for the decode only before they exit: the launches after it wait
+// on it alone.
+int launch_prefill_tc(const AttnArgs& a, const Workspace& ws, int num_sms, uint32_t* err, cudaStream_t s,
+                      int after_decode = 0);
 int encode_tensor_map_3d(CUtensorMap* map, const void* base, const uint64_t dims[3], const uint64_t strides[2],
                          const uint32_t box[3]);
 
