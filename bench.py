@@ -41,14 +41,14 @@ METRIC = "decode KV-read GB/s (% of HBM peak); mixed-step tokens/sec at 1 GB300"
 
 # DRAM traffic of the decode kernel per algorithmic byte, from one-pass ncu captures of one
 # decode launch of each workload (dram__bytes_read.sum + dram__bytes_write.sum):
-#   mixed step:      19.4999 GB + 36.1 MB for 19.409 GB of algorithmic bytes;
-#   batched decode:  505.07 MB + 3.86 MB for 503.62 MB (decode-only: K/V loaded evict-first).
+#   mixed step:      19.5008 GB + 36.5 MB for 19.409 GB of algorithmic bytes;
+#   batched decode:  505.08 MB + 3.57 MB for 503.62 MB (decode-only: K/V loaded evict-first).
 # A ratio is reported only for the workload it was measured on, and only while the
 # profiled sources are unchanged.
 NCU_TRAFFIC = {
     "sources": ("k_decode.cu", "ptx.cuh", "pkv_internal.cuh"),
-    "sha256": "dba3579f47b75b883b61585f59222874d1fe4858cc0dd7b9a44901b63befb782",
-    "decode": {"mixed": (19.499862e9 + 36.092416e6) / 19409039536, "decode": (505.069568e6 + 3.862784e6) / 503617604},
+    "sha256": "bd52ee75b47414e2651e720c64f46302a003ebdf162e4cc9d91f3baefcc98b9d",
+    "decode": {"mixed": (19.500793e9 + 36.525056e6) / 19409039536, "decode": (505.0816e6 + 3.57248e6) / 503617604},
 }
 
 
