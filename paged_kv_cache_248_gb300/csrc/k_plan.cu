@@ -67,8 +67,8 @@ __device__ void block_scan3(const int (&v)[3], int (&ex)[3], int (&tot)[3]) {
   __syncthreads();
 }
 
-// Shared-prefix membership: fills seq_prefix / seq_entry / member_ok and the
-// cascade item prefix over groups.  Called by the whole block.
+// Shared-prefix membership: fills seq_prefix / seq_entry and the cascade item prefix
+// over groups (member_ok is its scratch).  Called by the whole block.
 __device__ void plan_cascade(const PlanArgs& p) {
   __shared__ int s_ok;
   const CascadeArgs& g = p.cas;
@@ -149,7 +149,6 @@ __device__ void plan_cascade(const PlanArgs& p) {
     const int pb = p.member_ok[k];
     if (pb > 0) {
       p.seq_prefix[i] = pb * kBlock;
-      p.member_ok[k] = static_cast<int32_t>(p.qsl[i]) + 1;  // the member's query row + 1
     } else if (csr_ok && i >= 0 && i < p.num_seqs && p.seq_entry[i] == k && p.seq_prefix[i] == 0) {
       p.seq_entry[i] = -1;  // claimed but not a member
     }
@@ -259,7 +258,7 @@ constexpr int kCasOnchipSeqs = 8192;
 constexpr int kCasOnchipMembers = 8192;
 constexpr int kCasOnchipGroups = 1024;
 constexpr int kCasOnchipBlocks = 512;  // longest prefix table compared in this pass
-__host__ __device__ constexpr int64_t cas_onchip_ints(int64_t n, int64_t m, int64_t g) { return 2 * n + 4 * m + 2 * g + 1; }
+__host__ __device__ constexpr int64_t cas_onchip_ints(int64_t n, int64_t m, int64_t g) { return 2 * n + 2 * m + 2 * g + 1; }
 __device__ void plan_cascade_onchip(const PlanArgs& p, int32_t* sm, int32_t*& s_prefix, int32_t*& s_entry) {
   __shared__ int s_csr_ok;
   constexpr int kChunk = 16;
@@ -269,10 +268,8 @@ __device__ void plan_cascade_onchip(const PlanArgs& p, int32_t* sm, int32_t*& s_
   s_entry = sm;                    // [n]: claiming entry; -1 none; -2 listed more than once
   s_prefix = s_entry + n;          // [n]: prefix tokens of a member, else 0
   int32_t* s_pb = s_prefix + n;    // [M]: the entry's prefix blocks if its lengths pass, else 0
-  int32_t* s_req = s_pb + M;       // [M]: the entry's request
-  int32_t* s_diff = s_req + M;     // [M]: some chunk of the table differs from the prefix
-  int32_t* s_row = s_diff + M;     // [M]: the request's query row
-  int32_t* s_start = s_row + M;    // [G + 1]
+  int32_t* s_diff = s_pb + M;      // [M]: some chunk of the table differs from the prefix
+  int32_t* s_start = s_diff + M;   // [G + 1]
   int32_t* s_blocks = s_start + G + 1;  // [G]
   for (int i = tid; i < n; i += nthr) s_entry[i] = -1;
   for (int k = tid; k < M; k += nthr) s_diff[k] = 0;
@@ -303,12 +300,10 @@ __device__ void plan_cascade_onchip(const PlanArgs& p, int32_t* sm, int32_t*& s_
       if (i_ok) {
         if (atomicCAS(&s_entry[i], -1, k) != -1) atomicExch(&s_entry[i], -2);  // a second claim: listed twice
         const int64_t q0 = __ldg(p.qsl + i), q1 = __ldg(p.qsl + i + 1), L = __ldg(p.seq_lens + i);
-        s_row[k] = static_cast<int32_t>(q0);
         if (pb_ok && q0 >= 0 && q1 == q0 + 1 && q1 <= p.num_tokens && L <= p.max_seq_len &&
             (L + kBlock - 1) / kBlock <= p.max_blocks && L > static_cast<int64_t>(pb) * kBlock)
           keep = pb;
       }
-      s_req[k] = i_ok ? i : -1;
       s_pb[k] = keep;
     }
     if (i_ok && pb_ok && j0 < pb) {  // this chunk of the request's table against the prefix's
@@ -340,10 +335,6 @@ __device__ void plan_cascade_onchip(const PlanArgs& p, int32_t* sm, int32_t*& s_
     p.seq_entry[i] = pb > 0 ? k : -1;
   }
   __syncthreads();
-  for (int k = tid; k < M; k += nthr) {
-    const int i = csr_ok ? s_req[k] : -1;
-    p.member_ok[k] = (i >= 0 && s_entry[i] == k) ? s_row[k] + 1 : 0;  // the member's query row + 1
-  }
   // cascade items per group: member tiles x kv heads x prefix key splits
   int carry = 0;
   for (int base = 0; base < G; base += nthr) {

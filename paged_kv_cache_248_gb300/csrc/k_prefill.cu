@@ -1025,7 +1025,6 @@ int launch_cascade_tc(const AttnArgs& a, const CascadeArgs& cas, const Workspace
   p.bt = a.block_tables;
   p.seq_lens = a.seq_lens;
   p.qsl = a.qsl;
-  p.queue = ws.counters + kCascadeQueueSlot;
   p.err = err;
   p.num_blocks = a.cache.num_blocks;
   p.num_tokens = a.num_tokens;

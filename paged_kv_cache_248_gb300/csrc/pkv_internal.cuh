@@ -31,7 +31,6 @@ __host__ __device__ inline int64_t decode_splits(int64_t L) {
 }
 constexpr int kNumQueueCounters = 8; // work-queue counters in the workspace
 constexpr int kMergeCountSlot = 2;   // counters[2]: number of requests in the merge list
-constexpr int kCascadeQueueSlot = 3; // counters[3]: the shared-prefix kernel's work queue
 constexpr int kDecOrderSlot = 4;     // counters[4]: 1 when the decode items follow dec_order
 // A decode batch the planner orders (at most 16 items per SM) also gets a direct map
 // from queue position to (request, the request's first position); sized for GPUs of
