@@ -260,3 +260,37 @@ def test_step_with_copies_equals_the_separate_calls(pkv, seed, dtype):
     # the pools after the copies and the writes (the writes may land in a copy's source)
     for got, want, name in ((fus[2], ref_k, "k_cache"), (fus[3], ref_v, "v_cache")):
         assert np.array_equal(bits(got), want), name
+
+
+def test_step_with_copies_replays_from_a_cuda_graph(pkv):
+    # the copy launch, the planner that overlaps it and the cascade pass beside the
+    # planner, captured once and replayed: the same bits as the eager call
+    w, hints = wl.shared_prefix_case(34, prefix_blocks=(24,), members=(40,), bystanders=4, bad_hints=False)
+    used = np.unique(w.block_tables[w.block_tables >= 0])
+    free = np.setdiff1d(np.arange(w.num_blocks), used)
+    src, dst = dev(used[-3:].astype(np.int32)), dev(free[:3].astype(np.int32))
+    t = {k: v.cuda() for k, v in w.make_tensors("cpu").items()}
+    bt, sl, qsl = dev(w.block_tables), dev(w.seq_lens), dev(w.query_start_loc)
+    groups = hint_tensors(hints)
+    kc0, vc0 = t["k_cache"].clone(), t["v_cache"].clone()
+    out_e, out_g = torch.empty_like(t["q"]), torch.full_like(t["q"], float("nan"))
+
+    def call(out):
+        pkv.paged_attention_step(t["q"], t["k_new"], t["v_new"], t["k_cache"], t["v_cache"], bt, sl, qsl, w.scale,
+                                 max(1, w.max_query_len), w.max_seq_len, prefix_groups=groups, out=out,
+                                 cow=(src, dst))
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        call(out_e)
+    s.synchronize()
+    k_after, v_after = t["k_cache"].clone(), t["v_cache"].clone()
+    t["k_cache"].copy_(kc0)
+    t["v_cache"].copy_(vc0)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call(out_g)
+    g.replay()
+    torch.cuda.synchronize()
+    assert pkv.pkv_get_last_error() == 0
+    assert torch.equal(out_g, out_e)
+    assert torch.equal(t["k_cache"], k_after) and torch.equal(t["v_cache"], v_after)
