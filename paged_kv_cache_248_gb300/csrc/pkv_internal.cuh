@@ -21,7 +21,7 @@ enum : uint32_t {
 
 constexpr int kTileKeys = 128;       // keys per tensor-core tile (8 blocks)
 constexpr int kPrefillTilesPerItem = 2;  // query tiles of one prefill work item (sharing K/V)
-constexpr int kSplitKeys = 1024;     // decode key-split length (a multiple of kTileKeys)
+constexpr int kSplitKeys = 2048;     // decode key-split length (a multiple of kTileKeys)
 constexpr int kNoSplitKeys = 2048;   // decode contexts up to this length are never split
 
 // Key splits of a decode request of context length L: a function of L alone, so

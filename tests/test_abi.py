@@ -122,7 +122,7 @@ def test_step_with_copies_host_checks_fail_without_launching(lib):
 
 
 def test_noalloc_refuses_too_many_split_items_like_paged_attention(lib):
-    # 2^20 requests x 8 kv heads x ceil(2^18 / 1024) splits = 2^31 items: both calls
+    # 2^20 requests x 8 kv heads x ceil(2^19 / 2048) splits = 2^31 items: both calls
     # refuse the batch as unsupported on the host, before any CUDA call
     import paged_kv_cache_248_gb300 as pkv
     P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
@@ -132,7 +132,7 @@ def test_noalloc_refuses_too_many_split_items_like_paged_attention(lib):
     fn.restype = ctypes.c_int
     fake = P(0x1000)
     desc = _desc(pkv, nb=1 << 20, hkv=8, d=128, dt=1)
-    n, max_len = 1 << 20, 1 << 18
+    n, max_len = 1 << 20, 1 << 19
     args = (fake, fake, fake, ctypes.byref(desc), fake, max_len // 16, fake, fake, n, 32, n, 1, max_len,
             ctypes.c_float(0.1), fake)
     assert fn(*args, None, None) == pkv.PKV_ERR_UNSUPPORTED

@@ -309,10 +309,10 @@ def test_repeated_calls_match_oracle_and_each_other(pkv, seed, group, hkv):
 
 
 def test_split_decodes_repeat_bitwise(pkv):
-    # Requests of 2 to 9 key splits next to unsplit ones: the split that finishes last
-    # merges its (request, kv head), and which split that is changes from call to call;
-    # the merge runs in split order all the same, so the rows must be identical.
-    lens = [2049, 3000, 4096, 5121, 9000, 300, 2048, 7777]
+    # Requests of 2 to 9 key splits next to unsplit ones: which split finishes last
+    # changes from call to call; the merge runs in split order all the same, so the
+    # rows must be identical.
+    lens = [2049, 3000, 4096, 5121, 9000, 300, 2048, 7777, 18000]
     w = wl.sized_case(43, lens, [1] * len(lens), 16, 4, 128, "bf16")
     t_cpu = w.make_tensors("cpu")
     t = {k: v.cuda() for k, v in t_cpu.items()}
@@ -326,7 +326,7 @@ def test_split_decodes_repeat_bitwise(pkv):
 
 
 def test_bad_block_in_one_split_zeroes_the_merged_row(pkv):
-    # a bad block id in the third split of a 5121-key request: that request's merged
+    # a bad block id in the second split of a 5121-key request: that request's merged
     # rows are zero, every other request is unaffected
     w = wl.sized_case(44, [5121, 3000, 600], [1, 1, 1], 8, 2, 128, "bf16")
     t_cpu = w.make_tensors("cpu")
