@@ -41,14 +41,14 @@ METRIC = "decode KV-read GB/s (% of HBM peak); mixed-step tokens/sec at 1 GB300"
 
 # DRAM traffic of the decode kernel per algorithmic byte, from one-pass ncu captures of one
 # decode launch of each workload (dram__bytes_read.sum + dram__bytes_write.sum):
-#   mixed step:      19.5008 GB + 36.5 MB for 19.409 GB of algorithmic bytes;
-#   batched decode:  505.08 MB + 3.57 MB for 503.62 MB (decode-only: K/V loaded evict-first).
+#   mixed step:      19.5000 GB + 36.4 MB for 19.409 GB of algorithmic bytes;
+#   batched decode:  505.07 MB + 3.20 MB for 503.62 MB (decode-only: K/V loaded evict-first).
 # A ratio is reported only for the workload it was measured on, and only while the
 # profiled sources are unchanged.
 NCU_TRAFFIC = {
     "sources": ("k_decode.cu", "ptx.cuh", "pkv_internal.cuh"),
-    "sha256": "bd52ee75b47414e2651e720c64f46302a003ebdf162e4cc9d91f3baefcc98b9d",
-    "decode": {"mixed": (19.500793e9 + 36.525056e6) / 19409039536, "decode": (505.0816e6 + 3.57248e6) / 503617604},
+    "sha256": "396f2627c969ab1d0cedb14ea90942fb0cd0198eab2d7ecb813eee4160b87c5a",
+    "decode": {"mixed": (19.499962e9 + 36.431872e6) / 19409039536, "decode": (505.073408e6 + 3.199744e6) / 503617604},
 }
 
 
