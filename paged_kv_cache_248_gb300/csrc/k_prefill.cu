@@ -29,7 +29,8 @@
 //              A operand from there.  MMAs issued by one thread complete in order, so
 //              S_w(j+1) cannot overwrite P_w(j) before P_w(j) V(j) has read it, and S_w(j)
 //              complete means P_w(j-1) V(j-1) is complete too.  While one tile's softmax
-//              runs, the tensor core works on the other tile.
+//              runs, the tensor core works on the other tile.  P_w(j) arrives in two
+//              halves of 64 keys, and each half's P V is issued as soon as it is there.
 //   warps 2-5  softmax of query tile 0, warps 6-9 of tile 1: thread r owns row r.  Per
 //              key tile it reads its S row from TMEM twice -- for the row maximum, then
 //              for the exponents -- so that no whole row is held in registers, applies the
@@ -82,7 +83,8 @@ struct Ctl {
   // K and V tiles have rings of their own: a K tile is released when the S MMAs of
   // both query tiles have read it, a V tile when both P V MMAs have
   uint64_t kfull[kKStages], kempty[kKStages], vfull[kVStages], vempty[kVStages];
-  uint64_t s_full[2], p_full[2], o_full[2], o_free[2];  // per query tile
+  uint64_t s_full[2], o_full[2], o_free[2];  // per query tile
+  uint64_t p_full[2][2];                     // per query tile: P of keys 0-63, then of keys 64-127
   uint64_t q_full[2], q_free[2];
   uint64_t item_full[kRing], item_empty[kRing];
   uint64_t drain;
@@ -193,9 +195,10 @@ __device__ __forceinline__ float row_extremum(uint32_t taddr, int nvis) {
 // 32-column piece is loaded while the previous one is converted, and the 16 P columns
 // a piece gives land on columns this thread has already read.  A masked key's scaled
 // score is set to -inf before its exponent (an infinite raw score would give NaN at
-// scale 0).
-template <bool kMask>
-__device__ __forceinline__ float row_exp_to_p(uint32_t taddr, int nvis, float scale, float m_ref) {
+// scale 0).  Once the P of keys 0-63 is stored, half() runs (the hand-over of that
+// half) while the third piece's load is in flight.
+template <bool kMask, typename Half>
+__device__ __forceinline__ float row_exp_to_p(uint32_t taddr, int nvis, float scale, float m_ref, Half&& half) {
   float ls[4] = {0.f, 0.f, 0.f, 0.f};  // the row sum in four independent parts (two packed pairs)
   uint32_t a[32], b[32];
   tmem_ld32_issue(taddr, a);
@@ -219,6 +222,7 @@ __device__ __forceinline__ float row_exp_to_p(uint32_t taddr, int nvis, float sc
       pw[q] = *reinterpret_cast<uint32_t*>(&h2);
     }
     tmem_st16(taddr + 16 * h, pw);
+    if (h == 1) half();
     if (h < 3) tmem_ld32_wait(nxt);
   }
   return (ls[0] + ls[1]) + (ls[2] + ls[3]);
@@ -505,13 +509,16 @@ __device__ void mma_warp(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uint8_t*
     uint32_t it = 0, tk = 0, tv = 0;
     uint32_t qc0 = 0, qc1 = 0, pc0 = 0, pc1 = 0, ic0 = 0, ic1 = 0;  // per tile slot: Q tiles, P tiles, items
     bool issued = false, ok = true;
-    // O_w += P_w V (acc false: O_w = P_w V), V in ring slot sv; P_w is bf16 over S_w's first 64 columns
-    auto issue_pv = [&](int w, int sv, bool acc) {
+    // O_w += P_w V over keys 64 hf .. 64 hf + 63 (acc false: the item's first, O_w = P_w V),
+    // V in ring slot sv; P_w is bf16 over S_w's first 64 columns
+    auto issue_pv = [&](int w, int sv, bool acc, int hf) {
       const uint64_t bd = umma_smem_desc(smem_u32(vbuf + sv * kTileBytes), kHalfBytes, 1024, kLayout128B);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
+      for (int k4 = 0; k4 < 4; ++k4) {
+        const int kk = 4 * hf + k4;
         umma_f16_ts(tmem + kOCol + 128 * w, tmem + 128 * w + 8 * kk, umma_desc_advance(bd, kk * 2048), idesc_o,
                     (acc || kk > 0) ? 1u : 0u);
+      }
     };
     // S_w = Q_w K^T, K in ring slot sk
     auto issue_s = [&](int w, int sk) {
@@ -535,13 +542,14 @@ __device__ void mma_warp(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uint8_t*
         const int nt0 = info.nt[0], nt1 = info.nt[1];
         ok = (nt0 == 0 || mbar_wait(&c.q_full[0], qc0 & 1, abort_flag)) &&
              (nt1 == 0 || mbar_wait(&c.q_full[1], qc1 & 1, abort_flag));
-        // Step j: P_0(j-1) V(j-1), S_0(j), P_1(j-1) V(j-1), S_1(j).  An MMA issue returns
-        // only as the tensor core takes it in, so the MMAs are issued back to back: the
-        // only wait between the last MMA of one step and the first of the next is for
-        // P_0, and the K wait sits right after an MMA burst, where the tensor core still
-        // has queued work.  V needs no wait: tile 0's softmax warps hand P_0(j) over only
-        // after they have seen V(j) land and zeroed its rows past the context, and
-        // P_1(j) V(j) is issued after P_0(j) V(j).  The K and V ring slots are released
+        // Step j: P_0(j-1) V(j-1), S_0(j), P_1(j-1) V(j-1), S_1(j), each P V in two halves
+        // of 64 keys issued as the softmax hands them over.  An MMA issue returns only as
+        // the tensor core takes it in, so the MMAs are issued back to back: the waits
+        // between bursts are for the halves of P, and the K wait sits right after an MMA
+        // burst, where the tensor core still has queued work.  V needs no wait: tile 0's
+        // softmax warps hand the first half of P_0(j) over only after they have seen V(j)
+        // land and zeroed its rows past the context, and P_1(j) V(j) is issued after
+        // P_0(j) V(j).  The K and V ring slots are released
         // by the softmax warps, which learn from their own S and O barriers when the MMAs
         // reading a slot are done; a commit here would hold this thread for a queue slot
         // each time.  The item's first P V restarts O_w, once the previous item's O_w was
@@ -549,14 +557,20 @@ __device__ void mma_warp(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uint8_t*
         for (int j = 0; j <= nt0 && ok; ++j) {
           const int sk = tk % kKStages, sv = tv % kVStages;  // K(j), V(j-1)
           if (j > 0) {
-            if (!mbar_wait(&c.p_full[0], pc0 & 1, abort_flag) ||
+            if (!mbar_wait(&c.p_full[0][0], pc0 & 1, abort_flag) ||
                 (j == 1 && !mbar_wait(&c.o_free[0], (ic0 & 1) ^ 1, abort_flag))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_pv(0, sv, j > 1, 0);
+            if (!mbar_wait(&c.p_full[0][1], pc0 & 1, abort_flag)) {
               ok = false;
               break;
             }
             ++pc0;
             tc_fence_after();
-            issue_pv(0, sv, j > 1);
+            issue_pv(0, sv, j > 1, 1);
             if (j == nt0) umma_commit(&c.o_full[0]);
           }
           if (j < nt0) {
@@ -571,14 +585,20 @@ __device__ void mma_warp(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uint8_t*
             issued = true;
           }
           if (j > 0 && j - 1 < nt1) {
-            if (!mbar_wait(&c.p_full[1], pc1 & 1, abort_flag) ||
+            if (!mbar_wait(&c.p_full[1][0], pc1 & 1, abort_flag) ||
                 (j == 1 && !mbar_wait(&c.o_free[1], (ic1 & 1) ^ 1, abort_flag))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_pv(1, sv, j > 1, 0);
+            if (!mbar_wait(&c.p_full[1][1], pc1 & 1, abort_flag)) {
               ok = false;
               break;
             }
             ++pc1;
             tc_fence_after();
-            issue_pv(1, sv, j > 1);
+            issue_pv(1, sv, j > 1, 1);
             if (j == nt1) umma_commit(&c.o_full[1]);
           }
           if (j < nt1) {
@@ -771,29 +791,42 @@ __device__ void softmax_warps(const PrefillParams& P, Ctl& c, uint8_t* qbuf, uin
           m_ref = m_new;
         }
       }
-      // second read of S: the exponents, written as bf16 P over S's first 64 columns
-      l_sum += whole ? row_exp_to_p<false>(srow, nvis, scale, m_ref) : row_exp_to_p<true>(srow, nvis, scale, m_ref);
-      tmem_st_wait();
-      // V of this key tile has landed (also orders the producer's bad-block flag)
-      if (!mbar_wait(&c.vfull[sv], (vt / kVStages) & 1, abort_flag)) {
+      // second read of S: the exponents, written as bf16 P over S's first 64 columns.
+      // P goes to the MMA warp in two halves (keys 0-63, then 64-127), so that the first
+      // half's P V runs while the second half is computed.  Before the first hand-over,
+      // V of this key tile has landed (which also orders the producer's bad-block flag)
+      // and tile 0's warps have zeroed its rows past the context.
+      bool v_ok = true;
+      auto first_half = [&]() {
+        tmem_st_wait();
+        v_ok = mbar_wait(&c.vfull[sv], (vt / kVStages) & 1, abort_flag);
+        if (!v_ok) return;
+        if (w == 0 && k0 + r >= zero_from) {
+          // rows are 128 bytes apart, so every lane's k-th chunk would sit in the same
+          // four banks; starting each lane at chunk r mod 8 spreads eight lanes over all 32
+          uint8_t* vrow = vbuf + sv * kTileBytes + r * 128;
+#pragma unroll
+          for (int c16 = 0; c16 < 8; ++c16) {
+            const int off = ((c16 + r) & 7) * 16;
+            *reinterpret_cast<uint4*>(vrow + off) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(vrow + kHalfBytes + off) = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&c.p_full[w][0]);
+      };
+      l_sum += whole ? row_exp_to_p<false>(srow, nvis, scale, m_ref, first_half)
+                     : row_exp_to_p<true>(srow, nvis, scale, m_ref, first_half);
+      if (!v_ok) {
         ok = false;
         break;
       }
-      if (w == 0 && k0 + r >= zero_from) {
-        // rows are 128 bytes apart, so every lane's k-th chunk would sit in the same four
-        // banks; starting each lane at chunk r mod 8 spreads eight lanes over all 32
-        uint8_t* vrow = vbuf + sv * kTileBytes + r * 128;
-#pragma unroll
-        for (int c16 = 0; c16 < 8; ++c16) {
-          const int off = ((c16 + r) & 7) * 16;
-          *reinterpret_cast<uint4*>(vrow + off) = make_uint4(0, 0, 0, 0);
-          *reinterpret_cast<uint4*>(vrow + kHalfBytes + off) = make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
-      }
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&c.p_full[w]);
+      if (lane == 0) mbar_arrive(&c.p_full[w][1]);
       ++tc;
     }
     if (!ok) break;
@@ -914,7 +947,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     }
     for (int w = 0; w < 2; ++w) {
       mbar_init(&c.s_full[w], 1);
-      mbar_init(&c.p_full[w], 4);
+      mbar_init(&c.p_full[w][0], 4);
+      mbar_init(&c.p_full[w][1], 4);
       mbar_init(&c.o_full[w], 1);
       mbar_init(&c.o_free[w], 4);
       mbar_init(&c.q_full[w], kCas ? 4 : 1);  // cascade: the tile's four softmax warps gather Q
