@@ -206,7 +206,11 @@ PKV_API int paged_attention_cascade(const void* q, const void* k_cache, const vo
  * its blocks and attends over them).  On the bf16 path the mapping and the scatter
  * run in extra CTAs of the planning launch, so the step has two launches fewer and
  * no slot array round trip; the kernel boundary orders the writes before every
- * attention read.  Copy-on-write copies (pkv_copy_blocks) go before this call.
+ * attention read.  On an fp32 cache with max_query_len == 1 (every request brings
+ * one token) the attention launch itself stores each token's rows before it reads
+ * them, one launch in all; a request with more query tokens than that bound is then
+ * flagged (PKV_ERR_INDEX), its rows zeroed and its tokens not written.
+ * Copy-on-write copies (pkv_copy_blocks) go before this call.
  * k_new, v_new    device [num_tokens][num_kv_heads][head_dim], cache dtype, required
  * k_cache, v_cache  written at the new tokens' slots, then read
  * groups          NULL for none (see paged_attention_cascade)

@@ -10,6 +10,7 @@
 #include <vector>
 
 #include "pkv_internal.cuh"
+#include "k_generic.cuh"
 
 namespace pkv {
 
@@ -381,6 +382,10 @@ int attention_impl(const void* q, const void* k_new, const void* v_new, const vo
     if (st) return st;
   }
   if (cache->dtype == PKV_F32) {  // groups do not change results
+    if (write && max_query_len == 1) {  // one new token a request: written by the attention launch itself
+      const GenericWrite gw{k_new, v_new, slots_out};
+      return launch_generic_attention_write(a, gw, ctx->err, s);
+    }
     if (write) {  // slot mapping and scatter in the writer CTAs of a launch that plans nothing
       PlanArgs w{seq_lens, query_start_loc, num_seqs, num_tokens, cache->num_kv_heads, max_blocks_per_seq,
                  max_seq_len, kSplitKeys, 0, nullptr, nullptr, nullptr, nullptr, nullptr, ctx->err};

@@ -294,3 +294,77 @@ def test_step_with_copies_replays_from_a_cuda_graph(pkv):
     assert pkv.pkv_get_last_error() == 0
     assert torch.equal(out_g, out_e)
     assert torch.equal(t["k_cache"], k_after) and torch.equal(t["v_cache"], v_after)
+
+
+@pytest.mark.parametrize("seed,group,hkv,d", [(41, 2, 2, 64), (42, 12, 1, 64), (43, 4, 2, 128)])
+def test_fp32_one_token_step_writes_in_the_attention_launch(pkv, seed, group, hkv, d):
+    """An fp32 step whose requests each bring one token stores the rows in the attention
+    launch itself (each CTA its own token's rows; a group of 12 gives two head chunks
+    that both write them): bit-equal to the separate calls, and the oracle's slots,
+    caches and outputs."""
+    w = wl.random_case(seed, num_seqs=12, max_ctx=700, group=group, num_kv_heads=hkv, head_dim=d, dtype="f32",
+                       decode_frac=1.0)
+    assert w.max_query_len == 1
+    t_cpu = w.make_tensors("cpu")
+    t = {k: v.cuda() for k, v in t_cpu.items()}
+    sep, fus = both_ways(pkv, w, t)
+    assert sep[4] == 0
+    assert_same(sep, fus)
+    ref, ref_slots, ref_k, ref_v = oracle_step(w, t_cpu)
+    assert np.array_equal(fus[1].cpu().numpy(), ref_slots)
+    compare(fus[0], ref, "f32", w.name)
+    for got, want, name in ((fus[2], ref_k, "k_cache"), (fus[3], ref_v, "v_cache")):
+        assert np.array_equal(bits(got), want), name
+
+
+def test_fp32_one_token_step_with_copies(pkv):
+    w = wl.random_case(44, num_seqs=10, max_ctx=600, group=4, num_kv_heads=2, head_dim=64, dtype="f32",
+                       decode_frac=1.0, pool_slack=9)
+    used = np.unique(w.block_tables[w.block_tables >= 0])
+    free = np.setdiff1d(np.arange(w.num_blocks), used)
+    src, dst = used[:4].astype(np.int32), free[:4].astype(np.int32)
+    w.cow_src, w.cow_dst = src, dst
+    t_cpu = w.make_tensors("cpu")
+    t = {k: v.cuda() for k, v in t_cpu.items()}
+    sep, fus = both_ways_cow(pkv, w, t, src, dst)
+    assert sep[4] == 0
+    assert_same(sep, fus)
+    ref, _, ref_k, ref_v = oracle_step(w, t_cpu, cow=True)
+    compare(fus[0], ref, "f32", w.name)
+    for got, want, name in ((fus[2], ref_k, "k_cache"), (fus[3], ref_v, "v_cache")):
+        assert np.array_equal(bits(got), want), name
+
+
+def test_fp32_one_token_step_errors_match_the_separate_calls(pkv):
+    # a new token whose block id is past the pool: the slot is reported, the write
+    # skipped and flagged, and attention zeroes the request's row -- as the separate calls
+    w = wl.random_case(45, num_seqs=6, max_ctx=300, group=2, num_kv_heads=2, head_dim=64, dtype="f32",
+                       decode_frac=1.0)
+    i = 3
+    w.block_tables[i, (int(w.seq_lens[i]) - 1) // 16] = w.num_blocks + 3
+    t = {k: v.cuda() for k, v in w.make_tensors("cpu").items()}
+    sep, fus = both_ways(pkv, w, t)
+    assert sep[4] == pkv.PKV_ERR_INDEX
+    assert_same(sep, fus)
+
+
+def test_fp32_step_flags_a_request_past_the_one_token_bound(pkv):
+    # max_query_len 1 with a two-token request: that request is flagged, its rows are
+    # zeroed and its tokens not written; the other requests are attended as usual
+    w = wl.sized_case(46, seq_lens=[20, 33, 7], q_lens=[1, 2, 1], num_q_heads=2, num_kv_heads=1, head_dim=64,
+                      dtype="f32")
+    t_cpu = w.make_tensors("cpu")
+    t = {k: v.cuda() for k, v in t_cpu.items()}
+    bt, sl, qsl = dev(w.block_tables), dev(w.seq_lens), dev(w.query_start_loc)
+    kc, vc = t["k_cache"].clone(), t["v_cache"].clone()
+    out = pkv.paged_attention_step(t["q"], t["k_new"], t["v_new"], kc, vc, bt, sl, qsl, w.scale, 1, w.max_seq_len)
+    assert pkv.pkv_get_last_error() == pkv.PKV_ERR_INDEX
+    ref, ref_slots, _, _ = oracle_step(w, t_cpu)
+    got = out.cpu().numpy()
+    assert not got[1:3].any()
+    compare(out[[0, 3]], ref[[0, 3]], "f32", w.name)
+    kb, vb = bits(kc), bits(vc)
+    k0, v0 = bits(t_cpu["k_cache"]), bits(t_cpu["v_cache"])
+    for tok in (1, 2):  # the two-token request's slots keep what they held
+        b, off = divmod(int(ref_slots[tok]), 16)
+        assert np.array_equal(kb[b, :, off], k0[b, :, off]) and np.array_equal(vb[b, :, off], v0[b, :, off])
