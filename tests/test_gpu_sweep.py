@@ -11,6 +11,10 @@ The shared-prefix sweep draws the prefix groups too (their count, prefix lengths
 do and do not end on a 512-key split, member counts on both sides of the paired-tile
 choice, suffix lengths from one key to several decode splits, malformed hints or
 none) and checks ``paged_attention_cascade`` against the oracle's plain attention.
+
+The one-token fp32 sweep draws batches whose requests each bring one token (head_dim 64
+or 128, groups that do and do not split into two head chunks, contexts from one key up)
+and runs ``paged_attention_step``, where the attention launch stores the new rows itself.
 """
 import numpy as np
 import pytest
@@ -108,3 +112,43 @@ def test_shared_prefix_sweep(pkv, seed):
     ref = oracle.attention(bits(t_cpu["q"]), bits(t_cpu["k_cache"]), bits(t_cpu["v_cache"]), w.block_tables,
                            w.seq_lens, w.query_start_loc, w.scale)
     compare(cas, ref, "bf16", f"{w.name} {w.num_q_heads}/{w.num_kv_heads} prefixes {hints['prefix_num_blocks']}")
+
+
+def draw_one_token_f32(seed: int):
+    rng = np.random.default_rng(30_000 + seed)
+    d = int(rng.choice([64, 128]))
+    group = int(rng.choice([1, 2, 3, 4, 6, 8, 12, 16]))  # above 8: two head chunks per (token, kv head)
+    hkv = int(rng.choice([1, 2, 4, 8]))
+    while group * hkv > 64:
+        hkv //= 2
+    num_seqs = int(rng.integers(1, 40, endpoint=True))
+    max_ctx = int(rng.choice([1, 20, 300, 1500, 4000]))
+    while True:
+        w = wl.random_case(seed, num_seqs, max_ctx, 1, group, hkv, d, "f32", decode_frac=1.0)
+        work = float(np.sum(w.seq_lens.astype(np.float64))) * group * hkv * d * 4
+        if work <= ORACLE_BUDGET or num_seqs == 1:
+            return w
+        num_seqs -= 1
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_fp32_one_token_step_sweep(pkv, seed):
+    """paged_attention_step on fp32 batches of one-token requests, where the attention
+    launch itself stores the new rows: slots and pools bit-exact, outputs within 1e-4."""
+    w = draw_one_token_f32(seed)
+    assert w.max_query_len == 1
+    t_cpu = w.make_tensors("cpu")
+    t = {k: v.cuda() for k, v in t_cpu.items()}
+    m = {k: torch.from_numpy(np.ascontiguousarray(getattr(w, k))).cuda()
+         for k in ("block_tables", "seq_lens", "query_start_loc")}
+    slots = torch.full((w.num_tokens,), -7, dtype=torch.int64, device="cuda")
+    out = pkv.paged_attention_step(t["q"], t["k_new"], t["v_new"], t["k_cache"], t["v_cache"], m["block_tables"],
+                                   m["seq_lens"], m["query_start_loc"], w.scale, 1, max(1, w.max_seq_len),
+                                   slot_mapping=slots)
+    st = pkv.pkv_get_last_error()
+    assert st == 0, pkv.status_string(st)
+    ref, ref_slots, kc, vc = oracle_step(w, t_cpu)
+    assert np.array_equal(slots.cpu().numpy(), ref_slots)
+    assert np.array_equal(bits(t["k_cache"]).view(np.uint8), kc.view(np.uint8))
+    assert np.array_equal(bits(t["v_cache"]).view(np.uint8), vc.view(np.uint8))
+    compare(out, ref, "f32", f"{w.name} d{w.head_dim} {w.num_q_heads}/{w.num_kv_heads}")
